@@ -1,0 +1,469 @@
+"""Benchmark of the fused MoE router on GB300.
+
+Headline workload (one "step"): the decode router at M=8 verify rows,
+H=2048, E=256, top-8 softmax, run for 40 MoE layers back to back, each
+layer with its own W_gate, captured once as a CUDA graph and replayed. The
+W_gate pool rotates over 520 MiB (> the 129 MB L2), so every call streams
+its weights from HBM. Value = router tokens/s = rows routed per second
+summed over the layer calls (M x 40 per step).
+
+Also reported (``detail``): per-call latency and roofline fraction at each
+configuration of the router pages (decode M=1/2/8, sqrt-softplus+bias
+M=1/16/64, the M=16384 prefill with BF16 and NVFP4 weights, and the M=2
+router with its unique-route table), the fused-versus-unfused A/B, and the
+CPU oracle's throughput.
+
+``--impl reference`` times the CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LAYERS = 40          # router calls per decode token (one per MoE layer)
+W_POOL_BYTES = 520 << 20
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.p is not None:
+            time.sleep(0.25)
+            self.p.terminate()
+            try:
+                out, _ = self.p.communicate(timeout=5)
+                self.lines = [l for l in out.splitlines() if l.strip()]
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- GPU helpers
+def dev(a):
+    import torch
+    a = np.ascontiguousarray(a)
+    return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+
+def time_graph(graph_fn, reps, warm=3):
+    """Average ms of graph_fn() over reps, CUDA events on the current stream."""
+    import torch
+    for _ in range(warm):
+        graph_fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        graph_fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / reps
+
+
+class RouterSet:
+    """A pool of distinct (x, W) inputs for one configuration, with graphs
+    of ``calls`` back-to-back router calls over consecutive pool slots."""
+
+    def __init__(self, cfg, M, calls, w_dtype=None, pool_bytes=W_POOL_BYTES, table=False,
+                 flags=0, seed=0):
+        import torch
+
+        from moe_expert_router_02_gb300 import router as R
+        from moe_expert_router_02_gb300 import synth
+        self.R, self.cfg, self.M, self.calls, self.table = R, cfg, M, calls, table
+        self.H, self.E, self.k, self.act = cfg["H"], cfg["E"], cfg["k"], cfg["act"]
+        case = synth.make_case(cfg, M=M, seed=seed, w_dtype=w_dtype)
+        self.case = case
+        wb = case["W"].nbytes + (0 if case["scales"] is None else case["scales"].nbytes)
+        self.w_bytes = wb
+        n_w = max(calls, int(np.ceil(pool_bytes / wb)))
+        n_w = int(np.ceil(n_w / calls) * calls)
+        self.n_graphs = n_w // calls
+        W0 = dev(case["W"])
+        self.W = W0.unsqueeze(0).repeat(n_w, *([1] * W0.dim()))  # distinct buffers, same values
+        self.scales = None if case["scales"] is None else dev(case["scales"])
+        self.x = dev(case["x"]).unsqueeze(0).repeat(calls, *([1] * 2)).contiguous()
+        self.bias = None if case["bias"] is None else dev(case["bias"])
+        self.idx = torch.empty((calls, M, self.k), dtype=torch.int32, device="cuda")
+        self.w = torch.empty((calls, M, self.k), dtype=torch.float32, device="cuda")
+        self.tbl = None
+        if table:
+            n = 2 * self.k
+            G = M // 2
+            self.tbl = (torch.empty((calls, G, n), dtype=torch.int32, device="cuda"),
+                        torch.empty((calls, G, n), dtype=torch.uint8, device="cuda"),
+                        torch.empty((calls, G, 2, self.k), dtype=torch.uint8, device="cuda"),
+                        torch.empty((calls, G), dtype=torch.int32, device="cuda"))
+        self.flags = flags
+        self.stream = torch.cuda.Stream()
+        self.graphs = []
+
+    def opts(self, c):
+        tbl = None if self.tbl is None else tuple(t[c] for t in self.tbl)
+        return self.R.make_opts(x_dtype=self.case["x_dtype"], w_dtype=self.case["w_dtype"],
+                                w_scales=self.scales, w_global_scale=self.case["g"], table=tbl,
+                                flags=self.flags)
+
+    def call(self, c, wslot, stream):
+        self.R.router_forward_ex(self.x[c], self.W[wslot], self.bias, self.M, self.H, self.E,
+                                 self.k, self.act, self.idx[c], self.w[c], self.opts(c),
+                                 stream=stream)
+
+    def capture(self):
+        import torch
+        s = self.stream
+        with torch.cuda.stream(s):
+            for c in range(self.calls):  # sizes the library workspace outside capture
+                self.call(c, c, s)
+        s.synchronize()
+        for gi in range(self.n_graphs):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for c in range(self.calls):
+                    self.call(c, gi * self.calls + c, s)
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+        self.step_i = 0
+
+    def step(self):
+        self.graphs[self.step_i % self.n_graphs].replay()
+        self.step_i += 1
+
+    def algo_bytes(self):
+        M, H, E, k = self.M, self.H, self.E, self.k
+        xb = M * H * (4 if self.case["x_dtype"] == 0 else 2)
+        out = M * k * 8 + (0 if self.case["bias"] is None else E * 4)
+        tbl = 0 if not self.table else (M // 2) * (2 * k * 4 + 2 * k + 2 * k + 4)
+        return self.w_bytes + xb + out + tbl
+
+
+def per_call_stats(rs, steps):
+    """(us per call in graph replay, us isolated single call)."""
+    import torch
+    ms = time_graph(rs.step, steps)
+    us_pipe = ms * 1e3 / rs.calls
+    # isolated: one call, stream synchronised around it, W rotating
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tot = 0.0
+    n = 30
+    with torch.cuda.stream(rs.stream):
+        for i in range(n + 3):
+            torch.cuda.synchronize()
+            s.record(rs.stream)
+            rs.call(0, (7 * i) % rs.W.shape[0], rs.stream)
+            e.record(rs.stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                tot += s.elapsed_time(e)
+    return us_pipe, tot * 1e3 / n
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_tokens_per_s(cfg, M, budget_s=10.0, min_calls=1, w_dtype=None, rows=None):
+    """Oracle router throughput on host cores (single thread)."""
+    import oracle
+    from moe_expert_router_02_gb300 import synth
+    case = synth.make_case(cfg, M=M, seed=0, w_dtype=w_dtype)
+    if rows is not None:  # bounded sample of a large batch
+        case = dict(case, M=rows, x=case["x"][:rows])
+    t0 = time.perf_counter()
+    calls = 0
+    while calls < min_calls or time.perf_counter() - t0 < budget_s:
+        oracle.router(case)
+        calls += 1
+    dt = time.perf_counter() - t0
+    return case["M"] * calls / dt, calls, dt
+
+
+# ---------------------------------------------------------------- main arms
+def run_ours(args, rank, world, local):
+    import torch
+
+    from moe_expert_router_02_gb300 import router as R
+    from moe_expert_router_02_gb300 import synth
+    torch.cuda.set_device(local)
+    peaks = load_peaks()
+    C = synth.CONFIGS
+    M = 8
+    head = RouterSet(C["C1"], M, LAYERS)
+    head.capture()
+    for _ in range(args.warmup):
+        head.step()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev_s, ev_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        torch.cuda.synchronize()
+        ev_s.record()
+        for _ in range(args.steps):
+            head.step()
+        ev_e.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = ev_s.elapsed_time(ev_e)
+    ms = max_over_ranks(ms, world)
+    tokens = M * LAYERS * args.steps * world
+    value = tokens / (ms / 1e3)
+    us_call = ms * 1e3 / (args.steps * LAYERS)
+    algo = head.algo_bytes()
+    achieved = algo / (us_call * 1e-6) / 1e9
+
+    # end to end through the public API with host buffers
+    x_host = torch.empty((LAYERS, M, head.H), dtype=torch.int16).pin_memory()
+    x_host.copy_(head.x.cpu())
+    idx_host = torch.empty((LAYERS, M, head.k), dtype=torch.int32).pin_memory()
+    w_host = torch.empty((LAYERS, M, head.k), dtype=torch.float32).pin_memory()
+    s = head.stream
+
+    def e2e_step(i):
+        head.x.copy_(x_host, non_blocking=True)
+        for c in range(LAYERS):
+            R.router_forward(head.x[c], head.W[(i * LAYERS + c) % head.W.shape[0]], None, M,
+                             head.H, head.E, head.k, head.act, head.idx[c], head.w[c], stream=s)
+        idx_host.copy_(head.idx, non_blocking=True)
+        w_host.copy_(head.w, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e2e_s = time.perf_counter() - t0
+    e2e_value = max_over_ranks(e2e_s, world)
+    e2e_value = tokens / e2e_value
+
+    detail = {}
+    if not args.quick and rank == 0:
+        detail = run_detail(args, peaks)
+
+    cpu = None
+    if rank == 0 and world == 1:
+        tps, calls, dt = oracle_tokens_per_s(C["C1"], M, budget_s=args.cpu_budget)
+        cpu = {"value": tps, "unit": "router tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{calls} oracle router calls at M=8, H=2048, E=256, k=8 "
+                         f"({dt:.1f} s, single thread)"}
+
+    line = {
+        "metric": "router tokens/s (decode M=8, H=2048, E=256, top-8 softmax, 40 layers)",
+        "value": value, "unit": "router tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode router: M=8 rows, H=2048, E=256, k=8, softmax, "
+                               "BF16 x (RMS-normalised rows) and W_gate ~ N(0,0.02), "
+                               "40 layer calls per step (one CUDA graph)",
+                   "l2": "W_gate pool of 520 MiB rotated (> 129 MB L2)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": us_call,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm"], "traffic": None,
+                     "algo_bytes_per_call": algo, "peak_source": peaks["source"]},
+        "e2e": {"value": e2e_value, "unit": "router tokens/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 2),
+                "d2h_bytes_per_step": int(idx_host.numel() * 4 + w_host.numel() * 4)},
+        "gpu_launches": args.steps * LAYERS,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+        "detail": detail,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def run_detail(args, peaks):
+    """Per-configuration latency and roofline figures."""
+    import torch
+
+    from moe_expert_router_02_gb300 import router as R
+    from moe_expert_router_02_gb300 import synth
+    C = synth.CONFIGS
+    out = {}
+
+    def record(name, rs, steps=20, flops=None):
+        rs.capture()
+        us_pipe, us_iso = per_call_stats(rs, steps)
+        algo = rs.algo_bytes()
+        ent = {"M": rs.M, "us_per_call_pipelined": us_pipe, "us_per_call_isolated": us_iso,
+               "tokens_per_s": rs.M / (us_pipe * 1e-6),
+               "hbm_frac_pipelined": algo / (us_pipe * 1e-6) / 1e9 / peaks["hbm"],
+               "hbm_frac_isolated": algo / (us_iso * 1e-6) / 1e9 / peaks["hbm"],
+               "algo_bytes": algo,
+               "regime": R.router_regime(rs.M, rs.H, rs.E, rs.k, rs.opts(0))}
+        if flops:
+            ent["tflops"] = flops / (us_pipe * 1e-6) / 1e12
+            ent["bf16_frac"] = ent["tflops"] / peaks["bf16"]
+        out[name] = ent
+        del rs
+        torch.cuda.empty_cache()
+
+    for M in (1, 2, 8):
+        record(f"C1_softmax_M{M}", RouterSet(C["C1"], M, LAYERS))
+    record("C1_softmax_M8_unfused", RouterSet(C["C1"], 8, LAYERS, flags=R.GBR_FLAG_UNFUSED))
+    for M in (1, 16, 64):
+        record(f"C2_sqrtsoftplus_bias_M{M}", RouterSet(C["C2"], M, LAYERS))
+    record("C4_M2_router_table", RouterSet(C["C4"], 2, LAYERS, table=True))
+    record("C4_M2_router_no_table", RouterSet(C["C4"], 2, LAYERS))
+    if "C4_M2_router_table" in out:
+        out["C4_table_overhead_us"] = (out["C4_M2_router_table"]["us_per_call_pipelined"] -
+                                       out["C4_M2_router_no_table"]["us_per_call_pipelined"])
+    # unique-route table alone over 1e5 groups
+    G, k = C["C4"]["table_groups"], C["C4"]["k"]
+    idx = dev(synth.table_pairs(G, k, 256, seed=0))
+    tb = (torch.empty((G, 2 * k), dtype=torch.int32, device="cuda"),
+          torch.empty((G, 2 * k), dtype=torch.uint8, device="cuda"),
+          torch.empty((G, 2, k), dtype=torch.uint8, device="cuda"),
+          torch.empty((G,), dtype=torch.int32, device="cuda"))
+    ms = time_graph(lambda: R.route_table(idx, G, 2, k, *tb), 20)
+    tbytes = G * (2 * k * 4 + 2 * k * 4 + 2 * k + 2 * k + 4)
+    out["C4_table_only_1e5"] = {"us": ms * 1e3, "hbm_frac": tbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
+                                "algo_bytes": tbytes}
+    # prefill
+    cfg3 = C["C3"]
+    flops = 2 * cfg3["M"] * cfg3["H"] * cfg3["E"]
+    for name, wd in (("C3_prefill_bf16", synth.BF16), ("C3_prefill_nvfp4", synth.NVFP4)):
+        rs = RouterSet(cfg3, cfg3["M"], 1, w_dtype=wd, pool_bytes=0)
+        record(name, rs, steps=10, flops=flops)
+    return out
+
+
+def run_reference(args, rank, world):
+    """CPU oracle on the headline workload (rank 0 only)."""
+    if rank != 0:
+        return
+    from moe_expert_router_02_gb300 import synth
+    import oracle
+    cfg = synth.CONFIGS["C1"]
+    M = 8
+    case = synth.make_case(cfg, M=M, seed=0)
+    for _ in range(args.warmup):
+        oracle.router(case)
+    t0 = time.perf_counter()
+    per_step = max(1, args.ref_calls)
+    for _ in range(args.steps):
+        for _ in range(per_step):
+            oracle.router(case)
+    dt = time.perf_counter() - t0
+    value = M * per_step * args.steps / dt
+    line = {
+        "impl": "reference",
+        "metric": "router tokens/s (decode M=8, H=2048, E=256, top-8 softmax, 40 layers)",
+        "value": value, "unit": "router tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode router: M=8 rows, H=2048, E=256, k=8, softmax; "
+                               f"each step = {per_step} oracle router calls (sample of the 40 "
+                               "layer calls)"},
+        "cpu_baseline": {"value": value, "unit": "router tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} calls per step x {args.steps} steps, single thread"},
+        "e2e": {"value": value, "unit": "router tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline only, no per-config detail")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-calls", type=int, default=8)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

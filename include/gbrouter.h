@@ -1,0 +1,182 @@
+/*
+ * gbrouter — fused MoE router for one NVIDIA GB300 (sm_103a). C ABI.
+ *
+ * One call computes, for M token rows x[m, :]:
+ *   1. the gate projection  logits[m, e] = sum_h x[m, h] * W_gate[e, h]
+ *      with FP32 accumulation, kept on chip
+ *      (qwisp issue #145, "Observation" and "Change": postNorm[H] ->
+ *      gateLogits[E], "one kernel producing inds/scores directly from
+ *      postNorm", logits held on chip instead of round-tripping);
+ *   2. the score: softmax over E, or a = sqrt(softplus(logit)) with the
+ *      stable softplus max(z,0) + log1p(exp(-|z|)) and a per-expert bias
+ *      added for selection only
+ *      (dense_router_decode commit page, "DenseRouterDecodeKernel: BF16 GEMM
+ *      + sqrt(softplus) + bias + top-k", "Numerically stable softplus", heap
+ *      of "(score, index, unbiased act)");
+ *   3. top-k under the fixed comparison: higher key first, an equal key goes
+ *      to the lower expert index; slots are returned in that order
+ *      (qwisp issue #145, "Bit-exactness": the tie-break order is part of
+ *      the contract);
+ *   4. renormalisation of the chosen weights, w_j = s_j / sum_{i<k} s_i,
+ *      where s is the softmax probability or the unbiased activation
+ *      (commit page, "top-k + renorm");
+ *   5. optionally the M=2 unique-route table: encounter-ordered unique
+ *      experts, per-unique-expert token masks, slot-to-unique map and count
+ *      (b70 lab note "MTP1 M=2 gather/shared-add gate", section
+ *      "Unique-route router screen").
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a caller-owned DEVICE pointer; the library never
+ *     frees or retains it. Arrays are dense row-major.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream). The
+ *     return value reports argument errors and launch errors only.
+ *   - Argument errors return before any CUDA call: nothing is launched and
+ *     nothing is written.
+ *   - M == 0 (or groups == 0) returns GBR_OK without a launch.
+ *   - Inputs must be finite. -0.0 and +0.0 compare equal (lower index wins).
+ *   - If every chosen score of a row is zero, its weights are 1/k.
+ *   - W_gate, bias and NVFP4 scales may be read before the kernel waits on
+ *     the preceding kernel of the stream (programmatic dependent launch).
+ *     If the immediately preceding kernel writes them, set GBR_FLAG_NO_PDL.
+ */
+#ifndef GBROUTER_H_
+#define GBROUTER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* cudaStream_t;
+
+/* status codes */
+enum {
+  GBR_OK = 0,
+  GBR_EINVAL = 1,       /* bad argument: null pointer, k < 1, k > E, bad enum, ... */
+  GBR_EUNSUPPORTED = 2, /* valid but outside this build: E > 512, k > 16 */
+  GBR_ECUDA = 3,        /* a CUDA runtime call or launch failed */
+  GBR_EWORKSPACE = 4,   /* caller workspace smaller than router_workspace_size() */
+  GBR_ETIMEOUT = 5      /* a bounded device-side wait expired (see router_device_status) */
+};
+
+/* score activation */
+enum { GBR_ACT_SOFTMAX = 0, GBR_ACT_SQRT_SOFTPLUS = 1 };
+
+/* element types. NVFP4 is for W_gate only: packed E2M1 codes [E, H/2]
+ * (element 2j in the low nibble of byte j, 2j+1 in the high nibble), one
+ * E4M3 scale per 16 elements along H in w_scales [E, H/16], and an FP32
+ * global scale: W[e,h] = e2m1 * e4m3 * w_global_scale
+ * (dense_router_decode commit page, "NVFP4 blockscaled GEMM"). */
+enum { GBR_F32 = 0, GBR_BF16 = 1, GBR_NVFP4 = 2 };
+
+/* option flags */
+enum {
+  GBR_FLAG_NO_PDL = 1,        /* launch without programmatic dependent launch */
+  GBR_FLAG_FORCE_GENERIC = 2, /* use the generic row-per-CTA kernel (A/B and tests) */
+  GBR_FLAG_FORCE_GEMV = 4,    /* use the small-M tensor-core GEMV kernel when eligible */
+  GBR_FLAG_FORCE_TC = 8,      /* use the tcgen05 prefill kernel when eligible */
+  GBR_FLAG_UNFUSED = 16       /* two launches: gate logits, then router_select (A/B only) */
+};
+
+/* kernel families reported by router_regime() */
+enum { GBR_REGIME_GENERIC = 0, GBR_REGIME_GEMV = 1, GBR_REGIME_TC = 2, GBR_REGIME_UNFUSED = 3 };
+
+typedef struct {
+  int x_dtype;                /* GBR_F32 or GBR_BF16 (default for router_forward: BF16) */
+  int w_dtype;                /* GBR_F32, GBR_BF16 or GBR_NVFP4 */
+  const uint8_t* w_scales;    /* NVFP4 only: E4M3 codes [E, H/16] */
+  float w_global_scale;       /* NVFP4 only */
+  void* workspace;            /* nullable: library-owned per (device, stream) if NULL.
+                                 Must be 256-byte aligned and zero-filled before its
+                                 first use; every call leaves it ready for the next. */
+  size_t workspace_bytes;
+  /* optional M=2 unique-route table; all four or none; M must be even and
+     group g covers rows 2g and 2g+1 (layouts as in route_table, T = 2) */
+  int32_t* tbl_unique;        /* [M/2, 2k] */
+  uint8_t* tbl_mask;          /* [M/2, 2k] */
+  uint8_t* tbl_map;           /* [M/2, 2, k] */
+  int32_t* tbl_count;         /* [M/2] */
+  float* out_logits;          /* nullable FP32 [M, E]: the raw gate logits the
+                                 selection used (telemetry tap) */
+  int flags;                  /* GBR_FLAG_* */
+} gbr_opts;
+
+/*
+ * router_forward — steps 1-4 in one launch, BF16 x [M, H] and BF16
+ * W_gate [E, H], FP32 bias [E] (nullable; sqrt-softplus only).
+ * Outputs: out_idx int32 [M, k] (expert ids in slot order), out_w FP32
+ * [M, k]. Uses a library-owned workspace for (current device, stream),
+ * allocated and zero-filled on first use (call once before capturing the
+ * stream into a CUDA graph). Thread-safe.
+ * Errors: GBR_EINVAL for null required pointers, M < 0, H < 1, E < 1,
+ * k < 1, k > E, act outside the enum, bias with softmax; GBR_EUNSUPPORTED
+ * for E > 512 or k > 16; GBR_ECUDA if allocation or launch fails.
+ */
+int router_forward(const void* x, const void* W_gate, const float* bias, int M, int H, int E,
+                   int k, int act, int32_t* out_idx, float* out_w, cudaStream_t stream);
+
+/*
+ * router_forward_ex — as router_forward with dtypes, NVFP4 weights, an
+ * explicit workspace, the fused M=2 route table and the logits tap.
+ * opt may be NULL (BF16 x and W, library workspace). Extra errors:
+ * GBR_EINVAL for a partial table pointer set, a table with odd M, NVFP4
+ * without scales or with H % 16 != 0, dtypes outside the enums;
+ * GBR_EWORKSPACE when workspace_bytes < router_workspace_size(...).
+ * Concurrent calls that share one workspace race; give each stream its own.
+ */
+int router_forward_ex(const void* x, const void* W_gate, const float* bias, int M, int H, int E,
+                      int k, int act, int32_t* out_idx, float* out_w, const gbr_opts* opt,
+                      cudaStream_t stream);
+
+/* Bytes of workspace router_forward_ex needs for this shape (0 if none). */
+size_t router_workspace_size(int M, int H, int E, int k, const gbr_opts* opt);
+
+/* Which kernel family router_forward_ex would launch (GBR_REGIME_*), or -1
+ * for arguments it would reject. */
+int router_regime(int M, int H, int E, int k, const gbr_opts* opt);
+
+/*
+ * router_select — steps 2-4 alone, on caller FP32 logits [M, E]; bias
+ * nullable FP32 [E] (sqrt-softplus only). The same selection code the fused
+ * kernels run; it exists so the selection stage can be checked on identical
+ * FP32 logits (qwisp issue #145, "Gates", G-A: synthetic logits with exact
+ * and near ties at the top-k boundary). Errors as router_forward.
+ */
+int router_select(const float* logits, const float* bias, int M, int E, int k, int act,
+                  int32_t* out_idx, float* out_w, cudaStream_t stream);
+
+/*
+ * route_table — step 5 alone for `groups` groups of T = tokens_per_group
+ * rows (1 <= T <= 8), k slots each (1 <= k <= 16):
+ *   idx        int32 [groups, T, k]  expert ids (expected >= 0)
+ *   out_unique int32 [groups, T*k]   unique experts in encounter order
+ *                                    (token-major, slot order), -1 past count
+ *   out_mask   uint8 [groups, T*k]   bit t set when token t routes to
+ *                                    out_unique[u]; 0 past count
+ *   out_map    uint8 [groups, T, k]  u such that out_unique[u] == idx[t][s]
+ *   out_count  int32 [groups]        number of unique experts
+ * Duplicates within a row map to the same u. Weights and ids are untouched
+ * (the b70 note requires them preserved bit-for-bit).
+ * Errors: GBR_EINVAL for null pointers, groups < 0, T or k out of range.
+ */
+int route_table(const int32_t* idx, int groups, int tokens_per_group, int k, int32_t* out_unique,
+                uint8_t* out_mask, uint8_t* out_map, int32_t* out_count, cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* router_strerror(int status);
+
+/*
+ * router_device_status — synchronises the current device and reports
+ * GBR_ETIMEOUT if any kernel of this library gave up a bounded wait since
+ * the last clear (its outputs for that call are then undefined), else
+ * GBR_OK; GBR_ECUDA if the device cannot be queried. clear != 0 resets it.
+ */
+int router_device_status(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBROUTER_H_ */

@@ -1,0 +1,321 @@
+// Small-M (decode / verify widths) fused router and the generic router.
+//
+// Small-M design. At M <= 64 the router reads W_gate (E x H BF16, 1-4 MiB)
+// once and little else, so it is bound by HBM and by latency. The grid
+// spreads W over the whole GPU: CTA (r, eg) owns expert group eg (16
+// experts) and the r-th of CL slices of H; the CL CTAs of one expert group
+// form a thread-block cluster. Every thread issues its 16-byte W loads
+// before it waits on the preceding kernel (programmatic dependent launch),
+// so back-to-back calls overlap their W streams with the previous call's
+// tail. The contraction runs on the tensor cores with mma.sync m16n8k16
+// (experts as the 16-row operand, up to 8 tokens per n-tile), which keeps
+// the FP32-accumulate arithmetic far below the memory time even at M=64.
+//
+// Reductions. Per-warp partials are summed in shared memory, the CL slices
+// of a cluster through distributed shared memory, both in a fixed order, so
+// the logits are deterministic. Each cluster writes its 16 x M logits to a
+// small FP32 buffer [M, E] (L2-resident scratch, or the caller's logits
+// tap) and bumps an arrival ticket; the last cluster to arrive runs the
+// selection, one warp per row, and resets the ticket for the next call.
+// Nothing ever waits on another CTA except through the hardware cluster
+// barrier. This is the "threadgroup-level reduction" option that qwisp
+// issue #145 ("Change") leaves to measurement, with the E logits kept on
+// chip and in L2 instead of a separate launch.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "select.cuh"
+
+namespace gbr {
+namespace {
+
+constexpr int kGemvWarps = 4;
+constexpr int kChunkBatch = 4;  // 32-element H chunks held in registers per warp at once
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(const float* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void dsmem_st_u32(uint32_t* p, uint32_t rank, uint32_t v) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(r), "r"(v) : "memory");
+}
+
+// K permutation inside a 32-element chunk: thread t of a quad owns the 8
+// consecutive elements [8t, 8t+8). For MMA j (0, 1) its logical k slots
+// {2t, 2t+1, 2t+8, 2t+9} are the physical elements 8t + 4j + {0,1,2,3}.
+// A (W rows g, g+8) and B (x token g) use the same map, so every product
+// pairs the same h and each h is used once.
+template <int NT, int VPL, bool SELECT>
+__global__ void __launch_bounds__(kGemvWarps * 32)
+    k_gemv_router(const RouterArgs a, int CL) {
+  constexpr int NTOK = 8 * NT;
+  __shared__ float s_part[kGemvWarps][16][NTOK];
+  __shared__ float s_cta[16][NTOK];
+  __shared__ int32_t s_sel[kGemvWarps * kMaxK];
+  __shared__ int32_t s_rank[kGemvWarps][32];
+  __shared__ uint32_t s_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int rank = blockIdx.x;  // the grid's x extent equals the cluster size
+  const int e0 = blockIdx.y * 16;
+  const int H = a.H, M = a.M, E = a.E;
+  const int Hc = H / CL, nchunk = Hc / 32, h_begin = rank * Hc;
+  const uint16_t* __restrict__ x = static_cast<const uint16_t*>(a.x);
+  const uint16_t* w0 =
+      static_cast<const uint16_t*>(a.w) + (size_t)(e0 + g) * H + h_begin + 8 * t;
+  const uint16_t* w1 = w0 + (size_t)8 * H;
+  const int cpw = warp < nchunk ? (nchunk - warp + kGemvWarps - 1) / kGemvWarps : 0;
+
+  pdl_launch_dependents();
+
+  uint4 wa[kChunkBatch], wb[kChunkBatch];
+#pragma unroll
+  for (int i = 0; i < kChunkBatch; ++i) {
+    if (i < cpw) {
+      const int off = (warp + kGemvWarps * i) * 32;
+      wa[i] = ld_nc_v4(w0 + off);
+      wb[i] = ld_nc_v4(w1 + off);
+    }
+  }
+  pdl_wait();  // x, the scratch and the ticket belong to the preceding call until here
+
+  float acc[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+
+  for (int jb = 0; jb < cpw; jb += kChunkBatch) {
+    if (jb > 0) {
+#pragma unroll
+      for (int i = 0; i < kChunkBatch; ++i) {
+        if (jb + i < cpw) {
+          const int off = (warp + kGemvWarps * (jb + i)) * 32;
+          wa[i] = ld_nc_v4(w0 + off);
+          wb[i] = ld_nc_v4(w1 + off);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kChunkBatch; ++i) {
+      if (jb + i < cpw) {
+        const int hoff = h_begin + (warp + kGemvWarps * (jb + i)) * 32 + 8 * t;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const int tok = n * 8 + g;
+          uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+          if (tok < M) xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + hoff));
+          mma_bf16_16816(acc[n], wa[i].x, wb[i].x, wa[i].y, wb[i].y, xv.x, xv.y);
+          mma_bf16_16816(acc[n], wa[i].z, wb[i].z, wa[i].w, wb[i].w, xv.z, xv.w);
+        }
+      }
+    }
+  }
+
+  // accumulator layout: c0,c1 -> expert g, tokens 2t, 2t+1; c2,c3 -> expert g+8
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    s_part[warp][g][n * 8 + 2 * t] = acc[n][0];
+    s_part[warp][g][n * 8 + 2 * t + 1] = acc[n][1];
+    s_part[warp][g + 8][n * 8 + 2 * t] = acc[n][2];
+    s_part[warp][g + 8][n * 8 + 2 * t + 1] = acc[n][3];
+  }
+  __syncthreads();
+  for (int i = tid; i < 16 * NTOK; i += kGemvWarps * 32) {
+    const int el = i / NTOK, m = i % NTOK;
+    float v = s_part[0][el][m];
+#pragma unroll
+    for (int w = 1; w < kGemvWarps; ++w) v += s_part[w][el][m];
+    s_cta[el][m] = v;
+  }
+  cluster_sync_all();
+
+  // cluster reduction over the CL slices of H; item i = m * 16 + el
+  for (int i = rank + CL * tid; i < 16 * M; i += CL * kGemvWarps * 32) {
+    const int m = i >> 4, el = i & 15;
+    float v = 0.0f;
+    for (int q = 0; q < CL; ++q) v += dsmem_ld_f32(&s_cta[el][m], (uint32_t)q);
+    a.logits[(size_t)m * E + e0 + el] = v;
+  }
+  if (!SELECT) {
+    cluster_sync_all();  // keep shared memory alive until every peer has read it
+    return;
+  }
+  __threadfence();
+  cluster_sync_all();
+  if (rank == 0 && tid == 0) {
+    const uint32_t old = atomicAdd(a.ticket, 1u);
+    const uint32_t last = (old == gridDim.y - 1) ? 1u : 0u;
+    if (last) atomicExch(a.ticket, 0u);
+    for (int q = 0; q < CL; ++q) dsmem_st_u32(&s_flag, (uint32_t)q, last);
+  }
+  cluster_sync_all();
+  if (!s_flag) return;
+  __threadfence();
+
+  // the last cluster selects: row = base + warp, rows 2p and 2p+1 share a CTA
+  const bool table = a.tbl_unique != nullptr;
+  const int k = a.k;
+  for (int base = rank * kGemvWarps; base < M; base += CL * kGemvWarps) {
+    const int row = base + warp;
+    if (row < M)
+      warp_select_row<VPL>(LdCG{a.logits + (size_t)row * E}, a.bias, E, k, a.act,
+                           a.out_idx + (size_t)row * k, a.out_w + (size_t)row * k,
+                           s_sel + warp * k);
+    if (table) {
+      __syncthreads();
+      if ((warp & 1) == 0 && row + 1 < M) {
+        const size_t gi = (size_t)(row >> 1);
+        warp_route_table(s_sel + warp * k, s_rank[warp], 2, k, a.tbl_unique + gi * 2 * k,
+                         a.tbl_mask + gi * 2 * k, a.tbl_map + gi * 2 * k, a.tbl_count + gi);
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Generic router: one CTA per row (two rows when a table is fused), any
+// dtype, any H. W is decoded element by element (NVFP4: e2m1 * e4m3, the
+// global scale applied to the FP32 sum). Each expert's dot product is a
+// fixed per-lane FMA order followed by a fixed butterfly.
+constexpr int kGenWarps = 8;
+
+__device__ __forceinline__ float x_at(const RouterArgs& a, size_t i) {
+  return a.x_dtype == DT_F32 ? static_cast<const float*>(a.x)[i]
+                             : bf16_bits_to_f32(static_cast<const uint16_t*>(a.x)[i]);
+}
+
+__device__ __forceinline__ float w_at(const RouterArgs& a, int e, int h) {
+  if (a.w_dtype == DT_F32) return static_cast<const float*>(a.w)[(size_t)e * a.H + h];
+  if (a.w_dtype == DT_BF16)
+    return bf16_bits_to_f32(static_cast<const uint16_t*>(a.w)[(size_t)e * a.H + h]);
+  const uint32_t byte = static_cast<const uint8_t*>(a.w)[(size_t)e * (a.H / 2) + h / 2];
+  const uint32_t code = (h & 1) ? (byte >> 4) : (byte & 15u);
+  return e2m1_to_f32(code) * e4m3_to_f32(a.w_scales[(size_t)e * (a.H / 16) + h / 16]);
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(kGenWarps * 32) k_generic_router(const RouterArgs a, int rows) {
+  __shared__ float s_log[2][kMaxE];
+  __shared__ int32_t s_sel[2 * kMaxK];
+  __shared__ int32_t s_rank[32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row0 = blockIdx.x * rows;
+  const int M = a.M, H = a.H, E = a.E, k = a.k;
+  for (int r = 0; r < rows; ++r) {
+    const int m = row0 + r;
+    if (m >= M) break;
+    for (int e = warp; e < E; e += kGenWarps) {
+      float acc = 0.0f;
+      for (int h = lane; h < H; h += 32) acc = fmaf(x_at(a, (size_t)m * H + h), w_at(a, e, h), acc);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+      if (lane == 0) {
+        const float l = (a.w_dtype == DT_NVFP4) ? acc * a.w_global : acc;
+        s_log[r][e] = l;
+        if (a.logits) a.logits[(size_t)m * E + e] = l;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp < rows && row0 + warp < M) {
+    const size_t m = (size_t)(row0 + warp);
+    warp_select_row<VPL>(LdPlain{s_log[warp]}, a.bias, E, k, a.act, a.out_idx + m * k,
+                         a.out_w + m * k, s_sel + warp * k);
+  }
+  __syncthreads();
+  if (a.tbl_unique && rows == 2 && warp == 0 && row0 + 1 < M) {
+    const size_t gi = (size_t)(row0 >> 1);
+    warp_route_table(s_sel, s_rank, 2, k, a.tbl_unique + gi * 2 * k, a.tbl_mask + gi * 2 * k,
+                     a.tbl_map + gi * 2 * k, a.tbl_count + gi);
+  }
+}
+
+template <class Kern>
+cudaError_t launch_ex(Kern kern, dim3 grid, dim3 block, int cluster, bool pdl, cudaStream_t stream,
+                      const RouterArgs& a, int extra) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int n = 0;
+  if (cluster > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = cluster;
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, a, extra);
+}
+
+template <int NT, bool SELECT>
+cudaError_t gemv_dispatch_vpl(const RouterArgs& a, int CL, bool pdl, cudaStream_t s) {
+  const dim3 grid(CL, a.E / 16), block(kGemvWarps * 32);
+  if (a.E <= 128) return launch_ex(k_gemv_router<NT, 4, SELECT>, grid, block, CL, pdl, s, a, CL);
+  if (a.E <= 256) return launch_ex(k_gemv_router<NT, 8, SELECT>, grid, block, CL, pdl, s, a, CL);
+  return launch_ex(k_gemv_router<NT, 16, SELECT>, grid, block, CL, pdl, s, a, CL);
+}
+
+template <bool SELECT>
+cudaError_t gemv_dispatch(const RouterArgs& a, int CL, bool pdl, cudaStream_t s) {
+  if (a.M <= 8) return gemv_dispatch_vpl<1, SELECT>(a, CL, pdl, s);
+  if (a.M <= 16) return gemv_dispatch_vpl<2, SELECT>(a, CL, pdl, s);
+  if (a.M <= 32) return gemv_dispatch_vpl<4, SELECT>(a, CL, pdl, s);
+  return gemv_dispatch_vpl<8, SELECT>(a, CL, pdl, s);
+}
+
+}  // namespace
+
+int gemv_cluster_size(int H) {
+  for (int cl = 8; cl > 1; cl >>= 1)
+    if (H % (32 * cl) == 0) return cl;
+  return 1;
+}
+
+cudaError_t launch_gemv(const RouterArgs& a, bool select, bool pdl, cudaStream_t stream) {
+  const int CL = gemv_cluster_size(a.H);
+  return select ? gemv_dispatch<true>(a, CL, pdl, stream) : gemv_dispatch<false>(a, CL, pdl, stream);
+}
+
+cudaError_t launch_generic(const RouterArgs& a, bool pdl, cudaStream_t stream) {
+  const int rows = a.tbl_unique ? 2 : 1;
+  const dim3 grid((a.M + rows - 1) / rows), block(kGenWarps * 32);
+  if (a.E <= 32) return launch_ex(k_generic_router<1>, grid, block, 1, pdl, stream, a, rows);
+  if (a.E <= 64) return launch_ex(k_generic_router<2>, grid, block, 1, pdl, stream, a, rows);
+  if (a.E <= 128) return launch_ex(k_generic_router<4>, grid, block, 1, pdl, stream, a, rows);
+  if (a.E <= 256) return launch_ex(k_generic_router<8>, grid, block, 1, pdl, stream, a, rows);
+  return launch_ex(k_generic_router<16>, grid, block, 1, pdl, stream, a, rows);
+}
+
+}  // namespace gbr

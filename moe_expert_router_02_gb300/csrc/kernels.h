@@ -1,0 +1,29 @@
+// Host-side launchers of the router kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace gbr {
+
+cudaError_t launch_select(const float* logits, const float* bias, int M, int E, int k, int act,
+                          int32_t* out_idx, float* out_w, cudaStream_t stream);
+
+cudaError_t launch_route_table(const int32_t* idx, int groups, int T, int k, int32_t* unique,
+                               uint8_t* mask, uint8_t* map, int32_t* count, cudaStream_t stream);
+
+// Small-M tensor-core GEMV router. select == false writes the logits only
+// (first half of the unfused A/B pair).
+int gemv_cluster_size(int H);
+cudaError_t launch_gemv(const RouterArgs& a, bool select, bool pdl, cudaStream_t stream);
+
+// Row-per-CTA router for any dtype and shape.
+cudaError_t launch_generic(const RouterArgs& a, bool pdl, cudaStream_t stream);
+
+// tcgen05 prefill router.
+bool tc_eligible(int M, int H, int E, int k, int x_dtype, int w_dtype);
+cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream);
+int tc_read_status(int clear);  // 0 ok, 1 a bounded wait expired, -1 query failed
+
+}  // namespace gbr

@@ -1,0 +1,59 @@
+// router_select and route_table kernels: the selection stage and the
+// unique-route table as standalone launches.
+#include "kernels.h"
+#include "select.cuh"
+
+namespace gbr {
+namespace {
+
+constexpr int kSelWarps = 8;
+
+template <int VPL>
+__global__ void __launch_bounds__(kSelWarps * 32)
+    k_select(const float* __restrict__ logits, const float* __restrict__ bias, int M, int E, int k,
+             int act, int32_t* __restrict__ out_idx, float* __restrict__ out_w) {
+  const int row = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
+  if (row >= M) return;  // whole warps leave together
+  warp_select_row<VPL>(LdPlain{logits + (size_t)row * E}, bias, E, k, act,
+                       out_idx + (size_t)row * k, out_w + (size_t)row * k, nullptr);
+}
+
+constexpr int kTblWarps = 8;
+
+__global__ void __launch_bounds__(kTblWarps * 32)
+    k_route_table(const int32_t* __restrict__ idx, int G, int T, int k,
+                  int32_t* __restrict__ unique, uint8_t* __restrict__ mask,
+                  uint8_t* __restrict__ map, int32_t* __restrict__ count) {
+  __shared__ int32_t s_idx[kTblWarps][128];
+  __shared__ int32_t s_rank[kTblWarps][128];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * kTblWarps + warp;
+  if (g >= G) return;
+  const int n = T * k;
+  for (int p = lane; p < n; p += 32) s_idx[warp][p] = idx[(size_t)g * n + p];
+  __syncwarp();
+  warp_route_table(s_idx[warp], s_rank[warp], T, k, unique + (size_t)g * n, mask + (size_t)g * n,
+                   map + (size_t)g * n, count + g);
+}
+
+}  // namespace
+
+cudaError_t launch_select(const float* logits, const float* bias, int M, int E, int k, int act,
+                          int32_t* out_idx, float* out_w, cudaStream_t stream) {
+  const dim3 grid((M + kSelWarps - 1) / kSelWarps), block(kSelWarps * 32);
+  if (E <= 32) k_select<1><<<grid, block, 0, stream>>>(logits, bias, M, E, k, act, out_idx, out_w);
+  else if (E <= 64) k_select<2><<<grid, block, 0, stream>>>(logits, bias, M, E, k, act, out_idx, out_w);
+  else if (E <= 128) k_select<4><<<grid, block, 0, stream>>>(logits, bias, M, E, k, act, out_idx, out_w);
+  else if (E <= 256) k_select<8><<<grid, block, 0, stream>>>(logits, bias, M, E, k, act, out_idx, out_w);
+  else k_select<16><<<grid, block, 0, stream>>>(logits, bias, M, E, k, act, out_idx, out_w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_table(const int32_t* idx, int groups, int T, int k, int32_t* unique,
+                               uint8_t* mask, uint8_t* map, int32_t* count, cudaStream_t stream) {
+  const dim3 grid((groups + kTblWarps - 1) / kTblWarps), block(kTblWarps * 32);
+  k_route_table<<<grid, block, 0, stream>>>(idx, groups, T, k, unique, mask, map, count);
+  return cudaGetLastError();
+}
+
+}  // namespace gbr

@@ -1,0 +1,145 @@
+"""Python binding of the ``gbrouter`` C ABI (``include/gbrouter.h``).
+
+Argument marshalling only: every step of the router runs in the CUDA
+library. The functions carry the C names and take torch CUDA tensors (or
+``None`` for nullable pointers) and an optional ``torch.cuda.Stream``. A
+non-zero status raises :class:`RouterError`. There is no fallback: if the
+library is missing and cannot be built, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import build as _build
+
+GBR_OK, GBR_EINVAL, GBR_EUNSUPPORTED, GBR_ECUDA, GBR_EWORKSPACE, GBR_ETIMEOUT = range(6)
+GBR_ACT_SOFTMAX, GBR_ACT_SQRT_SOFTPLUS = 0, 1
+GBR_F32, GBR_BF16, GBR_NVFP4 = 0, 1, 2
+GBR_FLAG_NO_PDL, GBR_FLAG_FORCE_GENERIC, GBR_FLAG_FORCE_GEMV, GBR_FLAG_FORCE_TC, \
+    GBR_FLAG_UNFUSED = 1, 2, 4, 8, 16
+GBR_REGIME_GENERIC, GBR_REGIME_GEMV, GBR_REGIME_TC, GBR_REGIME_UNFUSED = 0, 1, 2, 3
+
+EXPORTS = ("router_forward", "router_forward_ex", "router_workspace_size", "router_regime",
+           "router_select", "route_table", "router_strerror", "router_device_status")
+
+
+class RouterError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {router_strerror(status)} (status {status})")
+
+
+class GbrOpts(ctypes.Structure):
+    _fields_ = [("x_dtype", ctypes.c_int), ("w_dtype", ctypes.c_int),
+                ("w_scales", ctypes.c_void_p), ("w_global_scale", ctypes.c_float),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("tbl_unique", ctypes.c_void_p), ("tbl_mask", ctypes.c_void_p),
+                ("tbl_map", ctypes.c_void_p), ("tbl_count", ctypes.c_void_p),
+                ("out_logits", ctypes.c_void_p), ("flags", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load (building first if stale) the in-tree ``libgbrouter.so``."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            L.router_forward.argtypes = [P, P, P, I, I, I, I, I, P, P, P]
+            L.router_forward_ex.argtypes = [P, P, P, I, I, I, I, I, P, P,
+                                            ctypes.POINTER(GbrOpts), P]
+            L.router_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(GbrOpts)]
+            L.router_workspace_size.restype = S
+            L.router_regime.argtypes = [I, I, I, I, ctypes.POINTER(GbrOpts)]
+            L.router_select.argtypes = [P, P, I, I, I, I, P, P, P]
+            L.route_table.argtypes = [P, I, I, I, P, P, P, P, P]
+            L.router_strerror.argtypes = [I]
+            L.router_strerror.restype = ctypes.c_char_p
+            L.router_device_status.argtypes = [I]
+            for f in (L.router_forward, L.router_forward_ex, L.router_regime, L.router_select,
+                      L.route_table, L.router_device_status):
+                f.restype = I
+            _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != GBR_OK:
+        raise RouterError(rc, where)
+
+
+def make_opts(x_dtype=GBR_BF16, w_dtype=GBR_BF16, w_scales=None, w_global_scale=1.0,
+              workspace=None, workspace_bytes=0, table=None, out_logits=None, flags=0) -> GbrOpts:
+    """``table`` is None or a tuple (unique, mask, map, count) of tensors."""
+    o = GbrOpts()
+    o.x_dtype, o.w_dtype = x_dtype, w_dtype
+    o.w_scales = _ptr(w_scales)
+    o.w_global_scale = float(w_global_scale)
+    o.workspace = _ptr(workspace)
+    o.workspace_bytes = int(workspace_bytes)
+    if table is not None:
+        o.tbl_unique, o.tbl_mask, o.tbl_map, o.tbl_count = (_ptr(t) for t in table)
+    o.out_logits = _ptr(out_logits)
+    o.flags = int(flags)
+    return o
+
+
+def router_strerror(status: int) -> str:
+    return lib().router_strerror(int(status)).decode()
+
+
+def router_forward(x, W_gate, bias, M, H, E, k, act, out_idx, out_w, stream=None):
+    _check(lib().router_forward(_ptr(x), _ptr(W_gate), _ptr(bias), M, H, E, k, act,
+                                _ptr(out_idx), _ptr(out_w), _stream(stream)), "router_forward")
+
+
+def router_forward_ex(x, W_gate, bias, M, H, E, k, act, out_idx, out_w, opts=None, stream=None):
+    _check(lib().router_forward_ex(_ptr(x), _ptr(W_gate), _ptr(bias), M, H, E, k, act,
+                                   _ptr(out_idx), _ptr(out_w),
+                                   ctypes.byref(opts) if opts is not None else None,
+                                   _stream(stream)), "router_forward_ex")
+
+
+def router_workspace_size(M, H, E, k, opts=None) -> int:
+    return lib().router_workspace_size(M, H, E, k, ctypes.byref(opts) if opts is not None else None)
+
+
+def router_regime(M, H, E, k, opts=None) -> int:
+    return lib().router_regime(M, H, E, k, ctypes.byref(opts) if opts is not None else None)
+
+
+def router_select(logits, bias, M, E, k, act, out_idx, out_w, stream=None):
+    _check(lib().router_select(_ptr(logits), _ptr(bias), M, E, k, act, _ptr(out_idx),
+                               _ptr(out_w), _stream(stream)), "router_select")
+
+
+def route_table(idx, groups, tokens_per_group, k, out_unique, out_mask, out_map, out_count,
+                stream=None):
+    _check(lib().route_table(_ptr(idx), groups, tokens_per_group, k, _ptr(out_unique),
+                             _ptr(out_mask), _ptr(out_map), _ptr(out_count), _stream(stream)),
+           "route_table")
+
+
+def router_device_status(clear: bool = False) -> int:
+    return lib().router_device_status(1 if clear else 0)

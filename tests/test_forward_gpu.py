@@ -1,0 +1,209 @@
+"""Fused router_forward / router_forward_ex against the oracle.
+
+Expert ids must equal the oracle's except on rows whose oracle key gap is
+below 1e-5 (counted); weights within 2e-5 absolute. The fused selection is
+also checked bit-exactly against the oracle run on the kernel's own FP32
+logits (the telemetry tap), and the fused M=2 table bit-exactly against the
+oracle table of the kernel's ids."""
+import numpy as np
+import pytest
+
+import oracle
+from moe_expert_router_02_gb300 import router as R
+from moe_expert_router_02_gb300 import synth
+from tests.helpers import W_TOL, check_routes, dev, empty_outputs
+
+pytestmark = pytest.mark.gpu
+
+
+def upload(case):
+    t = dict(x=dev(case["x"]), W=dev(case["W"]))
+    t["bias"] = None if case["bias"] is None else dev(case["bias"])
+    t["scales"] = None if case["scales"] is None else dev(case["scales"])
+    return t
+
+
+def run_case(case, flags=0, table=False, tap=False, t=None):
+    import torch
+    M, H, E, k = case["M"], case["H"], case["E"], case["k"]
+    t = t or upload(case)
+    idx, w = empty_outputs(M, k)
+    tbl = None
+    if table:
+        n = 2 * k
+        tbl = (torch.full((M // 2, n), -9, dtype=torch.int32, device="cuda"),
+               torch.full((M // 2, n), 0xEE, dtype=torch.uint8, device="cuda"),
+               torch.full((M // 2, 2, k), 0xEE, dtype=torch.uint8, device="cuda"),
+               torch.full((M // 2,), -9, dtype=torch.int32, device="cuda"))
+    logits = torch.full((M, E), float("nan"), device="cuda") if tap else None
+    opts = R.make_opts(x_dtype=case["x_dtype"], w_dtype=case["w_dtype"], w_scales=t["scales"],
+                       w_global_scale=case["g"], table=tbl, out_logits=logits, flags=flags)
+    R.router_forward_ex(t["x"], t["W"], t["bias"], M, H, E, k, case["act"], idx, w, opts)
+    torch.cuda.synchronize()
+    out = dict(idx=idx.cpu().numpy(), w=w.cpu().numpy())
+    if table:
+        out["table"] = [x.cpu().numpy() for x in tbl]
+    if tap:
+        out["logits"] = logits.cpu().numpy()
+    return out
+
+
+def check_case(case, flags=0, table=False, expect_regime=None):
+    if expect_regime is not None:
+        o = R.make_opts(x_dtype=case["x_dtype"], w_dtype=case["w_dtype"],
+                        w_scales=1 if case["scales"] is not None else None, flags=flags)
+        assert R.router_regime(case["M"], case["H"], case["E"], case["k"], o) == expect_regime
+    got = run_case(case, flags=flags, table=table, tap=True)
+    ref = oracle.router(case)
+    k = case["k"]
+    differ = check_routes(got["idx"], got["w"], ref["idx"], ref["w"], ref["keys"], k)
+    # selection stage on the kernel's own logits: bit-exact ids
+    lg = got["logits"]
+    assert np.all(np.isfinite(lg))
+    np.testing.assert_allclose(lg, ref["logits"], rtol=0, atol=1e-4)
+    oi, ow, _ = oracle.select(lg.astype(np.float64), k, case["act"], bias=case["bias"])
+    assert np.array_equal(got["idx"], oi)
+    assert np.max(np.abs(got["w"] - ow)) <= W_TOL
+    if table:
+        tref = oracle.route_table(got["idx"].reshape(-1, 2, k))
+        for name, g, r in zip(("unique", "mask", "map", "count"), got["table"], tref):
+            assert np.array_equal(g, r), name
+    return differ
+
+
+C = synth.CONFIGS
+
+
+def test_tiny_fp32_case():
+    check_case(synth.make_case(C["C0"], seed=0), expect_regime=R.GBR_REGIME_GENERIC)
+
+
+@pytest.mark.parametrize("M", [1, 2, 8])
+@pytest.mark.parametrize("dup", [0.0, 0.1])
+def test_decode_softmax(M, dup):
+    case = synth.make_case(C["C1"], M=M, seed=M, dup_frac=dup)
+    check_case(case, expect_regime=R.GBR_REGIME_GEMV)
+    check_case(case, flags=R.GBR_FLAG_FORCE_GENERIC)
+
+
+@pytest.mark.parametrize("M", [1, 16, 64])
+def test_sqrt_softplus_bias(M):
+    case = synth.make_case(C["C2"], M=M, seed=10 + M, dup_frac=0.1)
+    check_case(case, expect_regime=R.GBR_REGIME_GEMV)
+
+
+@pytest.mark.parametrize("M", [3, 5, 13, 37, 63])
+def test_ragged_M(M):
+    check_case(synth.make_case(C["C2"], M=M, seed=M))
+
+
+def test_m2_route_table_fused():
+    cfg = C["C4"]
+    for seed in range(6):
+        case = synth.make_case(cfg, M=2, seed=seed)
+        if seed % 2 == 0:
+            x = case["x"].copy()
+            x[1] = x[0]  # identical rows: identical expert sets
+            case["x"] = x
+        check_case(case, table=True, expect_regime=R.GBR_REGIME_GEMV)
+        check_case(case, table=True, flags=R.GBR_FLAG_FORCE_GENERIC)
+    for M in (4, 8, 64):
+        check_case(synth.make_case(cfg, M=M, seed=M), table=True)
+
+
+def test_exact_tie_from_duplicated_weights_goes_to_lower_index():
+    cfg = dict(C["C1"])
+    case = synth.make_case(cfg, M=4, seed=3)
+    W = synth.bf16_bits_to_f32(case["W"]).copy()
+    W[200] = W[37]  # experts 37 and 200 now have identical logits
+    x = np.tile(W[37] / np.sqrt(np.mean(W[37] ** 2)), (4, 1)).astype(np.float32)
+    case["W"] = synth.f32_to_bf16_bits(W)
+    case["x"] = synth.f32_to_bf16_bits(x)
+    for k in (1, 2, 8):
+        case["k"] = k
+        got = run_case(case)
+        assert np.all(got["idx"][:, 0] == 37)
+        if k >= 2:
+            assert np.all(got["idx"][:, 1] == 200)
+            np.testing.assert_allclose(got["w"][:, 0], got["w"][:, 1], rtol=0, atol=0)
+
+
+def test_unfused_pair_matches_fused_bitwise():
+    case = synth.make_case(C["C1"], M=8, seed=5)
+    a = run_case(case)
+    b = run_case(case, flags=R.GBR_FLAG_UNFUSED)
+    assert np.array_equal(a["idx"], b["idx"])
+    assert np.array_equal(a["w"], b["w"])
+
+
+@pytest.mark.parametrize("H", [64, 96, 160, 100, 2056])
+def test_odd_hidden_sizes(H):
+    cfg = dict(C["C1"], H=H)
+    check_case(synth.make_case(cfg, M=8, seed=H))
+
+
+@pytest.mark.parametrize("E,k", [(16, 2), (64, 16), (128, 4), (512, 8), (48, 3)])
+def test_expert_counts(E, k):
+    cfg = dict(C["C2"], E=E, k=k, H=512)
+    check_case(synth.make_case(cfg, M=8, seed=E))
+    check_case(synth.make_case(cfg, M=33, seed=E + 1))
+
+
+def test_nvfp4_weights_small_M():
+    case = synth.make_case(C["C2"], M=8, seed=4, w_dtype=synth.NVFP4)
+    check_case(case)
+    case = synth.make_case(C["C2"], M=2, seed=4, w_dtype=synth.NVFP4, nvfp4_global=0.5)
+    check_case(case)
+
+
+def test_repeated_calls_reuse_workspace_and_ticket():
+    import torch
+    case = synth.make_case(C["C1"], M=8, seed=1)
+    t = upload(case)
+    first = run_case(case, t=t)
+    for _ in range(20):
+        again = run_case(case, t=t)
+        assert np.array_equal(first["idx"], again["idx"])
+        assert np.array_equal(first["w"], again["w"])
+    # explicit caller workspace, zero-filled once
+    need = R.router_workspace_size(8, case["H"], case["E"], case["k"])
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    idx, w = empty_outputs(8, case["k"])
+    for _ in range(3):
+        R.router_forward_ex(t["x"], t["W"], None, 8, case["H"], case["E"], case["k"], case["act"],
+                            idx, w, R.make_opts(workspace=ws, workspace_bytes=need))
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), first["idx"])
+
+
+def test_graph_replay_with_changing_inputs():
+    import torch
+    cfg = C["C4"]
+    M, H, E, k = 2, cfg["H"], cfg["E"], cfg["k"]
+    cases = [synth.make_case(cfg, M=M, seed=s) for s in range(8)]
+    t = upload(cases[0])
+    idx, w = empty_outputs(M, k)
+    tbl = (torch.zeros((1, 2 * k), dtype=torch.int32, device="cuda"),
+           torch.zeros((1, 2 * k), dtype=torch.uint8, device="cuda"),
+           torch.zeros((1, 2, k), dtype=torch.uint8, device="cuda"),
+           torch.zeros((1,), dtype=torch.int32, device="cuda"))
+    opts = R.make_opts(table=tbl)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        R.router_forward_ex(t["x"], t["W"], t["bias"], M, H, E, k, cfg["act"], idx, w, opts,
+                            stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):  # three back-to-back calls inside one graph
+            R.router_forward_ex(t["x"], t["W"], t["bias"], M, H, E, k, cfg["act"], idx, w, opts,
+                                stream=s)
+    for case in cases[1:]:
+        t["x"].copy_(dev(case["x"]))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.router(case)
+        check_routes(idx.cpu().numpy(), w.cpu().numpy(), ref["idx"], ref["w"], ref["keys"], k)
+        tref = oracle.route_table(idx.cpu().numpy().reshape(1, 2, k))
+        for got, r in zip(tbl, tref):
+            assert np.array_equal(got.cpu().numpy(), r)
