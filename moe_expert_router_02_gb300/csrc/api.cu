@@ -53,8 +53,9 @@ int regime_of(const Shape& s) {
 }
 
 size_t workspace_for(const Shape& s, int regime) {
-  if (regime == GBR_REGIME_GEMV) return kTicketBytes + round_up((size_t)s.M * s.E * 4, 256);
-  if (regime == GBR_REGIME_UNFUSED) return round_up((size_t)s.M * s.E * 4, 256);
+  // ticket in the first 256 bytes, FP32 logits [M, E] after it
+  if (regime == GBR_REGIME_GEMV || regime == GBR_REGIME_UNFUSED)
+    return kTicketBytes + round_up((size_t)s.M * s.E * 4, 256);
   return 0;
 }
 
@@ -146,7 +147,8 @@ int router_forward_ex(const void* x, const void* W_gate, const float* bias, int 
 
   int regime = regime_of(s);
   if ((regime == GBR_REGIME_GEMV || regime == GBR_REGIME_UNFUSED || regime == GBR_REGIME_TC) &&
-      (!aligned16(x) || !aligned16(W_gate) || H % 8 != 0))
+      (!aligned16(x) || !aligned16(W_gate) || H % 8 != 0 ||
+       (s.w_dtype == GBR_NVFP4 && !aligned16(opt->w_scales))))
     regime = GBR_REGIME_GENERIC;
 
   RouterArgs a{};
@@ -188,7 +190,7 @@ int router_forward_ex(const void* x, const void* W_gate, const float* bias, int 
       err = gbr::launch_gemv(a, true, pdl, stream);
       break;
     case GBR_REGIME_UNFUSED: {
-      if (!a.logits) a.logits = static_cast<float*>(ws);
+      if (!a.logits) a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + kTicketBytes);
       err = gbr::launch_gemv(a, false, pdl, stream);
       if (err == cudaSuccess)
         err = gbr::launch_select(a.logits, bias, M, E, k, act, out_idx, out_w, stream);

@@ -50,7 +50,7 @@ __device__ __forceinline__ float dsmem_ld_f32(const float* p, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r));
   return v;
 }
 
@@ -152,8 +152,12 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
   // cluster reduction over the CL slices of H; item i = m * 16 + el
   for (int i = rank + CL * tid; i < 16 * M; i += CL * kGemvWarps * 32) {
     const int m = i >> 4, el = i & 15;
-    float v = 0.0f;
-    for (int q = 0; q < CL; ++q) v += dsmem_ld_f32(&s_cta[el][m], (uint32_t)q);
+    float part[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) part[q] = q < CL ? dsmem_ld_f32(&s_cta[el][m], (uint32_t)q) : 0.0f;
+    float v = part[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) v += part[q];  // fixed order; absent slices add +0
     a.logits[(size_t)m * E + e0 + el] = v;
   }
   if (!SELECT) {

@@ -1,6 +1,607 @@
+// Large-M (prefill) fused router on the 5th-generation tensor cores.
+//
+// One CTA owns 128 token rows and all E <= 256 experts, so a row's logits
+// never leave the SM: TMA streams x [128 x 64] and W_gate [E x 64] BF16
+// tiles (128-byte swizzle) into a shared-memory ring; one thread issues
+// tcgen05.mma (kind::f16, M=128, N=E, K=16) into an FP32 accumulator in
+// tensor memory; after the last k-step the four epilogue warps read their
+// rows back with tcgen05.ld (thread i of warp w owns row 32w+i) and run the
+// activation, top-k and renormalisation in registers. This is the
+// warp-specialised layout the dense_router_decode commit page sketches
+// ("Warp 5 (TMA) ... Warp 4 (MMA) ... Warps 0-3 (EPI)", "the heap
+// accumulates across subtiles, then merge+renorm+store once per row"),
+// written directly in PTX for sm_103a.
+//
+// NVFP4 weights (the same page's "NVFP4 blockscaled GEMM"): x stays BF16,
+// and tcgen05 has no BF16 x FP4 kind, so four extra warps decode each W
+// tile exactly into the BF16 shared-memory layout the MMA reads:
+// e2m1 * e4m3 has at most 6 significant bits and fits BF16's exponent
+// range, so the decoded tile equals W / g bit for bit; the FP32 global
+// scale g multiplies the accumulator in the epilogue.
+//
+// Every wait on an mbarrier gives up after about a second of
+// %globaltimer, records GBR_ETIMEOUT in a device status word and lets the
+// CTA unwind (free tensor memory, return) instead of hanging.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
 #include "kernels.h"
+#include "select.cuh"
+
 namespace gbr {
-bool tc_eligible(int, int, int, int, int, int) { return false; }
-cudaError_t launch_tc(const RouterArgs&, bool, cudaStream_t) { return cudaErrorNotSupported; }
-int tc_read_status(int) { return 0; }
+namespace {
+
+static __device__ unsigned g_tc_status = 0;
+
+constexpr int BM = 128;   // token rows per CTA (= MMA M, = TMEM lanes)
+constexpr int BK = 64;    // BF16 elements per k-step (one 128-byte swizzle atom)
+constexpr int kEpiWarps = 4;
+constexpr int kDeqWarps = 4;
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait; false (and the status word set) when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try(bar, parity)) {
+    if (globaltimer() - t0 > kWaitNs) {
+      atomicOr(&g_tc_status, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
+// 8-row core-matrix groups 1024 bytes apart, descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;               // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;     // stride byte offset
+  d |= (uint64_t)1 << 46;               // version
+  d |= (uint64_t)2 << 61;               // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: FP32 accumulator, BF16 A and B, both
+// K-major, N = E, M = 128.
+__host__ __device__ constexpr uint32_t idesc_bf16(int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive FP32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Row-local top list of capacity KC (>= k+1), kept sorted by (key desc,
+// index asc). Columns arrive in increasing expert order, so a strict
+// comparison keeps the lower index ahead on equal keys.
+template <int KC>
+struct TopList {
+  uint32_t o[KC];  // order-preserving key
+  int i[KC];
+  float z[KC];     // the logit
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      o[j] = 0u;
+      i[j] = 0x7fffffff;
+      z[j] = 0.0f;
+    }
+  }
+  __device__ __forceinline__ void push(uint32_t ok, int idx, float zz) {
+    if (ok <= o[KC - 1]) return;
+#pragma unroll
+    for (int j = KC - 1; j >= 0; --j) {
+      const bool up = (j > 0) && (ok > o[j - 1]);
+      if (ok > o[j]) {
+        o[j] = up ? o[j - 1] : ok;
+        i[j] = up ? i[j - 1] : idx;
+        z[j] = up ? z[j - 1] : zz;
+      }
+    }
+  }
+};
+
+template <int KC>
+struct TopList64 {
+  double v[KC];
+  int i[KC];
+  float z[KC];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      v[j] = -INFINITY;
+      i[j] = 0x7fffffff;
+      z[j] = 0.0f;
+    }
+  }
+  __device__ __forceinline__ void push(double kv, int idx, float zz) {
+    if (!(kv > v[KC - 1])) return;
+#pragma unroll
+    for (int j = KC - 1; j >= 0; --j) {
+      const bool up = (j > 0) && (kv > v[j - 1]);
+      if (kv > v[j]) {
+        v[j] = up ? v[j - 1] : kv;
+        i[j] = up ? i[j - 1] : idx;
+        z[j] = up ? z[j - 1] : zz;
+      }
+    }
+  }
+};
+
+struct TcParams {
+  RouterArgs a;
+  int stages;
+  uint32_t stage_bytes, a_bytes, b_bytes;
+  int tmem_cols;
+};
+
+// Serial unique-route table for one pair of rows (the thread owning the
+// even row of the pair builds it from ids in shared memory).
+__device__ void pair_table(const int32_t* r0, const int32_t* r1, int k, int32_t* unique,
+                           uint8_t* mask, uint8_t* map, int32_t* count) {
+  int32_t uq[2 * kMaxK];
+  uint32_t mk[2 * kMaxK];
+  int n = 0;
+  for (int p = 0; p < 2 * k; ++p) {
+    const int t = p / k;
+    const int32_t v = t ? r1[p - k] : r0[p];
+    int u = 0;
+    while (u < n && uq[u] != v) ++u;
+    if (u == n) {
+      uq[n] = v;
+      mk[n] = 0;
+      ++n;
+    }
+    mk[u] |= 1u << t;
+    map[p] = (uint8_t)u;
+  }
+  for (int u = 0; u < 2 * k; ++u) {
+    unique[u] = u < n ? uq[u] : -1;
+    mask[u] = u < n ? (uint8_t)mk[u] : 0;
+  }
+  *count = n;
+}
+
+template <int KC, bool FP4>
+__global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 1)
+    k_tc_router(const __grid_constant__ CUtensorMap tmap_x,
+                const __grid_constant__ CUtensorMap tmap_w, const TcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const RouterArgs& a = p.a;
+  const int S = p.stages;
+  // 1024-byte aligned tile ring, then barriers
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint8_t* tiles = base;
+  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + (size_t)S * p.stage_bytes);
+  uint64_t* empty = full + S;
+  uint64_t* accf = empty + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  int32_t* s_sel = reinterpret_cast<int32_t*>(tmem_slot + 4);  // [BM][kMaxK] for tables
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int producer_warp = kEpiWarps, mma_warp = kEpiWarps + 1;
+  const int m0 = blockIdx.x * BM;
+  const int nk = a.H / BK;
+  const int E = a.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), FP4 ? 1 + kDeqWarps * 32 : 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(accf), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == mma_warp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(p.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_launch_dependents();
+
+  if (warp == producer_warp) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+      pdl_wait();
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % S;
+        const uint32_t ph = (uint32_t)(kb / S) & 1u;
+        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) break;
+        uint8_t* st = tiles + (size_t)s * p.stage_bytes;
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_expect_tx(fb, FP4 ? p.a_bytes : p.a_bytes + p.b_bytes);
+        tma_load_2d(smem_u32(st), &tmap_x, kb * BK, m0, fb);
+        if (!FP4) tma_load_2d(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, 0, fb);
+        ++issued;
+      }
+      // let copies still in flight land before the CTA can exit
+      for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
+        mbar_wait(smem_u32(&full[kb % S]), (uint32_t)(kb / S) & 1u);
+    }
+  } else if (warp == mma_warp) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(E);
+      bool ok = true;
+      for (int kb = 0; kb < nk && ok; ++kb) {
+        const int s = kb % S;
+        const uint32_t ph = (uint32_t)(kb / S) & 1u;
+        ok = mbar_wait(smem_u32(&full[s]), ph);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(tiles + (size_t)s * p.stage_bytes);
+        const uint32_t sb = sa + p.a_bytes;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16(tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32), idesc,
+                   (kb > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&empty[s]));
+      }
+      mma_commit(smem_u32(accf));
+    }
+  } else if (FP4 && warp >= kEpiWarps + 2) {
+    // W decode warps: rows r = dt, dt + 128 of the E x 64 tile per k-step
+    const int dt = threadIdx.x - (kEpiWarps + 2) * 32;
+    const uint8_t* q = static_cast<const uint8_t*>(a.w);
+    const int Hb = a.H / 2, Hs = a.H / 16;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % S;
+      const uint32_t ph = (uint32_t)(kb / S) & 1u;
+      if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) break;
+      uint8_t* bt = tiles + (size_t)s * p.stage_bytes + p.a_bytes;
+      for (int r = dt; r < E; r += kDeqWarps * 32) {
+        const uint4* src = reinterpret_cast<const uint4*>(q + (size_t)r * Hb + kb * (BK / 2));
+        const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
+        const uint32_t sc = __ldg(reinterpret_cast<const uint32_t*>(a.w_scales + (size_t)r * Hs +
+                                                                     kb * (BK / 16)));
+        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c = elements 8c..8c+7
+          const float scale = e4m3_to_f32((sc >> (8 * (c >> 1))) & 0xffu);
+          uint32_t outw[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t byte = (qw[c] >> (8 * j)) & 0xffu;
+            const float lo = e2m1_to_f32(byte & 15u) * scale;
+            const float hi = e2m1_to_f32(byte >> 4) * scale;
+            outw[j] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xffff0000u);
+          }
+          const int phys = c ^ (r & 7);  // 128-byte swizzle: chunk index XOR row mod 8
+          *reinterpret_cast<uint4*>(bt + (size_t)r * 128 + phys * 16) =
+              make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(smem_u32(&full[s]));
+    }
+  } else if (warp < kEpiWarps) {
+    // epilogue: this thread's row of the accumulator
+    const int row = warp * 32 + lane;
+    const int m = m0 + row;
+    const bool ok = mbar_wait(smem_u32(accf), 0);
+    tc_fence_after();
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    const float g = FP4 ? a.w_global : 1.0f;
+    const int k = a.k;
+    const bool sp = a.act == ACT_SQRT_SOFTPLUS;
+    TopList<KC> top;
+    top.init();
+    float amax = 0.0f, kabs = 0.0f;
+    if (__all_sync(kFull, ok)) {
+      for (int c0 = 0; c0 < E; c0 += 32) {
+        float v[32];
+        tmem_ld32(trow + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int e = c0 + j;
+          if (e < E) {
+            const float z = FP4 ? v[j] * g : v[j];
+            float key = z;
+            if (sp) {
+              const float av = sqrt_softplus_f32(z);
+              key = a.bias ? av + __ldg(a.bias + e) : av;
+              amax = fmaxf(amax, av);
+              kabs = fmaxf(kabs, fabsf(key));
+            }
+            top.push(ord_of(key), e, z);
+          }
+        }
+      }
+      // FP64 guard-band refine (see select.cuh)
+      bool close = false;
+      double band = 0.0;
+      if (sp) {
+        const double err = 0x1p-23 * (2.25 * (double)amax + 0.5 * (double)kabs) + 0x1p-60;
+        band = 4.0 * err;
+        const int kk = min(k + 1, E);
+#pragma unroll
+        for (int j = 0; j + 1 < KC; ++j)
+          if (j + 1 < kk &&
+              (double)float_of_ord(top.o[j]) - (double)float_of_ord(top.o[j + 1]) <= band)
+            close = true;
+      }
+      if (__any_sync(kFull, close)) {
+        double thr = 0.0;
+#pragma unroll
+        for (int j = 0; j < KC; ++j)
+          if (j == k - 1) thr = (double)float_of_ord(top.o[j]) - band;
+        TopList64<KC> t64;
+        t64.init();
+        for (int c0 = 0; c0 < E; c0 += 32) {
+          float v[32];
+          tmem_ld32(trow + c0, v);
+          if (close) {
+            for (int j = 0; j < 32; ++j) {
+              const int e = c0 + j;
+              if (e < E) {
+                const float z = FP4 ? v[j] * g : v[j];
+                const float av = sqrt_softplus_f32(z);
+                const float key = a.bias ? av + __ldg(a.bias + e) : av;
+                if ((double)key >= thr)
+                  t64.push(sqrt_softplus_f64((double)z) + (a.bias ? (double)__ldg(a.bias + e) : 0.0),
+                           e, z);
+              }
+            }
+          }
+        }
+        if (close) {
+#pragma unroll
+          for (int j = 0; j < KC; ++j) {
+            top.i[j] = t64.i[j];
+            top.z[j] = t64.z[j];
+          }
+        }
+      }
+      if (m < a.M) {
+        float sv[KC];
+        float sum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < KC; ++j) {
+          sv[j] = sp ? sqrt_softplus_f32(top.z[j]) : expf(top.z[j] - top.z[0]);
+          if (j < k) sum += sv[j];
+        }
+#pragma unroll
+        for (int j = 0; j < KC; ++j) {
+          if (j < k) {
+            a.out_idx[(size_t)m * k + j] = top.i[j];
+            a.out_w[(size_t)m * k + j] = sum > 0.0f ? sv[j] / sum : 1.0f / (float)k;
+            if (a.tbl_unique) s_sel[row * kMaxK + j] = top.i[j];
+          }
+        }
+      }
+      if (a.logits) {  // telemetry tap; the loads are warp-collective, the stores per row
+        for (int c0 = 0; c0 < E; c0 += 32) {
+          float v[32];
+          tmem_ld32(trow + c0, v);
+          if (m < a.M)
+            for (int j = 0; j < 32 && c0 + j < E; ++j)
+              a.logits[(size_t)m * E + c0 + j] = FP4 ? v[j] * g : v[j];
+        }
+      }
+      if (a.tbl_unique) {
+        __syncwarp();
+        if ((lane & 1) == 0 && m + 1 < a.M) {
+          const size_t gi = (size_t)(m >> 1);
+          pair_table(s_sel + row * kMaxK, s_sel + (row + 1) * kMaxK, k,
+                     a.tbl_unique + gi * 2 * k, a.tbl_mask + gi * 2 * k, a.tbl_map + gi * 2 * k,
+                     a.tbl_count + gi);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == mma_warp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(p.tmem_cols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D BF16 tensor [rows, cols] row-major, box [box_rows, 64], 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KC, bool FP4>
+cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcParams& p,
+                      size_t smem, bool pdl, cudaStream_t stream) {
+  auto kern = k_tc_router<KC, FP4>;
+  static bool attr_done = false;  // per instantiation; idempotent if raced
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(227 * 1024));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.a.M + BM - 1) / BM);
+  cfg.blockDim = dim3((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, mx, mw, p);
+}
+
+template <bool FP4>
+cudaError_t dispatch_k(const CUtensorMap& mx, const CUtensorMap& mw, const TcParams& p,
+                       size_t smem, bool pdl, cudaStream_t s) {
+  const int k = p.a.k;
+  if (k <= 2) return launch_kc<3, FP4>(mx, mw, p, smem, pdl, s);
+  if (k <= 4) return launch_kc<5, FP4>(mx, mw, p, smem, pdl, s);
+  if (k <= 6) return launch_kc<7, FP4>(mx, mw, p, smem, pdl, s);
+  if (k <= 8) return launch_kc<9, FP4>(mx, mw, p, smem, pdl, s);
+  return launch_kc<17, FP4>(mx, mw, p, smem, pdl, s);
+}
+
+}  // namespace
+
+bool tc_eligible(int M, int H, int E, int k, int x_dtype, int w_dtype) {
+  return M >= 1 && x_dtype == DT_BF16 && (w_dtype == DT_BF16 || w_dtype == DT_NVFP4) &&
+         E % 16 == 0 && E >= 16 && E <= 256 && H % BK == 0 && k <= kMaxK;
+}
+
+cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
+  const bool fp4 = a.w_dtype == DT_NVFP4;
+  TcParams p{};
+  p.a = a;
+  p.a_bytes = BM * BK * 2;
+  p.b_bytes = (uint32_t)a.E * BK * 2;
+  p.stage_bytes = p.a_bytes + p.b_bytes;
+  const size_t extra = 1024 /*align*/ + 2 * 8 * 8 + 8 + 16 + BM * kMaxK * 4;
+  const size_t budget = 227 * 1024;
+  int S = (int)((budget - extra) / p.stage_bytes);
+  if (S > 6) S = 6;
+  if (S < 2) return cudaErrorInvalidValue;
+  p.stages = S;
+  int cols = 32;
+  while (cols < a.E) cols <<= 1;
+  p.tmem_cols = cols;
+  const size_t smem = (size_t)S * p.stage_bytes + extra;
+
+  CUtensorMap mx, mw;
+  if (!make_map(&mx, a.x, a.M, a.H, BM)) return cudaErrorInvalidValue;
+  if (fp4) {
+    mw = mx;  // unused: W tiles are decoded by the kernel
+  } else if (!make_map(&mw, a.w, a.E, a.H, a.E)) {
+    return cudaErrorInvalidValue;
+  }
+  return fp4 ? dispatch_k<true>(mx, mw, p, smem, pdl, stream)
+             : dispatch_k<false>(mx, mw, p, smem, pdl, stream);
+}
+
+int tc_read_status(int clear) {
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tc_status, sizeof v) != cudaSuccess) return -1;
+  if (clear) {
+    const unsigned z = 0;
+    if (cudaMemcpyToSymbol(g_tc_status, &z, sizeof z) != cudaSuccess) return -1;
+  }
+  return v ? 1 : 0;
+}
+
+}  // namespace gbr
