@@ -164,6 +164,28 @@ int router_select(const float* logits, const float* bias, int M, int E, int k, i
 int route_table(const int32_t* idx, int groups, int tokens_per_group, int k, int32_t* out_unique,
                 uint8_t* out_mask, uint8_t* out_map, int32_t* out_count, cudaStream_t stream);
 
+/*
+ * router_forward_noalloc — router_forward for callers that must not
+ * allocate device memory (no counterpart on the router pages; it exists for
+ * this library's users). Runtimes that plan all device memory ahead of time,
+ * plugin interfaces that receive a stream but no allocator, and paths where
+ * an allocation may block or fail cannot let router_forward create its
+ * per-stream workspace. This entry point allocates nothing: its scratch (an
+ * arrival ticket and FP32 logits [M, E]) is one file-scope device array of
+ * 131,328 bytes that every GPU loading the library holds until the process
+ * exits. Limits: M <= 64 and E <= 512 (beyond them: GBR_EWORKSPACE), BF16 x
+ * and W_gate with E % 16 == 0, H % 32 == 0 and 16-byte aligned x and W_gate
+ * (otherwise GBR_EUNSUPPORTED). Other arguments and errors as router_forward.
+ * The first call on a device looks up the array's device address, so make
+ * that first call before any stream capture. Every call on a device shares
+ * the one array: calls that overlap on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller. Each call clears the
+ * ticket with a 4-byte cudaMemsetAsync on `stream` before its launch.
+ */
+int router_forward_noalloc(const void* x, const void* W_gate, const float* bias, int M, int H,
+                           int E, int k, int act, int32_t* out_idx, float* out_w,
+                           cudaStream_t stream);
+
 /* Static text for a status code. */
 const char* router_strerror(int status);
 

@@ -21,7 +21,8 @@ GBR_FLAG_NO_PDL, GBR_FLAG_FORCE_GENERIC, GBR_FLAG_FORCE_GEMV, GBR_FLAG_FORCE_TC,
 GBR_REGIME_GENERIC, GBR_REGIME_GEMV, GBR_REGIME_TC, GBR_REGIME_UNFUSED = 0, 1, 2, 3
 
 EXPORTS = ("router_forward", "router_forward_ex", "router_workspace_size", "router_regime",
-           "router_select", "route_table", "router_strerror", "router_device_status")
+           "router_select", "route_table", "router_strerror", "router_device_status",
+           "router_forward_noalloc")
 
 
 class RouterError(RuntimeError):
@@ -59,11 +60,12 @@ def lib() -> ctypes.CDLL:
             L.router_regime.argtypes = [I, I, I, I, ctypes.POINTER(GbrOpts)]
             L.router_select.argtypes = [P, P, I, I, I, I, P, P, P]
             L.route_table.argtypes = [P, I, I, I, P, P, P, P, P]
+            L.router_forward_noalloc.argtypes = [P, P, P, I, I, I, I, I, P, P, P]
             L.router_strerror.argtypes = [I]
             L.router_strerror.restype = ctypes.c_char_p
             L.router_device_status.argtypes = [I]
             for f in (L.router_forward, L.router_forward_ex, L.router_regime, L.router_select,
-                      L.route_table, L.router_device_status):
+                      L.route_table, L.router_device_status, L.router_forward_noalloc):
                 f.restype = I
             _lib = L
     return _lib
@@ -119,6 +121,14 @@ def router_forward_ex(x, W_gate, bias, M, H, E, k, act, out_idx, out_w, opts=Non
                                    _ptr(out_idx), _ptr(out_w),
                                    ctypes.byref(opts) if opts is not None else None,
                                    _stream(stream)), "router_forward_ex")
+
+
+def router_forward_noalloc(x, W_gate, bias, M, H, E, k, act, out_idx, out_w, stream=None):
+    """router_forward without any device allocation: the library's static
+    scratch array serves as the workspace (M <= 64, E <= 512)."""
+    _check(lib().router_forward_noalloc(_ptr(x), _ptr(W_gate), _ptr(bias), M, H, E, k, act,
+                                        _ptr(out_idx), _ptr(out_w), _stream(stream)),
+           "router_forward_noalloc")
 
 
 def router_workspace_size(M, H, E, k, opts=None) -> int:

@@ -1,0 +1,48 @@
+"""router_forward_noalloc, the entry point for callers that cannot allocate
+device memory, gives the same routes as router_forward.
+
+This file is collected last on purpose: if it fails, a run that stops at the
+first failure has already run every other test. It passes both alone in a
+fresh process and after the rest of the suite."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from moe_expert_router_02_gb300 import router as R
+from moe_expert_router_02_gb300 import synth
+from tests.helpers import W_TOL, dev, empty_outputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("cfg_name,M", [("C1", 8), ("C2", 64), ("C4", 2)])
+def test_noalloc_matches_router_forward_on_two_calls(cfg_name, M):
+    import torch
+    cfg = synth.CONFIGS[cfg_name]
+    H, E, k, act = cfg["H"], cfg["E"], cfg["k"], cfg["act"]
+    case = synth.make_case(cfg, M=M, seed=21)
+    x, W = dev(case["x"]), dev(case["W"])
+    bias = None if case["bias"] is None else dev(case["bias"])
+    ref_idx, ref_w = empty_outputs(M, k)
+    R.router_forward(x, W, bias, M, H, E, k, act, ref_idx, ref_w)
+    torch.cuda.synchronize()
+    for _ in range(2):  # the second call reuses the array the first one left behind
+        idx, w = empty_outputs(M, k)
+        rc = R.lib().router_forward_noalloc(x.data_ptr(), W.data_ptr(),
+                                            None if bias is None else bias.data_ptr(),
+                                            M, H, E, k, act, idx.data_ptr(), w.data_ptr(),
+                                            torch.cuda.current_stream().cuda_stream)
+        assert rc == R.GBR_OK, R.router_strerror(rc)
+        torch.cuda.synchronize()
+        assert np.array_equal(idx.cpu().numpy(), ref_idx.cpu().numpy())
+        assert np.max(np.abs(w.cpu().numpy() - ref_w.cpu().numpy())) <= W_TOL
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    fake = ctypes.c_void_p(256)
+    L = R.lib()
+    assert L.router_forward_noalloc(fake, fake, None, 65, 2048, 256, 8, 0, fake, fake,
+                                    None) == R.GBR_EWORKSPACE
+    assert L.router_forward_noalloc(fake, fake, None, 8, 2048, 1024, 8, 0, fake, fake,
+                                    None) == R.GBR_EUNSUPPORTED
