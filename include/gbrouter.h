@@ -77,11 +77,18 @@ enum {
   GBR_FLAG_FORCE_GENERIC = 2, /* use the generic row-per-CTA kernel (A/B and tests) */
   GBR_FLAG_FORCE_GEMV = 4,    /* use the small-M tensor-core GEMV kernel when eligible */
   GBR_FLAG_FORCE_TC = 8,      /* use the tcgen05 prefill kernel when eligible */
-  GBR_FLAG_UNFUSED = 16       /* two launches: gate logits, then router_select (A/B only) */
+  GBR_FLAG_UNFUSED = 16,      /* two launches: gate logits, then router_select (A/B only) */
+  GBR_FLAG_NO_SINGLE_CLUSTER = 32 /* small M: skip the single-cluster kernel (A/B only) */
 };
 
 /* kernel families reported by router_regime() */
-enum { GBR_REGIME_GENERIC = 0, GBR_REGIME_GEMV = 1, GBR_REGIME_TC = 2, GBR_REGIME_UNFUSED = 3 };
+enum {
+  GBR_REGIME_GENERIC = 0, /* one CTA per row, any dtype and shape */
+  GBR_REGIME_GEMV = 1,    /* M <= 64: clusters split H, last cluster selects */
+  GBR_REGIME_TC = 2,      /* M > 64: tcgen05 GEMM with the selection in its epilogue */
+  GBR_REGIME_UNFUSED = 3, /* logits kernel + router_select (A/B baseline) */
+  GBR_REGIME_GEMV1C = 4   /* M <= 16, E <= 256: one cluster holds W_gate in shared memory */
+};
 
 typedef struct {
   int x_dtype;                /* GBR_F32 or GBR_BF16 (default for router_forward: BF16) */

@@ -46,15 +46,19 @@ int regime_of(const Shape& s) {
   const bool gv = gemv_eligible(s);
   if (f & GBR_FLAG_UNFUSED) return gv ? GBR_REGIME_UNFUSED : GBR_REGIME_GENERIC;
   if ((f & GBR_FLAG_FORCE_TC) && tc) return GBR_REGIME_TC;
-  if ((f & GBR_FLAG_FORCE_GEMV) && gv) return GBR_REGIME_GEMV;
-  if (gv) return GBR_REGIME_GEMV;
+  const bool one_cluster = gv && !(f & GBR_FLAG_NO_SINGLE_CLUSTER) &&
+                           gbr::gemv1c_eligible(s.M, s.H, s.E);
+  if ((f & GBR_FLAG_FORCE_GEMV) && gv) return one_cluster ? GBR_REGIME_GEMV1C : GBR_REGIME_GEMV;
+  if (gv) return one_cluster ? GBR_REGIME_GEMV1C : GBR_REGIME_GEMV;
   if (tc && s.M > 64) return GBR_REGIME_TC;
   return GBR_REGIME_GENERIC;
 }
 
 size_t workspace_for(const Shape& s, int regime) {
-  // ticket in the first 256 bytes, FP32 logits [M, E] after it
-  if (regime == GBR_REGIME_GEMV || regime == GBR_REGIME_UNFUSED)
+  // ticket in the first 256 bytes, FP32 logits [M, E] after it. The
+  // single-cluster kernel needs none, but reports the same size so that a
+  // workspace sized on one device also fits a device where it is not chosen.
+  if (regime == GBR_REGIME_GEMV || regime == GBR_REGIME_GEMV1C || regime == GBR_REGIME_UNFUSED)
     return kTicketBytes + round_up((size_t)s.M * s.E * 4, 256);
   return 0;
 }
@@ -146,7 +150,8 @@ int router_forward_ex(const void* x, const void* W_gate, const float* bias, int 
   if (!x || !W_gate || !out_idx || !out_w) return GBR_EINVAL;
 
   int regime = regime_of(s);
-  if ((regime == GBR_REGIME_GEMV || regime == GBR_REGIME_UNFUSED || regime == GBR_REGIME_TC) &&
+  if ((regime == GBR_REGIME_GEMV || regime == GBR_REGIME_GEMV1C || regime == GBR_REGIME_UNFUSED ||
+       regime == GBR_REGIME_TC) &&
       (!aligned16(x) || !aligned16(W_gate) || H % 8 != 0 ||
        (s.w_dtype == GBR_NVFP4 && !aligned16(opt->w_scales))))
     regime = GBR_REGIME_GENERIC;
@@ -169,6 +174,7 @@ int router_forward_ex(const void* x, const void* W_gate, const float* bias, int 
     a.tbl_count = opt->tbl_count;
   }
   const bool pdl = !(s.flags & GBR_FLAG_NO_PDL);
+  a.status = gbr::status_word();
 
   const size_t need = workspace_for(s, regime);
   void* ws = nullptr;
@@ -188,6 +194,9 @@ int router_forward_ex(const void* x, const void* W_gate, const float* bias, int 
       a.ticket = static_cast<uint32_t*>(ws);
       if (!a.logits) a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + kTicketBytes);
       err = gbr::launch_gemv(a, true, pdl, stream);
+      break;
+    case GBR_REGIME_GEMV1C:
+      err = gbr::launch_gemv1c(a, pdl, stream);
       break;
     case GBR_REGIME_UNFUSED: {
       if (!a.logits) a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + kTicketBytes);

@@ -23,6 +23,10 @@
 // chip and in L2 instead of a separate launch.
 #include <cuda_bf16.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "kernels.h"
 #include "select.cuh"
 
@@ -58,6 +62,19 @@ __device__ __forceinline__ void dsmem_st_u32(uint32_t* p, uint32_t rank, uint32_
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(r), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void atom_exch_relaxed_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.exch.relaxed.gpu.global.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
 }
 
 // K permutation inside a 32-element chunk: thread t of a quad owns the 8
@@ -164,17 +181,19 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
     cluster_sync_all();  // keep shared memory alive until every peer has read it
     return;
   }
-  __threadfence();
+  // The cluster barrier (release/acquire) orders every peer's logits stores
+  // before rank 0's acq_rel arrival on the ticket; the arrivals form one
+  // release sequence, so the cluster that arrives last observes all logits
+  // and hands them to its peers through the next cluster barrier.
   cluster_sync_all();
   if (rank == 0 && tid == 0) {
-    const uint32_t old = atomicAdd(a.ticket, 1u);
+    const uint32_t old = atom_add_acq_rel_gpu(a.ticket, 1u);
     const uint32_t last = (old == gridDim.y - 1) ? 1u : 0u;
-    if (last) atomicExch(a.ticket, 0u);
+    if (last) atom_exch_relaxed_gpu(a.ticket, 0u);
     for (int q = 0; q < CL; ++q) dsmem_st_u32(&s_flag, (uint32_t)q, last);
   }
   cluster_sync_all();
   if (!s_flag) return;
-  __threadfence();
 
   // the last cluster selects: row = base + warp, rows 2p and 2p+1 share a CTA
   const bool table = a.tbl_unique != nullptr;
@@ -183,6 +202,175 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
     const int row = base + warp;
     if (row < M)
       warp_select_row<VPL>(LdCG{a.logits + (size_t)row * E}, a.bias, E, k, a.act,
+                           a.out_idx + (size_t)row * k, a.out_w + (size_t)row * k,
+                           s_sel + warp * k);
+    if (table) {
+      __syncthreads();
+      if ((warp & 1) == 0 && row + 1 < M) {
+        const size_t gi = (size_t)(row >> 1);
+        warp_route_table(s_sel + warp * k, s_rank[warp], 2, k, a.tbl_unique + gi * 2 * k,
+                         a.tbl_mask + gi * 2 * k, a.tbl_map + gi * 2 * k, a.tbl_count + gi);
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Single-cluster small-M router (M <= 16, E <= 256). One cluster of E/16
+// CTAs holds all of W_gate in shared memory: CTA r owns experts
+// [16r, 16r+16) over the whole H, so there are no partial sums to combine
+// and no logits leave the cluster. Each CTA starts bulk copies of its 16 W
+// rows before it waits on the preceding kernel (programmatic dependent
+// launch), then reads x, runs the mma.sync contraction from shared memory,
+// and publishes its 16 x M logits in shared memory. After one cluster
+// barrier, one warp per row gathers the row's E logits from the cluster's
+// CTAs through distributed shared memory and selects. No global scratch,
+// no atomics, no memory fences.
+
+constexpr int k1cWarps = 16;
+constexpr int k1cBatch = 8;  // 32-element chunks of x held in registers per warp
+constexpr int kMaxE1c = 256;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_parity(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait (about one second of %globaltimer); false when it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned* status) {
+  if (mbar_try_parity(bar, parity)) return true;
+  uint64_t t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (!mbar_try_parity(bar, parity)) {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > 1000000000ull) {
+      if (status) atomicOr(status, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void dsmem_st_f32(float* p, uint32_t rank, float v) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(r), "f"(v) : "memory");
+}
+
+template <int NT, int VPL>
+__global__ void __launch_bounds__(k1cWarps * 32) k_gemv1c_router(const RouterArgs a, int pitch) {
+  constexpr int NTOK = 8 * NT;
+  extern __shared__ __align__(128) uint8_t s_w[];  // [16][pitch bytes]: this CTA's W rows
+  __shared__ float s_part[k1cWarps][16][NTOK];
+  __shared__ float s_all[NTOK][kMaxE1c];  // CTA 0: every expert's logit, row by row
+  __shared__ int32_t s_sel[k1cWarps * kMaxK];
+  __shared__ int32_t s_rank[k1cWarps][32];
+  __shared__ __align__(8) uint64_t s_bar;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int rank = blockIdx.x;  // one cluster spans the grid
+  const int e0 = rank * 16;
+  const int H = a.H, M = a.M, E = a.E;
+  const uint32_t bar = smem_u32(&s_bar);
+  const uint32_t wsm = smem_u32(s_w);
+
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"((uint32_t)(16 * H * 2))
+                 : "memory");
+  }
+  __syncthreads();
+  if (tid < 16) {  // this CTA's 16 W rows, one bulk copy per row into the padded pitch
+    const uint16_t* w = static_cast<const uint16_t*>(a.w) + (size_t)(e0 + tid) * H;
+    bulk_g2s(wsm + tid * pitch, w, H * 2, bar);
+  }
+  pdl_launch_dependents();
+  pdl_wait();  // x and the outputs belong to the preceding kernel until here
+
+  const uint16_t* __restrict__ x = static_cast<const uint16_t*>(a.x);
+  const int nchunk = H / 32;
+  const int cpw = warp < nchunk ? (nchunk - warp + k1cWarps - 1) / k1cWarps : 0;
+  float acc[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+  const uint8_t* w0 = s_w + g * pitch + 16 * t;
+  const uint8_t* w1 = w0 + 8 * pitch;
+  bool w_ok = true;
+  for (int jb = 0; jb < cpw; jb += k1cBatch) {
+    uint4 xv[k1cBatch][NT];
+#pragma unroll
+    for (int i = 0; i < k1cBatch; ++i) {
+      const int hoff = (warp + k1cWarps * (jb + i)) * 32 + 8 * t;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const int tok = n * 8 + g;
+        xv[i][n] = make_uint4(0u, 0u, 0u, 0u);
+        if (jb + i < cpw && tok < M)
+          xv[i][n] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + hoff));
+      }
+    }
+    if (jb == 0) w_ok = mbar_wait_bounded(bar, 0, a.status);  // x loads are in flight meanwhile
+#pragma unroll
+    for (int i = 0; i < k1cBatch; ++i) {
+      if (jb + i < cpw && w_ok) {
+        const int c = warp + k1cWarps * (jb + i);
+        const uint4 wa = *reinterpret_cast<const uint4*>(w0 + c * 64);
+        const uint4 wb = *reinterpret_cast<const uint4*>(w1 + c * 64);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          mma_bf16_16816(acc[n], wa.x, wb.x, wa.y, wb.y, xv[i][n].x, xv[i][n].y);
+          mma_bf16_16816(acc[n], wa.z, wb.z, wa.w, wb.w, xv[i][n].z, xv[i][n].w);
+        }
+      }
+    }
+  }
+  if (cpw == 0) mbar_wait_bounded(bar, 0, a.status);  // never leave with copies in flight
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    s_part[warp][g][n * 8 + 2 * t] = acc[n][0];
+    s_part[warp][g][n * 8 + 2 * t + 1] = acc[n][1];
+    s_part[warp][g + 8][n * 8 + 2 * t] = acc[n][2];
+    s_part[warp][g + 8][n * 8 + 2 * t + 1] = acc[n][3];
+  }
+  __syncthreads();
+  // sum the warps' partials in a fixed order and push them into CTA 0
+  for (int i = tid; i < 16 * M; i += k1cWarps * 32) {
+    const int m = i >> 4, el = i & 15;
+    float v = s_part[0][el][m];
+#pragma unroll
+    for (int w = 1; w < k1cWarps; ++w) v += s_part[w][el][m];
+    dsmem_st_f32(&s_all[m][e0 + el], 0u, v);
+    if (a.logits) a.logits[(size_t)m * E + e0 + el] = v;
+  }
+  cluster_sync_all();  // every logit is in CTA 0; no shared memory is read remotely after this
+  if (rank != 0) return;
+
+  const bool table = a.tbl_unique != nullptr;
+  const int k = a.k;
+  for (int base = 0; base < M; base += k1cWarps) {
+    const int row = base + warp;
+    if (row < M)
+      warp_select_row<VPL>(LdPlain{&s_all[row][0]}, a.bias, E, k, a.act,
                            a.out_idx + (size_t)row * k, a.out_w + (size_t)row * k,
                            s_sel + warp * k);
     if (table) {
@@ -299,7 +487,83 @@ cudaError_t gemv_dispatch(const RouterArgs& a, int CL, bool pdl, cudaStream_t s)
   return gemv_dispatch_vpl<8, SELECT>(a, CL, pdl, s);
 }
 
+int gemv1c_pitch(int H) { return 2 * H + ((2 * H) % 128 == 0 ? 64 : 0); }
+
+// Launches (or, with probe, only sizes) the single-cluster kernel.
+template <int NT, int VPL>
+cudaError_t launch_1c_inst(const RouterArgs& a, bool pdl, cudaStream_t stream, bool probe,
+                           bool* fits) {
+  auto kern = k_gemv1c_router<NT, VPL>;
+  const int CL = a.E / 16;
+  const int pitch = gemv1c_pitch(a.H);
+  const size_t dsmem = (size_t)16 * pitch;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)dsmem);
+  if (e != cudaSuccess) return e;
+  if (CL > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL);
+  cfg.blockDim = dim3(k1cWarps * 32);
+  cfg.dynamicSmemBytes = dsmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = CL;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = pdl ? 2 : 1;
+  if (probe) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    *fits = (e == cudaSuccess && n > 0);
+    return cudaSuccess;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, a, pitch);
+}
+
+template <int NT>
+cudaError_t launch_1c_vpl(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe, bool* fits) {
+  if (a.E <= 128) return launch_1c_inst<NT, 4>(a, pdl, s, probe, fits);
+  return launch_1c_inst<NT, 8>(a, pdl, s, probe, fits);
+}
+
+cudaError_t launch_1c(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe, bool* fits) {
+  if (a.M <= 8) return launch_1c_vpl<1>(a, pdl, s, probe, fits);
+  return launch_1c_vpl<2>(a, pdl, s, probe, fits);
+}
+
 }  // namespace
+
+bool gemv1c_eligible(int M, int H, int E) {
+  if (M < 1 || M > 16 || E % 16 != 0 || E < 16 || E > 256 || H % 32 != 0) return false;
+  if ((size_t)16 * gemv1c_pitch(H) > (size_t)200 * 1024) return false;
+  // the cluster must be schedulable with this much shared memory per CTA
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int>, bool> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const auto key = std::make_tuple(dev, M <= 8 ? 1 : 2, E, gemv1c_pitch(H));
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  RouterArgs probe_args{};
+  probe_args.M = M, probe_args.H = H, probe_args.E = E;
+  bool fits = false;
+  if (launch_1c(probe_args, true, 0, true, &fits) != cudaSuccess) fits = false;
+  cache[key] = fits;
+  return fits;
+}
+
+cudaError_t launch_gemv1c(const RouterArgs& a, bool pdl, cudaStream_t stream) {
+  bool unused = false;
+  return launch_1c(a, pdl, stream, false, &unused);
+}
 
 int gemv_cluster_size(int H) {
   for (int cl = 8; cl > 1; cl >>= 1)

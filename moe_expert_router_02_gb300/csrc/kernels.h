@@ -18,6 +18,10 @@ cudaError_t launch_route_table(const int32_t* idx, int groups, int T, int k, int
 int gemv_cluster_size(int H);
 cudaError_t launch_gemv(const RouterArgs& a, bool select, bool pdl, cudaStream_t stream);
 
+// Small-M single-cluster router (M <= 16, E <= 256, W_gate in shared memory).
+bool gemv1c_eligible(int M, int H, int E);
+cudaError_t launch_gemv1c(const RouterArgs& a, bool pdl, cudaStream_t stream);
+
 // Row-per-CTA router for any dtype and shape.
 cudaError_t launch_generic(const RouterArgs& a, bool pdl, cudaStream_t stream);
 
@@ -25,5 +29,6 @@ cudaError_t launch_generic(const RouterArgs& a, bool pdl, cudaStream_t stream);
 bool tc_eligible(int M, int H, int E, int k, int x_dtype, int w_dtype);
 cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream);
 int tc_read_status(int clear);  // 0 ok, 1 a bounded wait expired, -1 query failed
+unsigned* status_word();        // device address of that status word (current device)
 
 }  // namespace gbr

@@ -38,63 +38,85 @@ struct LdCG {  // global loads that bypass L1 (data written by other CTAs)
 // One warp selects the top-k of one row of E <= 32*VPL logits.
 // Lane r < k writes slot r of out_idx / out_w and, if sel_out is not null,
 // sel_out[r] (for a route table). All 32 lanes must call.
+//
+// Each lane holds the order-preserving keys of experts lane, lane+32, ...
+// and caches its own best; a round takes the warp maximum key (redux.sync),
+// then the lowest index among the lanes holding it (redux.sync), and only
+// the winning lane rescans its entries. The winner's score (logit or
+// unbiased activation) travels by shuffle, so the weights need no second
+// pass over the logits.
 template <int VPL, class Ld>
 __device__ __noinline__ void warp_select_row(const Ld ld, const float* __restrict__ bias, int E,
                                              int k, int act, int32_t* __restrict__ out_idx,
                                              float* __restrict__ out_w, int32_t* sel_out) {
   const int lane = threadIdx.x & 31;
-  float key[VPL];
-  uint32_t valid = 0;
+  uint32_t ok[VPL];  // order-preserving key, 0 = empty or taken (finite keys map above 0)
+  float sc[VPL];     // the score the weights use: logit (softmax) or unbiased activation
   float amax = 0.0f, kabs = 0.0f;
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
     const int e = lane + 32 * j;
-    key[j] = 0.0f;
+    ok[j] = 0u;
+    sc[j] = 0.0f;
     if (e < E) {
-      valid |= 1u << j;
       const float z = ld(e);
       if (act == ACT_SOFTMAX) {
-        key[j] = z;
+        ok[j] = ord_of(z);
+        sc[j] = z;
       } else {
         const float a = sqrt_softplus_f32(z);
         const float kv = bias ? a + __ldg(bias + e) : a;
-        key[j] = kv;
+        ok[j] = ord_of(kv);
+        sc[j] = a;
         amax = fmaxf(amax, a);
         kabs = fmaxf(kabs, fabsf(kv));
       }
     }
   }
-
-  // k+1 rounds of warp arg-best: the (k+1)-th key is kept for the gap test.
-  const int kk = min(k + 1, E);
-  uint32_t taken = 0;
-  int sel_idx = -1;
-  float sel_key = 0.0f;
-  for (int r = 0; r < kk; ++r) {
-    uint32_t bo = 0;
-    int bj = -1;
+  uint32_t bo = 0u;  // this lane's best key, its slot and score
+  int bj = 0;
+  float bs = 0.0f;
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      if (((valid & ~taken) >> j) & 1u) {
-        const uint32_t o = ord_of(key[j]);
-        if (bj < 0 || o > bo) {  // strict: the lower index wins inside a lane
-          bo = o;
-          bj = j;
-        }
-      }
+  for (int j = 0; j < VPL; ++j)
+    if (ok[j] > bo) {  // strict: the lower index wins inside a lane
+      bo = ok[j];
+      bj = j;
+      bs = sc[j];
     }
-    const uint32_t wbest = __reduce_max_sync(kFull, bj >= 0 ? bo : 0u);
-    const uint32_t cand = (bj >= 0 && bo == wbest) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+
+  // k+1 rounds: the (k+1)-th key is kept for the gap test.
+  const int kk = min(k + 1, E);
+  int sel_idx = -1;
+  float sel_key = 0.0f, sel_sc = 0.0f;
+  for (int r = 0; r < kk; ++r) {
+    const uint32_t wbest = __reduce_max_sync(kFull, bo);
+    const uint32_t cand = (bo == wbest) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
     const uint32_t widx = __reduce_min_sync(kFull, cand);  // lowest index among equal keys
-    if ((int)(widx & 31u) == lane) taken |= 1u << (widx >> 5);
+    const int wl = (int)(widx & 31u);
+    const float wsc = __shfl_sync(kFull, bs, wl);
     if (lane == r) {
       sel_idx = (int)widx;
       sel_key = float_of_ord(wbest);
+      sel_sc = wsc;
+    }
+    if (lane == wl) {
+      const int tj = (int)(widx >> 5);
+      bo = 0u;
+      bj = 0;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        if (j == tj) ok[j] = 0u;
+        if (ok[j] > bo) {
+          bo = ok[j];
+          bj = j;
+          bs = sc[j];
+        }
+      }
     }
   }
 
   if (act == ACT_SQRT_SOFTPLUS) {
-    // non-negative floats order like their bit patterns
+    // FP32 key error bound; non-negative floats order like their bit patterns
     const float amax_w = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(amax)));
     const float kabs_w = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(kabs)));
     const double err = 0x1p-23 * (2.25 * (double)amax_w + 0.5 * (double)kabs_w) + 0x1p-60;
@@ -102,6 +124,7 @@ __device__ __noinline__ void warp_select_row(const Ld ld, const float* __restric
     const float next_key = __shfl_down_sync(kFull, sel_key, 1);
     const bool close = (lane < kk - 1) && ((double)sel_key - (double)next_key <= band);
     if (__any_sync(kFull, close)) {
+      // re-rank every expert whose FP32 key lies within the band of the k-th
       const double thr = (double)__shfl_sync(kFull, sel_key, k - 1) - band;
       double k64[VPL];
       uint32_t cmask = 0;
@@ -109,45 +132,55 @@ __device__ __noinline__ void warp_select_row(const Ld ld, const float* __restric
       for (int j = 0; j < VPL; ++j) {
         k64[j] = 0.0;
         const int e = lane + 32 * j;
-        if (((valid >> j) & 1u) && (double)key[j] >= thr) {
-          cmask |= 1u << j;
-          k64[j] = sqrt_softplus_f64((double)ld(e)) + (bias ? (double)__ldg(bias + e) : 0.0);
+        if (e < E) {
+          const float z = ld(e);
+          const float a = sqrt_softplus_f32(z);
+          const float kv = bias ? a + __ldg(bias + e) : a;
+          if ((double)kv >= thr) {
+            cmask |= 1u << j;
+            k64[j] = sqrt_softplus_f64((double)z) + (bias ? (double)__ldg(bias + e) : 0.0);
+          }
         }
       }
       for (int r = 0; r < k; ++r) {
         double bv = -INFINITY;
         int bidx = 0x7fffffff;
+        float bsc = 0.0f;
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
           if (((cmask >> j) & 1u) && (bidx == 0x7fffffff || k64[j] > bv)) {
             bv = k64[j];
             bidx = lane + 32 * j;
+            bsc = sc[j];
           }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
           const double ov = __shfl_xor_sync(kFull, bv, off);
           const int oi = __shfl_xor_sync(kFull, bidx, off);
+          const float os = __shfl_xor_sync(kFull, bsc, off);
           if (ov > bv || (ov == bv && oi < bidx)) {
             bv = ov;
             bidx = oi;
+            bsc = os;
           }
         }
         if ((bidx & 31) == lane) cmask &= ~(1u << (bidx >> 5));
-        if (lane == r) sel_idx = bidx;
+        if (lane == r) {
+          sel_idx = bidx;
+          sel_sc = bsc;
+        }
       }
     }
   }
 
   // weights over the chosen k, summed in slot order
   float s = 0.0f;
-  if (lane < k) {
-    const float z = ld(sel_idx);
-    s = (act == ACT_SOFTMAX) ? z : sqrt_softplus_f32(z);
-  }
   if (act == ACT_SOFTMAX) {
-    const float z0 = __shfl_sync(kFull, s, 0);
-    if (lane < k) s = expf(s - z0);
+    const float z0 = __shfl_sync(kFull, sel_sc, 0);
+    if (lane < k) s = expf(sel_sc - z0);
+  } else if (lane < k) {
+    s = sel_sc;
   }
   float sum = 0.0f;
   for (int r = 0; r < k; ++r) sum += __shfl_sync(kFull, s, r);

@@ -23,6 +23,7 @@
 // %globaltimer, records GBR_ETIMEOUT in a device status word and lets the
 // CTA unwind (free tensor memory, return) instead of hanging.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -37,7 +38,7 @@ static __device__ unsigned g_tc_status = 0;
 
 constexpr int BM = 128;   // token rows per CTA (= MMA M, = TMEM lanes)
 constexpr int BK = 64;    // BF16 elements per k-step (one 128-byte swizzle atom)
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, each half of the columns
 constexpr int kDeqWarps = 4;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -69,6 +70,29 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for a whole warp: lane 0 polls with a growing sleep so the
+// waiting warp leaves the issue slots to the TMA and MMA threads, then the
+// warp synchronises. All lanes get the result.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
+  uint32_t ok = 1;
+  if ((threadIdx.x & 31) == 0 && !mbar_try(bar, parity)) {
+    const uint64_t t0 = globaltimer();
+    uint32_t ns = 32;
+    while (!mbar_try(bar, parity)) {
+      __nanosleep(ns);
+      if (ns < 512) ns <<= 1;
+      if (globaltimer() - t0 > kWaitNs) {
+        atomicOr(&g_tc_status, 1u);
+        ok = 0;
+        break;
+      }
+    }
+  }
+  ok = __shfl_sync(kFull, ok, 0);
+  __syncwarp();  // orders lane 0's observation of the phase before the other lanes' accesses
   return ok != 0;
 }
 
@@ -171,13 +195,18 @@ struct TopList {
   __device__ __forceinline__ void push(uint32_t ok, int idx, float zz) {
     if (ok <= o[KC - 1]) return;
 #pragma unroll
-    for (int j = KC - 1; j >= 0; --j) {
-      const bool up = (j > 0) && (ok > o[j - 1]);
+    for (int j = KC - 1; j > 0; --j) {
       if (ok > o[j]) {
+        const bool up = ok > o[j - 1];
         o[j] = up ? o[j - 1] : ok;
         i[j] = up ? i[j - 1] : idx;
         z[j] = up ? z[j - 1] : zz;
       }
+    }
+    if (ok > o[0]) {
+      o[0] = ok;
+      i[0] = idx;
+      z[0] = zz;
     }
   }
 };
@@ -198,16 +227,57 @@ struct TopList64 {
   __device__ __forceinline__ void push(double kv, int idx, float zz) {
     if (!(kv > v[KC - 1])) return;
 #pragma unroll
-    for (int j = KC - 1; j >= 0; --j) {
-      const bool up = (j > 0) && (kv > v[j - 1]);
+    for (int j = KC - 1; j > 0; --j) {
       if (kv > v[j]) {
+        const bool up = kv > v[j - 1];
         v[j] = up ? v[j - 1] : kv;
         i[j] = up ? i[j - 1] : idx;
         z[j] = up ? z[j - 1] : zz;
       }
     }
+    if (kv > v[0]) {
+      v[0] = kv;
+      i[0] = idx;
+      z[0] = zz;
+    }
   }
 };
+
+// FP64 re-ranking of one row (see select.cuh): every lane of the warp calls
+// it (the TMEM loads are warp-collective); lanes with close == false only
+// take part in the loads. Kept out of line so the common path's top list
+// stays in registers.
+template <int KC, bool FP4>
+__device__ __noinline__ void refine_row(uint32_t trow, int E, float g, const float* bias,
+                                        double thr, bool close, int* out_i, float* out_z) {
+  // out_i / out_z: KC entries, BM apart (shared memory)
+  TopList64<KC> t64;
+  t64.init();
+  for (int c0 = 0; c0 < E; c0 += 32) {
+    float v[32];
+    tmem_ld32(trow + c0, v);
+    if (close) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int e = c0 + j;
+        if (e < E) {
+          const float z = FP4 ? v[j] * g : v[j];
+          const float av = sqrt_softplus_f32(z);
+          const float key = bias ? av + __ldg(bias + e) : av;
+          if ((double)key >= thr)
+            t64.push(sqrt_softplus_f64((double)z) + (bias ? (double)__ldg(bias + e) : 0.0), e, z);
+        }
+      }
+    }
+  }
+  if (close) {
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      out_i[j * BM] = t64.i[j];
+      out_z[j * BM] = t64.z[j];
+    }
+  }
+}
 
 struct TcParams {
   RouterArgs a;
@@ -217,28 +287,36 @@ struct TcParams {
 };
 
 // Serial unique-route table for one pair of rows (the thread owning the
-// even row of the pair builds it from ids in shared memory).
+// even row of the pair builds it from ids in shared memory). The running
+// table lives in the output arrays themselves, which only this thread
+// touches, so no per-thread array is needed.
 __device__ void pair_table(const int32_t* r0, const int32_t* r1, int k, int32_t* unique,
                            uint8_t* mask, uint8_t* map, int32_t* count) {
-  int32_t uq[2 * kMaxK];
-  uint32_t mk[2 * kMaxK];
   int n = 0;
   for (int p = 0; p < 2 * k; ++p) {
-    const int t = p / k;
+    const int t = p >= k ? 1 : 0;
     const int32_t v = t ? r1[p - k] : r0[p];
-    int u = 0;
-    while (u < n && uq[u] != v) ++u;
-    if (u == n) {
-      uq[n] = v;
-      mk[n] = 0;
-      ++n;
+    int f = p;
+    for (int q = 0; q < p; ++q) {
+      if ((q >= k ? r1[q - k] : r0[q]) == v) {
+        f = q;
+        break;
+      }
     }
-    mk[u] |= 1u << t;
-    map[p] = (uint8_t)u;
+    if (f == p) {
+      unique[n] = v;
+      mask[n] = (uint8_t)(1u << t);
+      map[p] = (uint8_t)n;
+      ++n;
+    } else {
+      const int u = map[f];
+      map[p] = (uint8_t)u;
+      mask[u] = (uint8_t)(mask[u] | (1u << t));
+    }
   }
-  for (int u = 0; u < 2 * k; ++u) {
-    unique[u] = u < n ? uq[u] : -1;
-    mask[u] = u < n ? (uint8_t)mk[u] : 0;
+  for (int u = n; u < 2 * k; ++u) {
+    unique[u] = -1;
+    mask[u] = 0;
   }
   *count = n;
 }
@@ -248,6 +326,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
     k_tc_router(const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_w, const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint32_t s_lut[256];  // NVFP4: byte of two E2M1 codes -> two BF16 values
   const RouterArgs& a = p.a;
   const int S = p.stages;
   // 1024-byte aligned tile ring, then barriers
@@ -291,7 +370,9 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
   if (warp == producer_warp) {
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+      if (!FP4)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w))
+                     : "memory");
       pdl_wait();
       int issued = 0;
       for (int kb = 0; kb < nk; ++kb) {
@@ -312,12 +393,10 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
   } else if (warp == mma_warp) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(E);
-      bool ok = true;
-      for (int kb = 0; kb < nk && ok; ++kb) {
+      for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % S;
         const uint32_t ph = (uint32_t)(kb / S) & 1u;
-        ok = mbar_wait(smem_u32(&full[s]), ph);
-        if (!ok) break;
+        if (!mbar_wait(smem_u32(&full[s]), ph)) break;
         tc_fence_after();
         const uint32_t sa = smem_u32(tiles + (size_t)s * p.stage_bytes);
         const uint32_t sb = sa + p.a_bytes;
@@ -330,14 +409,20 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
       mma_commit(smem_u32(accf));
     }
   } else if (FP4 && warp >= kEpiWarps + 2) {
-    // W decode warps: rows r = dt, dt + 128 of the E x 64 tile per k-step
+    // W decode warps: E x 64 BF16 tile per k-step, rows dt and dt + 128.
     const int dt = threadIdx.x - (kEpiWarps + 2) * 32;
+    for (int b = dt; b < 256; b += kDeqWarps * 32) {
+      const uint32_t lo = __float_as_uint(e2m1_to_f32(b & 15u)) >> 16;
+      const uint32_t hi = __float_as_uint(e2m1_to_f32((uint32_t)b >> 4)) >> 16;
+      s_lut[b] = lo | (hi << 16);
+    }
+    asm volatile("bar.sync 2, %0;" ::"r"(kDeqWarps * 32) : "memory");
     const uint8_t* q = static_cast<const uint8_t*>(a.w);
     const int Hb = a.H / 2, Hs = a.H / 16;
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % S;
       const uint32_t ph = (uint32_t)(kb / S) & 1u;
-      if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) break;
+      if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1u)) break;
       uint8_t* bt = tiles + (size_t)s * p.stage_bytes + p.a_bytes;
       for (int r = dt; r < E; r += kDeqWarps * 32) {
         const uint4* src = reinterpret_cast<const uint4*>(q + (size_t)r * Hb + kb * (BK / 2));
@@ -347,14 +432,17 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
         const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
         for (int c = 0; c < 8; ++c) {  // 16-byte chunk c = elements 8c..8c+7
-          const float scale = e4m3_to_f32((sc >> (8 * (c >> 1))) & 0xffu);
+          // the scale in BF16 (exact: at most 4 significant bits), twice
+          const uint32_t sb16 = __float_as_uint(e4m3_to_f32((sc >> (8 * (c >> 1))) & 0xffu)) >> 16;
+          const __nv_bfloat162 scale2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)sb16),
+                                                           __ushort_as_bfloat16((unsigned short)sb16));
           uint32_t outw[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint32_t byte = (qw[c] >> (8 * j)) & 0xffu;
-            const float lo = e2m1_to_f32(byte & 15u) * scale;
-            const float hi = e2m1_to_f32(byte >> 4) * scale;
-            outw[j] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xffff0000u);
+            const uint32_t pair = s_lut[(qw[c] >> (8 * j)) & 0xffu];
+            __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pair);
+            v = __hmul2(v, scale2);  // exact: the product has at most 6 significant bits
+            outw[j] = *reinterpret_cast<const uint32_t*>(&v);
           }
           const int phys = c ^ (r & 7);  // 128-byte swizzle: chunk index XOR row mod 8
           *reinterpret_cast<uint4*>(bt + (size_t)r * 128 + phys * 16) =
@@ -365,26 +453,30 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
       mbar_arrive(smem_u32(&full[s]));
     }
   } else if (warp < kEpiWarps) {
-    // epilogue: this thread's row of the accumulator
-    const int row = warp * 32 + lane;
+    // epilogue: warp w reads TMEM lanes 32(w%4).. of columns half w/4
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;
     const int m = m0 + row;
-    const bool ok = mbar_wait(smem_u32(accf), 0);
+    const int E2 = ((E / 2 + 31) / 32) * 32;
+    const int c_lo = half * E2, c_hi = half ? E : min(E, E2);
+    const bool ok = mbar_wait_warp(smem_u32(accf), 0);
     tc_fence_after();
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     const float g = FP4 ? a.w_global : 1.0f;
     const int k = a.k;
     const bool sp = a.act == ACT_SQRT_SOFTPLUS;
+    const bool all_ok = __all_sync(kFull, ok);
     TopList<KC> top;
     top.init();
     float amax = 0.0f, kabs = 0.0f;
-    if (__all_sync(kFull, ok)) {
-      for (int c0 = 0; c0 < E; c0 += 32) {
+    if (all_ok) {
+      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
         float v[32];
         tmem_ld32(trow + c0, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int e = c0 + j;
-          if (e < E) {
+          if (e < c_hi) {
             const float z = FP4 ? v[j] * g : v[j];
             float key = z;
             if (sp) {
@@ -397,6 +489,28 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
           }
         }
       }
+    }
+    // hand the second half's list to the first half through the (now idle) tile ring
+    uint32_t* xo = reinterpret_cast<uint32_t*>(tiles);       // [KC][BM]
+    int32_t* xi = reinterpret_cast<int32_t*>(xo + KC * BM);  // [KC][BM]
+    float* xz = reinterpret_cast<float*>(xi + KC * BM);      // [KC][BM]
+    float* xm = xz + KC * BM;                                 // [2][BM]
+    if (half == 1) {
+#pragma unroll
+      for (int j = 0; j < KC; ++j) {
+        xo[j * BM + row] = top.o[j];
+        xi[j * BM + row] = top.i[j];
+        xz[j * BM + row] = top.z[j];
+      }
+      xm[row] = amax;
+      xm[BM + row] = kabs;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+    if (half == 0 && all_ok) {
+#pragma unroll
+      for (int j = 0; j < KC; ++j) top.push(xo[j * BM + row], xi[j * BM + row], xz[j * BM + row]);
+      amax = fmaxf(amax, xm[row]);
+      kabs = fmaxf(kabs, xm[BM + row]);
       // FP64 guard-band refine (see select.cuh)
       bool close = false;
       double band = 0.0;
@@ -411,34 +525,20 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
             close = true;
       }
       if (__any_sync(kFull, close)) {
-        double thr = 0.0;
+        // the k-th key is the smallest of the first k (the list is sorted);
+        // a min avoids an index by k, which would push the list to local memory
+        uint32_t kth = 0xffffffffu;
 #pragma unroll
         for (int j = 0; j < KC; ++j)
-          if (j == k - 1) thr = (double)float_of_ord(top.o[j]) - band;
-        TopList64<KC> t64;
-        t64.init();
-        for (int c0 = 0; c0 < E; c0 += 32) {
-          float v[32];
-          tmem_ld32(trow + c0, v);
-          if (close) {
-            for (int j = 0; j < 32; ++j) {
-              const int e = c0 + j;
-              if (e < E) {
-                const float z = FP4 ? v[j] * g : v[j];
-                const float av = sqrt_softplus_f32(z);
-                const float key = a.bias ? av + __ldg(a.bias + e) : av;
-                if ((double)key >= thr)
-                  t64.push(sqrt_softplus_f64((double)z) + (a.bias ? (double)__ldg(a.bias + e) : 0.0),
-                           e, z);
-              }
-            }
-          }
-        }
+          if (j < k) kth = min(kth, top.o[j]);
+        const double thr = (double)float_of_ord(kth) - band;
+        // results come back through this row's slots of the exchange area
+        refine_row<KC, FP4>(trow, E, g, a.bias, thr, close, xi + row, xz + row);
         if (close) {
 #pragma unroll
           for (int j = 0; j < KC; ++j) {
-            top.i[j] = t64.i[j];
-            top.z[j] = t64.z[j];
+            top.i[j] = xi[j * BM + row];
+            top.z[j] = xz[j * BM + row];
           }
         }
       }
@@ -463,9 +563,11 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
         for (int c0 = 0; c0 < E; c0 += 32) {
           float v[32];
           tmem_ld32(trow + c0, v);
-          if (m < a.M)
-            for (int j = 0; j < 32 && c0 + j < E; ++j)
-              a.logits[(size_t)m * E + c0 + j] = FP4 ? v[j] * g : v[j];
+          if (m < a.M) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c0 + j < E) a.logits[(size_t)m * E + c0 + j] = FP4 ? v[j] * g : v[j];
+          }
         }
       }
       if (a.tbl_unique) {
@@ -527,13 +629,8 @@ template <int KC, bool FP4>
 cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcParams& p,
                       size_t smem, bool pdl, cudaStream_t stream) {
   auto kern = k_tc_router<KC, FP4>;
-  static bool attr_done = false;  // per instantiation; idempotent if raced
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(227 * 1024));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.a.M + BM - 1) / BM);
   cfg.blockDim = dim3((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32);
@@ -573,7 +670,7 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
   p.b_bytes = (uint32_t)a.E * BK * 2;
   p.stage_bytes = p.a_bytes + p.b_bytes;
   const size_t extra = 1024 /*align*/ + 2 * 8 * 8 + 8 + 16 + BM * kMaxK * 4;
-  const size_t budget = 227 * 1024;
+  const size_t budget = 227 * 1024 - 2048;  // the rest holds the static NVFP4 table
   int S = (int)((budget - extra) / p.stage_bytes);
   if (S > 6) S = 6;
   if (S < 2) return cudaErrorInvalidValue;
@@ -592,6 +689,19 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
   }
   return fp4 ? dispatch_k<true>(mx, mw, p, smem, pdl, stream)
              : dispatch_k<false>(mx, mw, p, smem, pdl, stream);
+}
+
+unsigned* status_word() {
+  static std::mutex mu;
+  static unsigned* ptr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_tc_status) == cudaSuccess) ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return ptr[dev];
 }
 
 int tc_read_status(int clear) {

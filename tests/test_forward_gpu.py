@@ -52,7 +52,8 @@ def check_case(case, flags=0, table=False, expect_regime=None):
     if expect_regime is not None:
         o = R.make_opts(x_dtype=case["x_dtype"], w_dtype=case["w_dtype"],
                         w_scales=1 if case["scales"] is not None else None, flags=flags)
-        assert R.router_regime(case["M"], case["H"], case["E"], case["k"], o) == expect_regime
+        want = expect_regime if isinstance(expect_regime, tuple) else (expect_regime,)
+        assert R.router_regime(case["M"], case["H"], case["E"], case["k"], o) in want
     got = run_case(case, flags=flags, table=table, tap=True)
     ref = oracle.router(case)
     k = case["k"]
@@ -72,6 +73,7 @@ def check_case(case, flags=0, table=False, expect_regime=None):
 
 
 C = synth.CONFIGS
+SMALL = (R.GBR_REGIME_GEMV, R.GBR_REGIME_GEMV1C)
 
 
 def test_tiny_fp32_case():
@@ -82,19 +84,22 @@ def test_tiny_fp32_case():
 @pytest.mark.parametrize("dup", [0.0, 0.1])
 def test_decode_softmax(M, dup):
     case = synth.make_case(C["C1"], M=M, seed=M, dup_frac=dup)
-    check_case(case, expect_regime=R.GBR_REGIME_GEMV)
+    check_case(case, expect_regime=R.GBR_REGIME_GEMV1C)
+    check_case(case, flags=R.GBR_FLAG_NO_SINGLE_CLUSTER, expect_regime=R.GBR_REGIME_GEMV)
     check_case(case, flags=R.GBR_FLAG_FORCE_GENERIC)
 
 
 @pytest.mark.parametrize("M", [1, 16, 64])
 def test_sqrt_softplus_bias(M):
     case = synth.make_case(C["C2"], M=M, seed=10 + M, dup_frac=0.1)
-    check_case(case, expect_regime=R.GBR_REGIME_GEMV)
+    check_case(case, expect_regime=R.GBR_REGIME_GEMV1C if M <= 16 else R.GBR_REGIME_GEMV)
+    check_case(case, flags=R.GBR_FLAG_NO_SINGLE_CLUSTER, expect_regime=R.GBR_REGIME_GEMV)
 
 
-@pytest.mark.parametrize("M", [3, 5, 13, 37, 63])
+@pytest.mark.parametrize("M", [3, 5, 9, 13, 16, 17, 37, 63])
 def test_ragged_M(M):
     check_case(synth.make_case(C["C2"], M=M, seed=M))
+    check_case(synth.make_case(C["C1"], M=M, seed=M), flags=R.GBR_FLAG_NO_SINGLE_CLUSTER)
 
 
 def test_m2_route_table_fused():
@@ -105,10 +110,13 @@ def test_m2_route_table_fused():
             x = case["x"].copy()
             x[1] = x[0]  # identical rows: identical expert sets
             case["x"] = x
-        check_case(case, table=True, expect_regime=R.GBR_REGIME_GEMV)
+        check_case(case, table=True, expect_regime=R.GBR_REGIME_GEMV1C)
+        check_case(case, table=True, flags=R.GBR_FLAG_NO_SINGLE_CLUSTER)
         check_case(case, table=True, flags=R.GBR_FLAG_FORCE_GENERIC)
-    for M in (4, 8, 64):
+    for M in (4, 8, 16, 64):
         check_case(synth.make_case(cfg, M=M, seed=M), table=True)
+        check_case(synth.make_case(cfg, M=M, seed=M), table=True,
+                   flags=R.GBR_FLAG_NO_SINGLE_CLUSTER)
 
 
 def test_exact_tie_from_duplicated_weights_goes_to_lower_index():
@@ -129,8 +137,9 @@ def test_exact_tie_from_duplicated_weights_goes_to_lower_index():
 
 
 def test_unfused_pair_matches_fused_bitwise():
+    # the unfused pair runs the split-cluster logits kernel, then router_select
     case = synth.make_case(C["C1"], M=8, seed=5)
-    a = run_case(case)
+    a = run_case(case, flags=R.GBR_FLAG_NO_SINGLE_CLUSTER)
     b = run_case(case, flags=R.GBR_FLAG_UNFUSED)
     assert np.array_equal(a["idx"], b["idx"])
     assert np.array_equal(a["w"], b["w"])
@@ -142,11 +151,18 @@ def test_odd_hidden_sizes(H):
     check_case(synth.make_case(cfg, M=8, seed=H))
 
 
-@pytest.mark.parametrize("E,k", [(16, 2), (64, 16), (128, 4), (512, 8), (48, 3)])
+@pytest.mark.parametrize("E,k", [(16, 2), (64, 16), (128, 4), (512, 8), (48, 3), (256, 1)])
 def test_expert_counts(E, k):
     cfg = dict(C["C2"], E=E, k=k, H=512)
     check_case(synth.make_case(cfg, M=8, seed=E))
+    check_case(synth.make_case(cfg, M=12, seed=E + 2), flags=R.GBR_FLAG_NO_SINGLE_CLUSTER)
     check_case(synth.make_case(cfg, M=33, seed=E + 1))
+
+
+@pytest.mark.parametrize("H", [32, 6144, 7168])
+def test_single_cluster_hidden_limits(H):
+    cfg = dict(C["C1"], H=H)
+    check_case(synth.make_case(cfg, M=4, seed=H))
 
 
 def test_nvfp4_weights_small_M():

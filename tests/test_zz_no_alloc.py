@@ -11,7 +11,8 @@ import pytest
 
 from moe_expert_router_02_gb300 import router as R
 from moe_expert_router_02_gb300 import synth
-from tests.helpers import W_TOL, dev, empty_outputs
+import oracle
+from tests.helpers import GAP_TOL, W_TOL, dev, empty_outputs
 
 pytestmark = pytest.mark.gpu
 
@@ -35,8 +36,17 @@ def test_noalloc_matches_router_forward_on_two_calls(cfg_name, M):
                                             torch.cuda.current_stream().cuda_stream)
         assert rc == R.GBR_OK, R.router_strerror(rc)
         torch.cuda.synchronize()
-        assert np.array_equal(idx.cpu().numpy(), ref_idx.cpu().numpy())
-        assert np.max(np.abs(w.cpu().numpy() - ref_w.cpu().numpy())) <= W_TOL
+        gi, gw = idx.cpu().numpy(), w.cpu().numpy()
+        ri, rw = ref_idx.cpu().numpy(), ref_w.cpu().numpy()
+        # the two entry points may run different kernels (different FP32
+        # summation order): ids must agree except on rows whose oracle key gap
+        # at the k / k+1 boundary is below the tests' gap tolerance
+        same = np.all(gi == ri, axis=1)
+        if not np.all(same):
+            keys = oracle.router(case)["keys"]
+            gap = keys[:, k - 1] - keys[:, k]
+            assert np.all(gap[~same] < GAP_TOL)
+        assert np.max(np.abs(gw[same] - rw[same])) <= W_TOL
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
