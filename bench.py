@@ -112,13 +112,21 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(rows_per_rank, layers, steps, world, ms_max):
+    """Whole-job router tokens/s: every rank routes its own batch (replicas,
+    no exchange), and the job takes as long as its slowest rank."""
+    return rows_per_rank * layers * steps * world / (ms_max / 1e3)
 
 
 # ---------------------------------------------------------------- GPU helpers
@@ -221,23 +229,27 @@ class RouterSet:
 
 
 def per_call_stats(rs, steps):
-    """(us per call in graph replay, us isolated single call)."""
+    """(us per call in the back-to-back graph, us of one call alone).
+
+    The single call is a one-kernel CUDA graph replayed with the device idle
+    before it, so the figure includes the graph launch but no host Python."""
     import torch
     ms = time_graph(rs.step, steps)
     us_pipe = ms * 1e3 / rs.calls
-    # isolated: one call, stream synchronised around it, W rotating
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=rs.stream):
+        rs.call(0, 0, rs.stream)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     tot = 0.0
     n = 30
-    with torch.cuda.stream(rs.stream):
-        for i in range(n + 3):
-            torch.cuda.synchronize()
-            s.record(rs.stream)
-            rs.call(0, (7 * i) % rs.W.shape[0], rs.stream)
-            e.record(rs.stream)
-            torch.cuda.synchronize()
-            if i >= 3:
-                tot += s.elapsed_time(e)
+    for i in range(n + 3):
+        torch.cuda.synchronize()
+        s.record()
+        g.replay()
+        e.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            tot += s.elapsed_time(e)
     return us_pipe, tot * 1e3 / n
 
 
@@ -286,7 +298,7 @@ def run_ours(args, rank, world, local):
     ms = ev_s.elapsed_time(ev_e)
     ms = max_over_ranks(ms, world)
     tokens = M * LAYERS * args.steps * world
-    value = tokens / (ms / 1e3)
+    value = job_throughput(M, LAYERS, args.steps, world, ms)
     us_call = ms * 1e3 / (args.steps * LAYERS)
     algo = head.algo_bytes()
     achieved = algo / (us_call * 1e-6) / 1e9

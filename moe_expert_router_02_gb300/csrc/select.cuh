@@ -35,83 +35,74 @@ struct LdCG {  // global loads that bypass L1 (data written by other CTAs)
   __device__ __forceinline__ float operator()(int e) const { return __ldcg(p + e); }
 };
 
+// Compare-exchange on packed (key, index) pairs: larger packed value first.
+__device__ __forceinline__ void cas_desc(uint64_t& a, uint64_t& b) {
+  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
+// Sorts VPL packed values descending in registers (odd-even transposition;
+// fully unrolled, so every index is static).
+template <int VPL>
+__device__ __forceinline__ void sort_desc(uint64_t (&v)[VPL]) {
+#pragma unroll
+  for (int pass = 0; pass < VPL; ++pass) {
+#pragma unroll
+    for (int j = pass & 1; j + 1 < VPL; j += 2) cas_desc(v[j], v[j + 1]);
+  }
+}
+
 // One warp selects the top-k of one row of E <= 32*VPL logits.
 // Lane r < k writes slot r of out_idx / out_w and, if sel_out is not null,
 // sel_out[r] (for a route table). All 32 lanes must call.
 //
-// Each lane holds the order-preserving keys of experts lane, lane+32, ...
-// and caches its own best; a round takes the warp maximum key (redux.sync),
-// then the lowest index among the lanes holding it (redux.sync), and only
-// the winning lane rescans its entries. The winner's score (logit or
-// unbiased activation) travels by shuffle, so the weights need no second
-// pass over the logits.
+// Each lane packs its entries as (order-preserving key << 32 | ~index) and
+// sorts them once; a round takes the warp maximum key (redux.sync), then
+// the lowest index among the lanes holding it (redux.sync), and the winning
+// lane shifts its sorted list by one. Scores are read back once at the end.
 template <int VPL, class Ld>
 __device__ __noinline__ void warp_select_row(const Ld ld, const float* __restrict__ bias, int E,
                                              int k, int act, int32_t* __restrict__ out_idx,
                                              float* __restrict__ out_w, int32_t* sel_out) {
   const int lane = threadIdx.x & 31;
-  uint32_t ok[VPL];  // order-preserving key, 0 = empty or taken (finite keys map above 0)
-  float sc[VPL];     // the score the weights use: logit (softmax) or unbiased activation
+  uint64_t pk[VPL];  // (key << 32) | (0xffffffff - expert); 0 = empty
   float amax = 0.0f, kabs = 0.0f;
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
     const int e = lane + 32 * j;
-    ok[j] = 0u;
-    sc[j] = 0.0f;
+    pk[j] = 0ull;
     if (e < E) {
       const float z = ld(e);
-      if (act == ACT_SOFTMAX) {
-        ok[j] = ord_of(z);
-        sc[j] = z;
-      } else {
+      float key = z;
+      if (act != ACT_SOFTMAX) {
         const float a = sqrt_softplus_f32(z);
-        const float kv = bias ? a + __ldg(bias + e) : a;
-        ok[j] = ord_of(kv);
-        sc[j] = a;
+        key = bias ? a + __ldg(bias + e) : a;
         amax = fmaxf(amax, a);
-        kabs = fmaxf(kabs, fabsf(kv));
+        kabs = fmaxf(kabs, fabsf(key));
       }
+      pk[j] = ((uint64_t)ord_of(key) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
     }
   }
-  uint32_t bo = 0u;  // this lane's best key, its slot and score
-  int bj = 0;
-  float bs = 0.0f;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j)
-    if (ok[j] > bo) {  // strict: the lower index wins inside a lane
-      bo = ok[j];
-      bj = j;
-      bs = sc[j];
-    }
+  sort_desc<VPL>(pk);
 
   // k+1 rounds: the (k+1)-th key is kept for the gap test.
   const int kk = min(k + 1, E);
   int sel_idx = -1;
-  float sel_key = 0.0f, sel_sc = 0.0f;
+  float sel_key = 0.0f;
   for (int r = 0; r < kk; ++r) {
+    const uint32_t bo = (uint32_t)(pk[0] >> 32);
     const uint32_t wbest = __reduce_max_sync(kFull, bo);
-    const uint32_t cand = (bo == wbest) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+    const uint32_t cand = (bo == wbest) ? 0xffffffffu - (uint32_t)pk[0] : 0xffffffffu;
     const uint32_t widx = __reduce_min_sync(kFull, cand);  // lowest index among equal keys
-    const int wl = (int)(widx & 31u);
-    const float wsc = __shfl_sync(kFull, bs, wl);
     if (lane == r) {
       sel_idx = (int)widx;
       sel_key = float_of_ord(wbest);
-      sel_sc = wsc;
     }
-    if (lane == wl) {
-      const int tj = (int)(widx >> 5);
-      bo = 0u;
-      bj = 0;
+    if ((int)(widx & 31u) == lane) {
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        if (j == tj) ok[j] = 0u;
-        if (ok[j] > bo) {
-          bo = ok[j];
-          bj = j;
-          bs = sc[j];
-        }
-      }
+      for (int j = 0; j + 1 < VPL; ++j) pk[j] = pk[j + 1];
+      pk[VPL - 1] = 0ull;
     }
   }
 
@@ -145,31 +136,24 @@ __device__ __noinline__ void warp_select_row(const Ld ld, const float* __restric
       for (int r = 0; r < k; ++r) {
         double bv = -INFINITY;
         int bidx = 0x7fffffff;
-        float bsc = 0.0f;
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
           if (((cmask >> j) & 1u) && (bidx == 0x7fffffff || k64[j] > bv)) {
             bv = k64[j];
             bidx = lane + 32 * j;
-            bsc = sc[j];
           }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
           const double ov = __shfl_xor_sync(kFull, bv, off);
           const int oi = __shfl_xor_sync(kFull, bidx, off);
-          const float os = __shfl_xor_sync(kFull, bsc, off);
           if (ov > bv || (ov == bv && oi < bidx)) {
             bv = ov;
             bidx = oi;
-            bsc = os;
           }
         }
         if ((bidx & 31) == lane) cmask &= ~(1u << (bidx >> 5));
-        if (lane == r) {
-          sel_idx = bidx;
-          sel_sc = bsc;
-        }
+        if (lane == r) sel_idx = bidx;
       }
     }
   }
@@ -177,13 +161,18 @@ __device__ __noinline__ void warp_select_row(const Ld ld, const float* __restric
   // weights over the chosen k, summed in slot order
   float s = 0.0f;
   if (act == ACT_SOFTMAX) {
-    const float z0 = __shfl_sync(kFull, sel_sc, 0);
-    if (lane < k) s = expf(sel_sc - z0);
+    // the key is the logit (-0.0 read back as +0.0, which exp treats alike)
+    const float z0 = __shfl_sync(kFull, sel_key, 0);
+    if (lane < k) s = expf(sel_key - z0);
   } else if (lane < k) {
-    s = sel_sc;
+    s = sqrt_softplus_f32(ld(sel_idx));
   }
   float sum = 0.0f;
-  for (int r = 0; r < k; ++r) sum += __shfl_sync(kFull, s, r);
+#pragma unroll
+  for (int r = 0; r < kMaxK; ++r) {
+    const float v = __shfl_sync(kFull, s, r);
+    if (r < k) sum += v;
+  }
   if (lane < k) {
     out_idx[lane] = sel_idx;
     out_w[lane] = (sum > 0.0f) ? s / sum : 1.0f / (float)k;

@@ -279,11 +279,52 @@ __device__ __noinline__ void refine_row(uint32_t trow, int E, float g, const flo
   }
 }
 
+// FP64 refine of one row from its candidate lists (both column halves):
+// only experts whose FP32 key lies within `band` of another candidate at or
+// above thr get an FP64 key; the others keep their FP32 key, which orders
+// them correctly against everything more than `band` away. The best KC by
+// (key desc, index asc) are written to out_i / out_z (KC entries, BM apart).
+template <int KC>
+__device__ __noinline__ void refine_candidates(const int32_t* e0, const float* z0, const float* k0,
+                                               int n0, const int32_t* e1, const float* z1,
+                                               const float* k1, int n1, const float* bias,
+                                               double thr, double band, int* out_i,
+                                               float* out_z) {
+  TopList64<KC> t64;
+  t64.init();
+  const int n = n0 + n1;
+  for (int p = 0; p < n; ++p) {
+    const bool h0 = p < n0;
+    const int q = h0 ? p : p - n0;
+    const double kp = (double)(h0 ? k0[q] : k1[q]);
+    if (kp < thr) continue;
+    bool near = false;
+    for (int r = 0; r < n && !near; ++r) {
+      if (r == p) continue;
+      const double kr = (double)(r < n0 ? k0[r] : k1[r - n0]);
+      if (kr >= thr - band && fabs(kp - kr) <= band) near = true;
+    }
+    const int e = h0 ? e0[q] : e1[q];
+    const float z = h0 ? z0[q] : z1[q];
+    const double key =
+        near ? sqrt_softplus_f64((double)z) + (bias ? (double)__ldg(bias + e) : 0.0) : kp;
+    t64.push(key, e, z);
+  }
+#pragma unroll
+  for (int j = 0; j < KC; ++j) {
+    out_i[j * BM] = t64.i[j];
+    out_z[j * BM] = t64.z[j];
+  }
+}
+
+constexpr size_t kCandOffset = 32768;  // candidate lists start after the exchange area
+
 struct TcParams {
   RouterArgs a;
   int stages;
   uint32_t stage_bytes, a_bytes, b_bytes;
   int tmem_cols;
+  int cap;  // candidate slots per (column half, row)
 };
 
 // Serial unique-route table for one pair of rows (the thread owning the
@@ -459,17 +500,47 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
     const int m = m0 + row;
     const int E2 = ((E / 2 + 31) / 32) * 32;
     const int c_lo = half * E2, c_hi = half ? E : min(E, E2);
-    const bool ok = mbar_wait_warp(smem_u32(accf), 0);
-    tc_fence_after();
-    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     const float g = FP4 ? a.w_global : 1.0f;
     const int k = a.k;
     const bool sp = a.act == ACT_SQRT_SOFTPLUS;
+    const bool has_bias = sp && a.bias != nullptr;
+    // range of the selection-only bias (read before the accumulator is ready)
+    float bmin = 0.0f, bmax = 0.0f;
+    if (has_bias) {
+      bmin = INFINITY;
+      bmax = -INFINITY;
+      for (int e = lane; e < E; e += 32) {
+        const float b = __ldg(a.bias + e);
+        bmin = fminf(bmin, b);
+        bmax = fmaxf(bmax, b);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        bmin = fminf(bmin, __shfl_xor_sync(kFull, bmin, off));
+        bmax = fmaxf(bmax, __shfl_xor_sync(kFull, bmax, off));
+      }
+    }
+    const bool ok = mbar_wait_warp(smem_u32(accf), 0);
+    tc_fence_after();
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
     const bool all_ok = __all_sync(kFull, ok);
+    // the idle tile ring: exchange area, then per-(half, row) candidate lists
+    uint32_t* xo = reinterpret_cast<uint32_t*>(tiles);       // [KC][BM]
+    int32_t* xi = reinterpret_cast<int32_t*>(xo + KC * BM);  // [KC][BM]
+    float* xz = reinterpret_cast<float*>(xi + KC * BM);      // [KC][BM]
+    float* xm = xz + KC * BM;                                 // [3][BM]
+    const int cap = p.cap, CP = p.cap + 1;
+    int32_t* cand_e = reinterpret_cast<int32_t*>(tiles + kCandOffset);
+    float* cand_z = reinterpret_cast<float*>(cand_e + 2 * BM * CP);
+    float* cand_k = cand_z + 2 * BM * CP;
+    const size_t my_list = (size_t)(half * BM + row) * CP;
     TopList<KC> top;
     top.init();
     float amax = 0.0f, kabs = 0.0f;
-    if (all_ok) {
+    int ncand = 0;
+    bool overflow = false;
+    if (all_ok && !sp) {
+      // softmax: the key is the logit itself
       for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
         float v[32];
         tmem_ld32(trow + c0, v);
@@ -478,23 +549,110 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
           const int e = c0 + j;
           if (e < c_hi) {
             const float z = FP4 ? v[j] * g : v[j];
-            float key = z;
-            if (sp) {
-              const float av = sqrt_softplus_f32(z);
-              key = a.bias ? av + __ldg(a.bias + e) : av;
-              amax = fmaxf(amax, av);
-              kabs = fmaxf(kabs, fabsf(key));
+            top.push(ord_of(z), e, z);
+          }
+        }
+      }
+    } else if (all_ok) {
+      // Pass A: this half's k-th largest logit z_k. The half holds k experts
+      // with key >= a(z_k) + b_min, so an expert can reach the top k only if
+      // a(z) + b_max >= a(z_k) + b_min: z >= a^-1(a(z_k) - (b_max - b_min)).
+      uint32_t zo[KC];
+#pragma unroll
+      for (int j = 0; j < KC; ++j) zo[j] = 0u;
+      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+        float v[32];
+        tmem_ld32(trow + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (c0 + j < c_hi) {
+            const uint32_t o = ord_of(FP4 ? v[j] * g : v[j]);
+            if (o > zo[KC - 1]) {
+#pragma unroll
+              for (int q = KC - 1; q > 0; --q)
+                if (o > zo[q]) zo[q] = (o > zo[q - 1]) ? zo[q - 1] : o;
+              if (o > zo[0]) zo[0] = o;
             }
-            top.push(ord_of(key), e, z);
+          }
+        }
+      }
+      uint32_t kth = 0xffffffffu;
+#pragma unroll
+      for (int j = 0; j < KC; ++j)
+        if (j < k) kth = min(kth, zo[j]);
+      // the threshold, rounded down with margins far above the FP32 errors of
+      // sqrt_softplus (<= 2.25 ulp), expm1f and logf (<= 1 ulp each)
+      float tz;
+      if (kth == 0u) {
+        tz = -INFINITY;  // fewer than k experts in this half: keep them all
+      } else if (!has_bias) {
+        tz = float_of_ord(kth);  // a is increasing: the top k by key are the top k by logit
+      } else {
+        const float ak = sqrt_softplus_f32(float_of_ord(kth));
+        const float y = ak * (1.0f - 0x1p-20f) - (bmax - bmin) * (1.0f + 0x1p-20f) - 0x1p-40f;
+        if (!(y > 0.0f)) {
+          tz = -INFINITY;
+        } else {
+          const float t = logf(expm1f(y * y * (1.0f - 0x1p-21f)));
+          tz = t - 0x1p-18f * (1.0f + fabsf(t));
+        }
+      }
+      // Pass B: compact this row-half's candidates into shared memory
+      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+        float v[32];
+        tmem_ld32(trow + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int e = c0 + j;
+          if (e < c_hi) {
+            const float z = FP4 ? v[j] * g : v[j];
+            if (z >= tz) {
+              if (ncand < cap) {
+                cand_e[my_list + ncand] = e;
+                cand_z[my_list + ncand] = z;
+              }
+              ++ncand;
+            }
+          }
+        }
+      }
+      overflow = ncand > cap;
+      // Pass C: the activation for the candidates only, lanes in lockstep
+      const int nmax = (int)__reduce_max_sync(kFull, overflow ? 0u : (uint32_t)ncand);
+      for (int i = 0; i < nmax; ++i) {
+        if (!overflow && i < ncand) {
+          const int e = cand_e[my_list + i];
+          const float z = cand_z[my_list + i];
+          const float av = sqrt_softplus_f32(z);
+          const float key = has_bias ? av + __ldg(a.bias + e) : av;
+          cand_k[my_list + i] = key;
+          amax = fmaxf(amax, av);
+          kabs = fmaxf(kabs, fabsf(key));
+          top.push(ord_of(key), e, z);
+        }
+      }
+      if (__any_sync(kFull, overflow)) {  // too many candidates: every column of the half
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+          float v[32];
+          tmem_ld32(trow + c0, v);
+          if (overflow) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int e = c0 + j;
+              if (e < c_hi) {
+                const float z = FP4 ? v[j] * g : v[j];
+                const float av = sqrt_softplus_f32(z);
+                const float key = has_bias ? av + __ldg(a.bias + e) : av;
+                amax = fmaxf(amax, av);
+                kabs = fmaxf(kabs, fabsf(key));
+                top.push(ord_of(key), e, z);
+              }
+            }
           }
         }
       }
     }
-    // hand the second half's list to the first half through the (now idle) tile ring
-    uint32_t* xo = reinterpret_cast<uint32_t*>(tiles);       // [KC][BM]
-    int32_t* xi = reinterpret_cast<int32_t*>(xo + KC * BM);  // [KC][BM]
-    float* xz = reinterpret_cast<float*>(xi + KC * BM);      // [KC][BM]
-    float* xm = xz + KC * BM;                                 // [2][BM]
+    // hand the second half's list to the first half
     if (half == 1) {
 #pragma unroll
       for (int j = 0; j < KC; ++j) {
@@ -504,6 +662,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
       }
       xm[row] = amax;
       xm[BM + row] = kabs;
+      xm[2 * BM + row] = __int_as_float(overflow ? -1 : ncand);
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
     if (half == 0 && all_ok) {
@@ -511,6 +670,8 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
       for (int j = 0; j < KC; ++j) top.push(xo[j * BM + row], xi[j * BM + row], xz[j * BM + row]);
       amax = fmaxf(amax, xm[row]);
       kabs = fmaxf(kabs, xm[BM + row]);
+      const int ncand1 = __float_as_int(xm[2 * BM + row]);
+      const bool any_overflow = overflow || ncand1 < 0;
       // FP64 guard-band refine (see select.cuh)
       bool close = false;
       double band = 0.0;
@@ -524,17 +685,29 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
               (double)float_of_ord(top.o[j]) - (double)float_of_ord(top.o[j + 1]) <= band)
             close = true;
       }
-      if (__any_sync(kFull, close)) {
-        // the k-th key is the smallest of the first k (the list is sorted);
-        // a min avoids an index by k, which would push the list to local memory
-        uint32_t kth = 0xffffffffu;
+      // the k-th key is the smallest of the first k (the list is sorted);
+      // a min avoids an index by k, which would push the list to local memory
+      uint32_t kth = 0xffffffffu;
 #pragma unroll
-        for (int j = 0; j < KC; ++j)
-          if (j < k) kth = min(kth, top.o[j]);
-        const double thr = (double)float_of_ord(kth) - band;
-        // results come back through this row's slots of the exchange area
-        refine_row<KC, FP4>(trow, E, g, a.bias, thr, close, xi + row, xz + row);
-        if (close) {
+      for (int j = 0; j < KC; ++j)
+        if (j < k) kth = min(kth, top.o[j]);
+      const double thr = (double)float_of_ord(kth) - band;
+      if (close && !any_overflow) {
+        refine_candidates<KC>(cand_e + (size_t)row * CP, cand_z + (size_t)row * CP,
+                              cand_k + (size_t)row * CP, ncand,
+                              cand_e + (size_t)(BM + row) * CP, cand_z + (size_t)(BM + row) * CP,
+                              cand_k + (size_t)(BM + row) * CP, ncand1, a.bias, thr, band,
+                              xi + row, xz + row);
+#pragma unroll
+        for (int j = 0; j < KC; ++j) {
+          top.i[j] = xi[j * BM + row];
+          top.z[j] = xz[j * BM + row];
+        }
+      }
+      const bool slow = close && any_overflow;
+      if (__any_sync(kFull, slow)) {  // rows whose candidate lists overflowed
+        refine_row<KC, FP4>(trow, E, g, a.bias, thr, slow, xi + row, xz + row);
+        if (slow) {
 #pragma unroll
           for (int j = 0; j < KC; ++j) {
             top.i[j] = xi[j * BM + row];
@@ -678,6 +851,15 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
   int cols = 32;
   while (cols < a.E) cols <<= 1;
   p.tmem_cols = cols;
+  // candidate lists reuse the tile ring after the main loop: 3 arrays of
+  // [2 halves][BM rows][cap + 1] 4-byte entries after the exchange area
+  const size_t ring = (size_t)S * p.stage_bytes;
+  const int per_half = (((a.E / 2) + 31) / 32) * 32;
+  long cap = ((long)ring - (long)kCandOffset) / (3L * 2 * BM * 4) - 1;
+  if (cap > 40) cap = 40;
+  if (cap > per_half) cap = per_half;
+  if (cap < 1) return cudaErrorInvalidValue;
+  p.cap = (int)cap;
   const size_t smem = (size_t)S * p.stage_bytes + extra;
 
   CUtensorMap mx, mw;

@@ -48,6 +48,16 @@ def run_case(case, flags=0, table=False, tap=False, t=None):
     return out
 
 
+def run_select_on(lg, k, act, bias):
+    import torch
+    M, E = lg.shape
+    idx, w = empty_outputs(M, k)
+    R.router_select(dev(np.ascontiguousarray(lg, dtype=np.float32)),
+                    None if bias is None else dev(bias), M, E, k, act, idx, w)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), w.cpu().numpy()
+
+
 def check_case(case, flags=0, table=False, expect_regime=None):
     if expect_regime is not None:
         o = R.make_opts(x_dtype=case["x_dtype"], w_dtype=case["w_dtype"],
@@ -65,6 +75,11 @@ def check_case(case, flags=0, table=False, expect_regime=None):
     oi, ow, _ = oracle.select(lg.astype(np.float64), k, case["act"], bias=case["bias"])
     assert np.array_equal(got["idx"], oi)
     assert np.max(np.abs(got["w"] - ow)) <= W_TOL
+    # qwisp #145 G-A: the fused kernel and the unfused selection stage give
+    # bit-identical ids and weights on the same FP32 logits
+    si, sw = run_select_on(lg, k, case["act"], case["bias"])
+    assert np.array_equal(got["idx"], si)
+    assert np.array_equal(got["w"].view(np.uint32), sw.view(np.uint32))
     if table:
         tref = oracle.route_table(got["idx"].reshape(-1, 2, k))
         for name, g, r in zip(("unique", "mask", "map", "count"), got["table"], tref):
