@@ -39,7 +39,6 @@ static __device__ unsigned g_tc_status = 0;
 constexpr int BM = 128;   // token rows per CTA (= MMA M, = TMEM lanes)
 constexpr int BK = 64;    // BF16 elements per k-step (one 128-byte swizzle atom)
 constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, each half of the columns
-constexpr int kDeqWarps = 4;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -183,7 +182,7 @@ template <int KC>
 struct TopList {
   uint32_t o[KC];  // order-preserving key
   int i[KC];
-  float z[KC];     // the logit
+  float z[KC];     // the score the weights use (logit for softmax, activation otherwise)
   __device__ __forceinline__ void init() {
 #pragma unroll
     for (int j = 0; j < KC; ++j) {
@@ -224,24 +223,34 @@ struct TopList64 {
       z[j] = 0.0f;
     }
   }
+  // (kv, idx) ahead of (v[j], i[j]): larger key, or equal key and lower index
+  __device__ __forceinline__ static bool ahead(double kv, int idx, double vj, int ij) {
+    return kv > vj || (kv == vj && idx < ij);
+  }
   __device__ __forceinline__ void push(double kv, int idx, float zz) {
-    if (!(kv > v[KC - 1])) return;
+    if (!ahead(kv, idx, v[KC - 1], i[KC - 1])) return;
 #pragma unroll
     for (int j = KC - 1; j > 0; --j) {
-      if (kv > v[j]) {
-        const bool up = kv > v[j - 1];
+      if (ahead(kv, idx, v[j], i[j])) {
+        const bool up = ahead(kv, idx, v[j - 1], i[j - 1]);
         v[j] = up ? v[j - 1] : kv;
         i[j] = up ? i[j - 1] : idx;
         z[j] = up ? z[j - 1] : zz;
       }
     }
-    if (kv > v[0]) {
+    if (ahead(kv, idx, v[0], i[0])) {
       v[0] = kv;
       i[0] = idx;
       z[0] = zz;
     }
   }
 };
+
+// FP64 key of one expert; out of line so that the FP64 work runs only for
+// the entries that need it.
+__device__ __noinline__ double key64(float z, const float* bias, int e) {
+  return sqrt_softplus_f64((double)z) + (bias ? (double)__ldg(bias + e) : 0.0);
+}
 
 // FP64 re-ranking of one row (see select.cuh): every lane of the warp calls
 // it (the TMEM loads are warp-collective); lanes with close == false only
@@ -265,7 +274,7 @@ __device__ __noinline__ void refine_row(uint32_t trow, int E, float g, const flo
           const float av = sqrt_softplus_f32(z);
           const float key = bias ? av + __ldg(bias + e) : av;
           if ((double)key >= thr)
-            t64.push(sqrt_softplus_f64((double)z) + (bias ? (double)__ldg(bias + e) : 0.0), e, z);
+            t64.push(sqrt_softplus_f64((double)z) + (bias ? (double)__ldg(bias + e) : 0.0), e, av);
         }
       }
     }
@@ -279,52 +288,14 @@ __device__ __noinline__ void refine_row(uint32_t trow, int E, float g, const flo
   }
 }
 
-// FP64 refine of one row from its candidate lists (both column halves):
-// only experts whose FP32 key lies within `band` of another candidate at or
-// above thr get an FP64 key; the others keep their FP32 key, which orders
-// them correctly against everything more than `band` away. The best KC by
-// (key desc, index asc) are written to out_i / out_z (KC entries, BM apart).
-template <int KC>
-__device__ __noinline__ void refine_candidates(const int32_t* e0, const float* z0, const float* k0,
-                                               int n0, const int32_t* e1, const float* z1,
-                                               const float* k1, int n1, const float* bias,
-                                               double thr, double band, int* out_i,
-                                               float* out_z) {
-  TopList64<KC> t64;
-  t64.init();
-  const int n = n0 + n1;
-  for (int p = 0; p < n; ++p) {
-    const bool h0 = p < n0;
-    const int q = h0 ? p : p - n0;
-    const double kp = (double)(h0 ? k0[q] : k1[q]);
-    if (kp < thr) continue;
-    bool near = false;
-    for (int r = 0; r < n && !near; ++r) {
-      if (r == p) continue;
-      const double kr = (double)(r < n0 ? k0[r] : k1[r - n0]);
-      if (kr >= thr - band && fabs(kp - kr) <= band) near = true;
-    }
-    const int e = h0 ? e0[q] : e1[q];
-    const float z = h0 ? z0[q] : z1[q];
-    const double key =
-        near ? sqrt_softplus_f64((double)z) + (bias ? (double)__ldg(bias + e) : 0.0) : kp;
-    t64.push(key, e, z);
-  }
-#pragma unroll
-  for (int j = 0; j < KC; ++j) {
-    out_i[j * BM] = t64.i[j];
-    out_z[j * BM] = t64.z[j];
-  }
-}
-
-constexpr size_t kCandOffset = 32768;  // candidate lists start after the exchange area
+constexpr size_t kCandOffset = 32768;  // the logits copy starts after the exchange area
+constexpr int kListCap = 1024;         // pooled candidates per warp (4 KB each)
 
 struct TcParams {
   RouterArgs a;
   int stages;
   uint32_t stage_bytes, a_bytes, b_bytes;
   int tmem_cols;
-  int cap;  // candidate slots per (column half, row)
 };
 
 // Serial unique-route table for one pair of rows (the thread owning the
@@ -363,11 +334,12 @@ __device__ void pair_table(const int32_t* r0, const int32_t* r1, int k, int32_t*
 }
 
 template <int KC, bool FP4>
-__global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 1)
+__global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
     k_tc_router(const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_w, const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_lut[256];  // NVFP4: byte of two E2M1 codes -> two BF16 values
+  __shared__ float s_bias[256];    // the selection bias (sqrt-softplus)
   const RouterArgs& a = p.a;
   const int S = p.stages;
   // 1024-byte aligned tile ring, then barriers
@@ -388,7 +360,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&full[s]), FP4 ? 1 + kDeqWarps * 32 : 1);
+      mbar_init(smem_u32(&full[s]), FP4 ? 1 + kEpiWarps * 32 : 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(accf), 1);
@@ -449,50 +421,6 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
       }
       mma_commit(smem_u32(accf));
     }
-  } else if (FP4 && warp >= kEpiWarps + 2) {
-    // W decode warps: E x 64 BF16 tile per k-step, rows dt and dt + 128.
-    const int dt = threadIdx.x - (kEpiWarps + 2) * 32;
-    for (int b = dt; b < 256; b += kDeqWarps * 32) {
-      const uint32_t lo = __float_as_uint(e2m1_to_f32(b & 15u)) >> 16;
-      const uint32_t hi = __float_as_uint(e2m1_to_f32((uint32_t)b >> 4)) >> 16;
-      s_lut[b] = lo | (hi << 16);
-    }
-    asm volatile("bar.sync 2, %0;" ::"r"(kDeqWarps * 32) : "memory");
-    const uint8_t* q = static_cast<const uint8_t*>(a.w);
-    const int Hb = a.H / 2, Hs = a.H / 16;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % S;
-      const uint32_t ph = (uint32_t)(kb / S) & 1u;
-      if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1u)) break;
-      uint8_t* bt = tiles + (size_t)s * p.stage_bytes + p.a_bytes;
-      for (int r = dt; r < E; r += kDeqWarps * 32) {
-        const uint4* src = reinterpret_cast<const uint4*>(q + (size_t)r * Hb + kb * (BK / 2));
-        const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
-        const uint32_t sc = __ldg(reinterpret_cast<const uint32_t*>(a.w_scales + (size_t)r * Hs +
-                                                                     kb * (BK / 16)));
-        const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c = elements 8c..8c+7
-          // the scale in BF16 (exact: at most 4 significant bits), twice
-          const uint32_t sb16 = __float_as_uint(e4m3_to_f32((sc >> (8 * (c >> 1))) & 0xffu)) >> 16;
-          const __nv_bfloat162 scale2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)sb16),
-                                                           __ushort_as_bfloat16((unsigned short)sb16));
-          uint32_t outw[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t pair = s_lut[(qw[c] >> (8 * j)) & 0xffu];
-            __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pair);
-            v = __hmul2(v, scale2);  // exact: the product has at most 6 significant bits
-            outw[j] = *reinterpret_cast<const uint32_t*>(&v);
-          }
-          const int phys = c ^ (r & 7);  // 128-byte swizzle: chunk index XOR row mod 8
-          *reinterpret_cast<uint4*>(bt + (size_t)r * 128 + phys * 16) =
-              make_uint4(outw[0], outw[1], outw[2], outw[3]);
-        }
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(smem_u32(&full[s]));
-    }
   } else if (warp < kEpiWarps) {
     // epilogue: warp w reads TMEM lanes 32(w%4).. of columns half w/4
     const int quad = warp & 3, half = warp >> 2;
@@ -520,6 +448,82 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
         bmax = fmaxf(bmax, __shfl_xor_sync(kFull, bmax, off));
       }
     }
+    if (has_bias && warp == 0)
+      for (int e = lane; e < E; e += 32) s_bias[e] = __ldg(a.bias + e);
+    asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+    if (FP4) {
+      // During the main loop these warps decode W: thread t owns row t of
+      // every E x 64 BF16 tile; the packed bytes and scales of k-step kb + 2
+      // are loaded while kb is decoded.
+      const int r = threadIdx.x;  // 0..255
+      for (int b = r; b < 256; b += kEpiWarps * 32) {
+        const uint32_t lo = __float_as_uint(e2m1_to_f32(b & 15u)) >> 16;
+        const uint32_t hi = __float_as_uint(e2m1_to_f32((uint32_t)b >> 4)) >> 16;
+        s_lut[b] = lo | (hi << 16);
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+      const uint8_t* qp = static_cast<const uint8_t*>(a.w);
+      const int Hb = a.H / 2, Hs = a.H / 16;
+      const bool has_row = r < E;
+      uint4 pq[2][2];  // [slot][half of the 32 packed bytes]
+      uint32_t ps[2];  // [slot] four E4M3 scales
+#define GBR_FP4_LOAD(slot, kbl)                                                                  \
+  do {                                                                                           \
+    if ((kbl) < nk && has_row) {                                                                 \
+      const uint4* src = reinterpret_cast<const uint4*>(qp + (size_t)r * Hb + (kbl) * (BK / 2)); \
+      pq[slot][0] = __ldg(src);                                                                  \
+      pq[slot][1] = __ldg(src + 1);                                                              \
+      ps[slot] = __ldg(                                                                          \
+          reinterpret_cast<const uint32_t*>(a.w_scales + (size_t)r * Hs + (kbl) * (BK / 16)));   \
+    }                                                                                            \
+  } while (0)
+      GBR_FP4_LOAD(0, 0);
+      GBR_FP4_LOAD(1, 1);
+      bool dec_ok = true;
+      for (int kb2 = 0; kb2 < nk && dec_ok; kb2 += 2) {
+#pragma unroll
+        for (int slot = 0; slot < 2; ++slot) {  // unrolled so the register slots are static
+          const int kb = kb2 + slot;
+          if (kb >= nk) break;
+          const int s = kb % S;
+          const uint32_t ph = (uint32_t)(kb / S) & 1u;
+          if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1u)) {
+            dec_ok = false;
+            break;
+          }
+          if (has_row) {
+            uint8_t* bt = tiles + (size_t)s * p.stage_bytes + p.a_bytes;
+            const uint32_t qw[8] = {pq[slot][0].x, pq[slot][0].y, pq[slot][0].z, pq[slot][0].w,
+                                    pq[slot][1].x, pq[slot][1].y, pq[slot][1].z, pq[slot][1].w};
+            const uint32_t sc = ps[slot];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // 16-byte chunk c = elements 8c..8c+7
+              // the scale in BF16 (exact: at most 4 significant bits), twice
+              const uint32_t sb16 =
+                  __float_as_uint(e4m3_to_f32((sc >> (8 * (c >> 1))) & 0xffu)) >> 16;
+              const __nv_bfloat162 scale2 =
+                  __halves2bfloat162(__ushort_as_bfloat16((unsigned short)sb16),
+                                     __ushort_as_bfloat16((unsigned short)sb16));
+              uint32_t outw[4];
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                const uint32_t pair = s_lut[(qw[c] >> (8 * jj)) & 0xffu];
+                __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pair);
+                v = __hmul2(v, scale2);  // exact: the product has at most 6 significant bits
+                outw[jj] = *reinterpret_cast<const uint32_t*>(&v);
+              }
+              const int phys = c ^ (r & 7);  // 128-byte swizzle: chunk index XOR row mod 8
+              *reinterpret_cast<uint4*>(bt + (size_t)r * 128 + phys * 16) =
+                  make_uint4(outw[0], outw[1], outw[2], outw[3]);
+            }
+          }
+          GBR_FP4_LOAD(slot, kb + 2);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(smem_u32(&full[s]));
+        }
+      }
+#undef GBR_FP4_LOAD
+    }
     const bool ok = mbar_wait_warp(smem_u32(accf), 0);
     tc_fence_after();
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
@@ -529,66 +533,58 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
     int32_t* xi = reinterpret_cast<int32_t*>(xo + KC * BM);  // [KC][BM]
     float* xz = reinterpret_cast<float*>(xi + KC * BM);      // [KC][BM]
     float* xm = xz + KC * BM;                                 // [3][BM]
-    const int cap = p.cap, CP = p.cap + 1;
-    int32_t* cand_e = reinterpret_cast<int32_t*>(tiles + kCandOffset);
-    float* cand_z = reinterpret_cast<float*>(cand_e + 2 * BM * CP);
-    float* cand_k = cand_z + 2 * BM * CP;
-    const size_t my_list = (size_t)(half * BM + row) * CP;
+    float* zbuf = reinterpret_cast<float*>(tiles + kCandOffset);  // [E][BM] logits, column-major
     TopList<KC> top;
     top.init();
     float amax = 0.0f, kabs = 0.0f;
-    int ncand = 0;
-    bool overflow = false;
-    if (all_ok && !sp) {
-      // softmax: the key is the logit itself
-      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-        float v[32];
-        tmem_ld32(trow + c0, v);
+    if (all_ok) {
+      // Pass A: a lower bound L on this half's k-th largest logit, branch-free:
+      // the k-th largest of the maxima of G >= 2k interleaved column groups
+      // (k distinct experts are >= it). The half holds k experts with
+      // key >= a(L) + b_min, so an expert can reach the top k only if
+      // a(z) + b_max >= a(L) + b_min: z >= a^-1(a(L) - (b_max - b_min)).
+      // For softmax the key is the logit: z >= L.
+      constexpr int G = KC <= 4 ? 4 : (KC <= 6 ? 8 : (KC <= 10 ? 16 : 32));  // >= 2 (KC - 2) >= 2k
+      float gmax[G];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int e = c0 + j;
-          if (e < c_hi) {
-            const float z = FP4 ? v[j] * g : v[j];
-            top.push(ord_of(z), e, z);
-          }
-        }
-      }
-    } else if (all_ok) {
-      // Pass A: this half's k-th largest logit z_k. The half holds k experts
-      // with key >= a(z_k) + b_min, so an expert can reach the top k only if
-      // a(z) + b_max >= a(z_k) + b_min: z >= a^-1(a(z_k) - (b_max - b_min)).
-      uint32_t zo[KC];
-#pragma unroll
-      for (int j = 0; j < KC; ++j) zo[j] = 0u;
+      for (int q = 0; q < G; ++q) gmax[q] = -INFINITY;
       for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
         float v[32];
         tmem_ld32(trow + c0, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if (c0 + j < c_hi) {
-            const uint32_t o = ord_of(FP4 ? v[j] * g : v[j]);
-            if (o > zo[KC - 1]) {
-#pragma unroll
-              for (int q = KC - 1; q > 0; --q)
-                if (o > zo[q]) zo[q] = (o > zo[q - 1]) ? zo[q - 1] : o;
-              if (o > zo[0]) zo[0] = o;
-            }
+            const float z = FP4 ? v[j] * g : v[j];
+            gmax[j % G] = fmaxf(gmax[j % G], z);
+            zbuf[(c0 + j) * BM + row] = z;  // lanes store consecutive words
           }
         }
       }
-      uint32_t kth = 0xffffffffu;
+      // k-th largest of the G maxima: a sorted list of KC - 1 >= k values kept
+      // with min/max only (new[j] = max(old[j], min(old[j-1], x)))
+      float srt[KC - 1];
 #pragma unroll
-      for (int j = 0; j < KC; ++j)
-        if (j < k) kth = min(kth, zo[j]);
+      for (int j = 0; j < KC - 1; ++j) srt[j] = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < G; ++q) {
+        const float xq = gmax[q];
+#pragma unroll
+        for (int j = KC - 2; j > 0; --j) srt[j] = fmaxf(srt[j], fminf(srt[j - 1], xq));
+        srt[0] = fmaxf(srt[0], xq);
+      }
+      float lz = INFINITY;
+#pragma unroll
+      for (int j = 0; j < KC - 1; ++j)
+        if (j < k) lz = fminf(lz, srt[j]);
       // the threshold, rounded down with margins far above the FP32 errors of
       // sqrt_softplus (<= 2.25 ulp), expm1f and logf (<= 1 ulp each)
       float tz;
-      if (kth == 0u) {
-        tz = -INFINITY;  // fewer than k experts in this half: keep them all
-      } else if (!has_bias) {
-        tz = float_of_ord(kth);  // a is increasing: the top k by key are the top k by logit
+      if (!(lz > -INFINITY)) {
+        tz = -INFINITY;  // fewer than G experts in this half: keep them all
+      } else if (!sp || !has_bias) {
+        tz = lz;  // the key is increasing in the logit
       } else {
-        const float ak = sqrt_softplus_f32(float_of_ord(kth));
+        const float ak = sqrt_softplus_f32(lz);
         const float y = ak * (1.0f - 0x1p-20f) - (bmax - bmin) * (1.0f + 0x1p-20f) - 0x1p-40f;
         if (!(y > 0.0f)) {
           tz = -INFINITY;
@@ -597,58 +593,84 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
           tz = t - 0x1p-18f * (1.0f + fabsf(t));
         }
       }
-      // Pass B: compact this row-half's candidates into shared memory
-      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-        float v[32];
-        tmem_ld32(trow + c0, v);
+      // Pass B: a bit per candidate column, branch-free (at most 4 chunks of 32)
+      uint32_t cm[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int e = c0 + j;
-          if (e < c_hi) {
-            const float z = FP4 ? v[j] * g : v[j];
-            if (z >= tz) {
-              if (ncand < cap) {
-                cand_e[my_list + ncand] = e;
-                cand_z[my_list + ncand] = z;
-              }
-              ++ncand;
-            }
-          }
-        }
-      }
-      overflow = ncand > cap;
-      // Pass C: the activation for the candidates only, lanes in lockstep
-      const int nmax = (int)__reduce_max_sync(kFull, overflow ? 0u : (uint32_t)ncand);
-      for (int i = 0; i < nmax; ++i) {
-        if (!overflow && i < ncand) {
-          const int e = cand_e[my_list + i];
-          const float z = cand_z[my_list + i];
-          const float av = sqrt_softplus_f32(z);
-          const float key = has_bias ? av + __ldg(a.bias + e) : av;
-          cand_k[my_list + i] = key;
-          amax = fmaxf(amax, av);
-          kabs = fmaxf(kabs, fabsf(key));
-          top.push(ord_of(key), e, z);
-        }
-      }
-      if (__any_sync(kFull, overflow)) {  // too many candidates: every column of the half
-        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+      for (int ch = 0; ch < 4; ++ch) {
+        const int c0 = c_lo + 32 * ch;
+        if (c0 < c_hi) {
           float v[32];
           tmem_ld32(trow + c0, v);
-          if (overflow) {
+          uint32_t mbits = 0u;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int e = c0 + j;
-              if (e < c_hi) {
-                const float z = FP4 ? v[j] * g : v[j];
-                const float av = sqrt_softplus_f32(z);
-                const float key = has_bias ? av + __ldg(a.bias + e) : av;
-                amax = fmaxf(amax, av);
-                kabs = fmaxf(kabs, fabsf(key));
-                top.push(ord_of(key), e, z);
-              }
-            }
+          for (int j = 0; j < 32; ++j)
+            mbits |= ((c0 + j < c_hi) && (FP4 ? v[j] * g : v[j]) >= tz ? 1u : 0u) << j;
+          cm[ch] = mbits;
+        }
+      }
+      // Pass C. For sqrt-softplus the warp pools its 32 rows' candidates into
+      // one list and computes their activations spread evenly over the lanes,
+      // writing each score over its logit in the copy; then every row inserts
+      // its own candidates (lanes in lockstep, cheap). Softmax needs no
+      // activation: the key is the logit.
+      const int ncand = __popc(cm[0]) + __popc(cm[1]) + __popc(cm[2]) + __popc(cm[3]);
+      int off = ncand;  // inclusive warp scan of the counts
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(kFull, off, d);
+        if (lane >= d) off += t;
+      }
+      const int total = __shfl_sync(kFull, off, 31);
+      off -= ncand;
+      uint32_t* wl = reinterpret_cast<uint32_t*>(tiles + kCandOffset + (size_t)E * BM * 4) +
+                     warp * kListCap;
+      const bool shared_act = sp && total <= kListCap;
+      if (shared_act) {
+        uint32_t mm[4] = {cm[0], cm[1], cm[2], cm[3]};
+        int o = off;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          while (mm[ch]) {
+            const int col = 32 * ch + __ffs(mm[ch]) - 1;
+            mm[ch] &= mm[ch] - 1u;
+            wl[o++] = ((uint32_t)lane << 8) | (uint32_t)(c_lo + col);
           }
+        }
+        __syncwarp();
+        for (int t = lane; t < total; t += 32) {  // each item becomes its score
+          const uint32_t item = wl[t];
+          const int zi = (int)(item & 255u) * BM + quad * 32 + (int)(item >> 8);
+          wl[t] = __float_as_uint(sqrt_softplus_f32(zbuf[zi]));
+        }
+        __syncwarp();
+      }
+      const int nmax = (int)__reduce_max_sync(kFull, (uint32_t)ncand);
+      for (int i = 0; i < nmax; ++i) {
+        if (i < ncand) {
+          int col;
+          if (cm[0]) {
+            col = __ffs(cm[0]) - 1;
+            cm[0] &= cm[0] - 1u;
+          } else if (cm[1]) {
+            col = 31 + __ffs(cm[1]);
+            cm[1] &= cm[1] - 1u;
+          } else if (cm[2]) {
+            col = 63 + __ffs(cm[2]);
+            cm[2] &= cm[2] - 1u;
+          } else {
+            col = 95 + __ffs(cm[3]);
+            cm[3] &= cm[3] - 1u;
+          }
+          const int e = c_lo + col;
+          float sc = zbuf[e * BM + row];  // the score: the logit, or its activation
+          if (sp) sc = shared_act ? __uint_as_float(wl[off + i]) : sqrt_softplus_f32(sc);
+          float key = sc;
+          if (sp) {
+            key = has_bias ? sc + s_bias[e] : sc;
+            amax = fmaxf(amax, sc);
+            kabs = fmaxf(kabs, fabsf(key));
+          }
+          top.push(ord_of(key), e, sc);
         }
       }
     }
@@ -662,7 +684,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
       }
       xm[row] = amax;
       xm[BM + row] = kabs;
-      xm[2 * BM + row] = __int_as_float(overflow ? -1 : ncand);
+
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
     if (half == 0 && all_ok) {
@@ -670,8 +692,6 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
       for (int j = 0; j < KC; ++j) top.push(xo[j * BM + row], xi[j * BM + row], xz[j * BM + row]);
       amax = fmaxf(amax, xm[row]);
       kabs = fmaxf(kabs, xm[BM + row]);
-      const int ncand1 = __float_as_int(xm[2 * BM + row]);
-      const bool any_overflow = overflow || ncand1 < 0;
       // FP64 guard-band refine (see select.cuh)
       bool close = false;
       double band = 0.0;
@@ -692,20 +712,38 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
       for (int j = 0; j < KC; ++j)
         if (j < k) kth = min(kth, top.o[j]);
       const double thr = (double)float_of_ord(kth) - band;
-      if (close && !any_overflow) {
-        refine_candidates<KC>(cand_e + (size_t)row * CP, cand_z + (size_t)row * CP,
-                              cand_k + (size_t)row * CP, ncand,
-                              cand_e + (size_t)(BM + row) * CP, cand_z + (size_t)(BM + row) * CP,
-                              cand_k + (size_t)(BM + row) * CP, ncand1, a.bias, thr, band,
-                              xi + row, xz + row);
+      // Near ties inside the merged list: when every key at or above the band
+      // below the k-th is in the list, only list entries next to a gap of at
+      // most `band` need an FP64 key; the others keep their FP32 key, which
+      // orders them correctly against everything more than `band` away.
+      bool in_list = false;
+      if (close) {
+        const double lo = thr - band;
+        in_list = top.o[KC - 1] == 0u || (double)float_of_ord(top.o[KC - 1]) < lo;
+        if (in_list) {
+          double kd[KC];
 #pragma unroll
-        for (int j = 0; j < KC; ++j) {
-          top.i[j] = xi[j * BM + row];
-          top.z[j] = xz[j * BM + row];
+          for (int j = 0; j < KC; ++j) kd[j] = (double)float_of_ord(top.o[j]);
+          TopList64<KC> t64;
+          t64.init();
+#pragma unroll
+          for (int j = 0; j < KC; ++j) {
+            if (top.o[j] == 0u) continue;
+            const bool nr = kd[j] >= lo && ((j > 0 && kd[j - 1] - kd[j] <= band) ||
+                                            (j + 1 < KC && top.o[j + 1] != 0u &&
+                                             kd[j] - kd[j + 1] <= band));
+            const double key = nr ? key64(zbuf[top.i[j] * BM + row], a.bias, top.i[j]) : kd[j];
+            t64.push(key, top.i[j], top.z[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < KC; ++j) {
+            top.i[j] = t64.i[j];
+            top.z[j] = t64.z[j];
+          }
         }
       }
-      const bool slow = close && any_overflow;
-      if (__any_sync(kFull, slow)) {  // rows whose candidate lists overflowed
+      const bool slow = close && !in_list;
+      if (__any_sync(kFull, slow)) {  // near ties reaching past the list: every column
         refine_row<KC, FP4>(trow, E, g, a.bias, thr, slow, xi + row, xz + row);
         if (slow) {
 #pragma unroll
@@ -720,7 +758,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32, 
         float sum = 0.0f;
 #pragma unroll
         for (int j = 0; j < KC; ++j) {
-          sv[j] = sp ? sqrt_softplus_f32(top.z[j]) : expf(top.z[j] - top.z[0]);
+          sv[j] = sp ? top.z[j] : expf(top.z[j] - top.z[0]);  // the list keeps scores
           if (j < k) sum += sv[j];
         }
 #pragma unroll
@@ -806,7 +844,7 @@ cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcPara
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.a.M + BM - 1) / BM);
-  cfg.blockDim = dim3((kEpiWarps + 2 + (FP4 ? kDeqWarps : 0)) * 32);
+  cfg.blockDim = dim3((kEpiWarps + 2) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -820,12 +858,14 @@ cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcPara
 template <bool FP4>
 cudaError_t dispatch_k(const CUtensorMap& mx, const CUtensorMap& mw, const TcParams& p,
                        size_t smem, bool pdl, cudaStream_t s) {
+  // KC >= k + 2: the list keeps one key past the (k+1)-th, so a near tie at
+  // the k / k+1 boundary can be settled inside the list
   const int k = p.a.k;
-  if (k <= 2) return launch_kc<3, FP4>(mx, mw, p, smem, pdl, s);
-  if (k <= 4) return launch_kc<5, FP4>(mx, mw, p, smem, pdl, s);
-  if (k <= 6) return launch_kc<7, FP4>(mx, mw, p, smem, pdl, s);
-  if (k <= 8) return launch_kc<9, FP4>(mx, mw, p, smem, pdl, s);
-  return launch_kc<17, FP4>(mx, mw, p, smem, pdl, s);
+  if (k <= 2) return launch_kc<4, FP4>(mx, mw, p, smem, pdl, s);
+  if (k <= 4) return launch_kc<6, FP4>(mx, mw, p, smem, pdl, s);
+  if (k <= 6) return launch_kc<8, FP4>(mx, mw, p, smem, pdl, s);
+  if (k <= 8) return launch_kc<10, FP4>(mx, mw, p, smem, pdl, s);
+  return launch_kc<18, FP4>(mx, mw, p, smem, pdl, s);
 }
 
 }  // namespace
@@ -851,15 +891,10 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
   int cols = 32;
   while (cols < a.E) cols <<= 1;
   p.tmem_cols = cols;
-  // candidate lists reuse the tile ring after the main loop: 3 arrays of
-  // [2 halves][BM rows][cap + 1] 4-byte entries after the exchange area
-  const size_t ring = (size_t)S * p.stage_bytes;
-  const int per_half = (((a.E / 2) + 31) / 32) * 32;
-  long cap = ((long)ring - (long)kCandOffset) / (3L * 2 * BM * 4) - 1;
-  if (cap > 40) cap = 40;
-  if (cap > per_half) cap = per_half;
-  if (cap < 1) return cudaErrorInvalidValue;
-  p.cap = (int)cap;
+  // after the main loop the tile ring holds the exchange area and a copy
+  // of the logits [E][BM]
+  if ((size_t)S * p.stage_bytes < kCandOffset + (size_t)a.E * BM * 4 + (size_t)kEpiWarps * kListCap * 4)
+    return cudaErrorInvalidValue;
   const size_t smem = (size_t)S * p.stage_bytes + extra;
 
   CUtensorMap mx, mw;
