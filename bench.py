@@ -31,6 +31,27 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 LAYERS = 40          # router calls per decode token (one per MoE layer)
+
+# DRAM bytes per launch of the headline kernel from one ncu capture
+# (profiles/decode_router_m8_h2048_e256.md), valid only for the kernel
+# sources it was taken on.
+TRAFFIC = {"decode": {"bytes": 1163691, "src_sha": "3506906028364dd0"}}
+
+
+def kernel_src_sha():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "moe_expert_router_02_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(name):
+    t = TRAFFIC.get(name)
+    return t["bytes"] if t and t["src_sha"] == kernel_src_sha() else None
 W_POOL_BYTES = 520 << 20
 
 
@@ -353,7 +374,7 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}"},
         "us_per_call": us_call,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm"], "traffic": None,
+                     "frac": achieved / peaks["hbm"], "traffic": traffic_for("decode"),
                      "algo_bytes_per_call": algo, "peak_source": peaks["source"]},
         "e2e": {"value": e2e_value, "unit": "router tokens/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 2),
@@ -423,6 +444,30 @@ def run_detail(args, peaks):
     return out
 
 
+def run_only(args):
+    """Run one workload's router calls and print its per-call time (for
+    profiling the kernel of one configuration under ncu)."""
+    import torch
+
+    from moe_expert_router_02_gb300 import synth
+    C = synth.CONFIGS
+    table = {
+        "decode": lambda: RouterSet(C["C1"], 8, LAYERS),
+        "decode_m1": lambda: RouterSet(C["C1"], 1, LAYERS),
+        "sqrtsoftplus_m64": lambda: RouterSet(C["C2"], 64, LAYERS),
+        "m2_table": lambda: RouterSet(C["C4"], 2, LAYERS, table=True),
+        "prefill_bf16": lambda: RouterSet(C["C3"], C["C3"]["M"], 1, pool_bytes=0),
+        "prefill_nvfp4": lambda: RouterSet(C["C3"], C["C3"]["M"], 1, w_dtype=synth.NVFP4,
+                                           pool_bytes=0),
+    }
+    rs = table[args.only]()
+    rs.capture()
+    ms = time_graph(rs.step, args.steps, warm=args.warmup)
+    print(json.dumps({"workload": args.only, "us_per_call": ms * 1e3 / rs.calls,
+                      "calls_per_step": rs.calls, "steps": args.steps}))
+    torch.cuda.synchronize()
+
+
 def run_reference(args, rank, world):
     """CPU oracle on the headline workload (rank 0 only)."""
     if rank != 0:
@@ -467,7 +512,14 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only, no per-config detail")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-calls", type=int, default=8)
+    ap.add_argument("--only", default=None,
+                    choices=["decode", "decode_m1", "sqrtsoftplus_m64", "m2_table",
+                             "prefill_bf16", "prefill_nvfp4"],
+                    help="run one workload's calls only (profiling)")
     args = ap.parse_args()
+    if args.only:
+        run_only(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
