@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "kernels.h"
@@ -117,6 +118,38 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// TMA load delivered to the same shared-memory offset (and mbarrier offset)
+// in every CTA of the cluster named in cta_mask.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c0,
+                                               int c1, uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+// Arrive on the mbarrier at this offset in every CTA of cta_mask once the
+// MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_tc() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
 // 8-row core-matrix groups 1024 bytes apart, descriptor version 1.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
@@ -191,22 +224,25 @@ struct TopList {
       z[j] = 0.0f;
     }
   }
+  // Branch-free insertion (selects only): the lanes of a warp insert at
+  // different positions, and per-slot branches would diverge.
   __device__ __forceinline__ void push(uint32_t ok, int idx, float zz) {
     if (ok <= o[KC - 1]) return;
 #pragma unroll
     for (int j = KC - 1; j > 0; --j) {
-      if (ok > o[j]) {
-        const bool up = ok > o[j - 1];
-        o[j] = up ? o[j - 1] : ok;
-        i[j] = up ? i[j - 1] : idx;
-        z[j] = up ? z[j - 1] : zz;
-      }
+      const bool c = ok > o[j];
+      const bool u = ok > o[j - 1];
+      const uint32_t no = u ? o[j - 1] : ok;
+      const int ni = u ? i[j - 1] : idx;
+      const float nz = u ? z[j - 1] : zz;
+      o[j] = c ? no : o[j];
+      i[j] = c ? ni : i[j];
+      z[j] = c ? nz : z[j];
     }
-    if (ok > o[0]) {
-      o[0] = ok;
-      i[0] = idx;
-      z[0] = zz;
-    }
+    const bool c0 = ok > o[0];
+    o[0] = c0 ? ok : o[0];
+    i[0] = c0 ? idx : i[0];
+    z[0] = c0 ? zz : z[0];
   }
 };
 
@@ -296,6 +332,7 @@ struct TcParams {
   int stages;
   uint32_t stage_bytes, a_bytes, b_bytes;
   int tmem_cols;
+  int mc;  // CTAs per cluster sharing each W tile through TMA multicast (1 or 2)
 };
 
 // Serial unique-route table for one pair of rows (the thread owning the
@@ -355,13 +392,14 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int producer_warp = kEpiWarps, mma_warp = kEpiWarps + 1;
   const int m0 = blockIdx.x * BM;
+  const int crank = p.mc > 1 ? (int)cluster_rank() : 0;
   const int nk = a.H / BK;
   const int E = a.E;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), FP4 ? 1 + kEpiWarps * 32 : 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), (uint32_t)p.mc);  // one release per CTA using the stage
     }
     mbar_init(smem_u32(accf), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -396,7 +434,16 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         const uint32_t fb = smem_u32(&full[s]);
         mbar_expect_tx(fb, FP4 ? p.a_bytes : p.a_bytes + p.b_bytes);
         tma_load_2d(smem_u32(st), &tmap_x, kb * BK, m0, fb);
-        if (!FP4) tma_load_2d(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, 0, fb);
+        if (!FP4) {
+          if (p.mc == 1) {
+            tma_load_2d(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, 0, fb);
+          } else {
+            // this CTA's share of the W tile, written into every CTA of the pair
+            const int rows = E / p.mc;
+            tma_load_2d_mc(smem_u32(st + p.a_bytes + crank * rows * 128), &tmap_w, kb * BK,
+                           crank * rows, fb, (uint16_t)((1u << p.mc) - 1u));
+          }
+        }
         ++issued;
       }
       // let copies still in flight land before the CTA can exit
@@ -417,7 +464,8 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         for (int kk = 0; kk < BK / 16; ++kk)
           mma_bf16(tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32), idesc,
                    (kb > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&empty[s]));
+        if (p.mc == 1) mma_commit(smem_u32(&empty[s]));
+        else mma_commit_mc(smem_u32(&empty[s]), (uint16_t)((1u << p.mc) - 1u));
       }
       mma_commit(smem_u32(accf));
     }
@@ -647,21 +695,17 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       const int nmax = (int)__reduce_max_sync(kFull, (uint32_t)ncand);
       for (int i = 0; i < nmax; ++i) {
         if (i < ncand) {
-          int col;
-          if (cm[0]) {
-            col = __ffs(cm[0]) - 1;
-            cm[0] &= cm[0] - 1u;
-          } else if (cm[1]) {
-            col = 31 + __ffs(cm[1]);
-            cm[1] &= cm[1] - 1u;
-          } else if (cm[2]) {
-            col = 63 + __ffs(cm[2]);
-            cm[2] &= cm[2] - 1u;
-          } else {
-            col = 95 + __ffs(cm[3]);
-            cm[3] &= cm[3] - 1u;
-          }
-          const int e = c_lo + col;
+          // next candidate column, branch-free: the lowest set bit of the
+          // first non-empty chunk mask
+          const bool n0 = cm[0] != 0u, n1 = cm[1] != 0u, n2 = cm[2] != 0u;
+          const uint32_t mw = n0 ? cm[0] : (n1 ? cm[1] : (n2 ? cm[2] : cm[3]));
+          const int base = n0 ? 0 : (n1 ? 32 : (n2 ? 64 : 96));
+          const uint32_t rest = mw & (mw - 1u);
+          cm[0] = n0 ? rest : cm[0];
+          cm[1] = (!n0 && n1) ? rest : cm[1];
+          cm[2] = (!n0 && !n1 && n2) ? rest : cm[2];
+          cm[3] = (!n0 && !n1 && !n2) ? rest : cm[3];
+          const int e = c_lo + base + __ffs(mw) - 1;
           float sc = zbuf[e * BM + row];  // the score: the logit, or its activation
           if (sp) sc = shared_act ? __uint_as_float(wl[off + i]) : sqrt_softplus_f32(sc);
           float key = sc;
@@ -795,6 +839,8 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
 
   tc_fence_before();
   __syncthreads();
+  // the peer may still signal this CTA's barriers until it is done as well
+  if (p.mc > 1) cluster_sync_tc();
   if (warp == mma_warp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -843,15 +889,27 @@ cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcPara
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p.a.M + BM - 1) / BM);
+  const int tiles = (p.a.M + BM - 1) / BM;
+  cfg.gridDim = dim3((tiles + p.mc - 1) / p.mc * p.mc);
   cfg.blockDim = dim3((kEpiWarps + 2) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (p.mc > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = p.mc;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, mx, mw, p);
 }
 
@@ -897,11 +955,19 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   const size_t smem = (size_t)S * p.stage_bytes + extra;
 
+  // BF16 W can be shared by pairs of CTAs through TMA multicast
+  // (GBR_TC_MULTICAST=1 turns it on). Measured on GB300 it does not speed the
+  // main loop up, which is bound by shared-memory traffic rather than by L2.
+  static const int mc_env = [] {
+    const char* v = getenv("GBR_TC_MULTICAST");
+    return (v && v[0] == '1') ? 2 : 1;
+  }();
+  p.mc = (!fp4 && a.E % 16 == 0) ? mc_env : 1;
   CUtensorMap mx, mw;
   if (!make_map(&mx, a.x, a.M, a.H, BM)) return cudaErrorInvalidValue;
   if (fp4) {
     mw = mx;  // unused: W tiles are decoded by the kernel
-  } else if (!make_map(&mw, a.w, a.E, a.H, a.E)) {
+  } else if (!make_map(&mw, a.w, a.E, a.H, a.E / p.mc)) {
     return cudaErrorInvalidValue;
   }
   return fp4 ? dispatch_k<true>(mx, mw, p, smem, pdl, stream)
