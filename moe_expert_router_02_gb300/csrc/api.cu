@@ -47,7 +47,11 @@ int regime_of(const Shape& s) {
   if (f & GBR_FLAG_UNFUSED) return gv ? GBR_REGIME_UNFUSED : GBR_REGIME_GENERIC;
   if ((f & GBR_FLAG_FORCE_TC) && tc) return GBR_REGIME_TC;
   const bool one_cluster = gv && !(f & GBR_FLAG_NO_SINGLE_CLUSTER) &&
-                           gbr::gemv1c_eligible(s.M, s.H, s.E);
+                           gbr::gemv1c_eligible(s.M, s.H, s.E, false);
+  // NVFP4 weights at small M: only the single-cluster kernel decodes them
+  if (s.x_dtype == GBR_BF16 && s.w_dtype == GBR_NVFP4 && !(f & GBR_FLAG_NO_SINGLE_CLUSTER) &&
+      !(f & GBR_FLAG_FORCE_TC) && gbr::gemv1c_eligible(s.M, s.H, s.E, true))
+    return GBR_REGIME_GEMV1C;
   if ((f & GBR_FLAG_FORCE_GEMV) && gv) return one_cluster ? GBR_REGIME_GEMV1C : GBR_REGIME_GEMV;
   if (gv) return one_cluster ? GBR_REGIME_GEMV1C : GBR_REGIME_GEMV;
   if (tc && s.M > 64) return GBR_REGIME_TC;

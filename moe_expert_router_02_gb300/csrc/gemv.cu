@@ -268,41 +268,110 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   return true;
 }
 
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait with cluster-scope acquire (about one second of %globaltimer).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned* status) {
+  if (mbar_try_cluster(bar, parity)) return true;
+  uint64_t t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (!mbar_try_cluster(bar, parity)) {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > 1000000000ull) {
+      if (status) atomicOr(status, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Eight NVFP4 values (4 packed bytes, element 2j in the low nibble of byte j)
+// times their E4M3 block scale, as four BF16 pairs in memory order. Exact:
+// e2m1 * e4m3 has at most 6 significant bits and fits BF16's exponent range.
+__device__ __forceinline__ uint4 fp4_frag(uint32_t packed, uint8_t scale_code, const uint32_t* lut) {
+  const uint32_t sb = __float_as_uint(e4m3_to_f32(scale_code)) >> 16;
+  const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)sb),
+                                               __ushort_as_bfloat16((unsigned short)sb));
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t pair = lut[(packed >> (8 * j)) & 0xffu];
+    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pair);
+    v = __hmul2(v, s2);
+    o[j] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __device__ __forceinline__ void dsmem_st_f32(float* p, uint32_t rank, float v) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(r), "f"(v) : "memory");
 }
 
-template <int NT, int VPL>
+// NVFP4 weights: the CTA stages its 16 packed rows (pitch bytes apart) and
+// their E4M3 block scales; each 16-byte A fragment (8 BF16 values) is
+// decoded from 4 packed bytes through a byte -> two-BF16 table and one exact
+// BF16 multiply by the block scale, so the MMA sees W / g exactly and g
+// multiplies the FP32 sum.
+template <int NT, int VPL, bool FP4>
 __global__ void __launch_bounds__(k1cWarps * 32) k_gemv1c_router(const RouterArgs a, int pitch) {
   constexpr int NTOK = 8 * NT;
   extern __shared__ __align__(128) uint8_t s_w[];  // [16][pitch bytes]: this CTA's W rows
+  __shared__ uint32_t s_lut[FP4 ? 256 : 1];
   __shared__ float s_part[k1cWarps][16][NTOK];
   __shared__ float s_all[NTOK][kMaxE1c];  // CTA 0: every expert's logit, row by row
   __shared__ int32_t s_sel[k1cWarps * kMaxK];
   __shared__ int32_t s_rank[k1cWarps][32];
   __shared__ __align__(8) uint64_t s_bar;
+  __shared__ __align__(8) uint64_t s_join;  // CTA 0: one arrival per CTA once its logits are in
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const int rank = blockIdx.x;  // one cluster spans the grid
+  const int CL = gridDim.x;
   const int e0 = rank * 16;
   const int H = a.H, M = a.M, E = a.E;
   const uint32_t bar = smem_u32(&s_bar);
   const uint32_t wsm = smem_u32(s_w);
 
+  const int row_bytes = FP4 ? H / 2 : H * 2;
+  const int scale_bytes = FP4 ? 16 * (H / 16) : 0;
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&s_join)), "r"(CL)
+                 : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                 "r"((uint32_t)(16 * H * 2))
+                 "r"((uint32_t)(16 * row_bytes + scale_bytes))
                  : "memory");
   }
+  if (FP4) {
+    for (int b = tid; b < 256; b += k1cWarps * 32) {
+      const uint32_t lo = __float_as_uint(e2m1_to_f32(b & 15u)) >> 16;
+      const uint32_t hi = __float_as_uint(e2m1_to_f32((uint32_t)b >> 4)) >> 16;
+      s_lut[b] = lo | (hi << 16);
+    }
+  }
   __syncthreads();
+  // publish the join barrier's initialisation; the matching wait comes just
+  // before the first remote arrival, long after every CTA has arrived here
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   if (tid < 16) {  // this CTA's 16 W rows, one bulk copy per row into the padded pitch
-    const uint16_t* w = static_cast<const uint16_t*>(a.w) + (size_t)(e0 + tid) * H;
-    bulk_g2s(wsm + tid * pitch, w, H * 2, bar);
+    const uint8_t* w = static_cast<const uint8_t*>(a.w) + (size_t)(e0 + tid) * row_bytes;
+    bulk_g2s(wsm + tid * pitch, w, row_bytes, bar);
+  } else if (FP4 && tid == 16) {  // the 16 rows of block scales are contiguous
+    bulk_g2s(wsm + 16 * pitch, a.w_scales + (size_t)e0 * (H / 16), scale_bytes, bar);
   }
   pdl_launch_dependents();
   pdl_wait();  // x and the outputs belong to the preceding kernel until here
@@ -313,8 +382,10 @@ __global__ void __launch_bounds__(k1cWarps * 32) k_gemv1c_router(const RouterArg
   float acc[NT][4];
 #pragma unroll
   for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-  const uint8_t* w0 = s_w + g * pitch + 16 * t;
+  const uint8_t* w0 = s_w + g * pitch + (FP4 ? 4 : 16) * t;
   const uint8_t* w1 = w0 + 8 * pitch;
+  const uint8_t* sc0 = s_w + 16 * pitch + g * (H / 16) + (t >> 1);  // NVFP4 block scales
+  const uint8_t* sc1 = sc0 + 8 * (H / 16);
   bool w_ok = true;
   for (int jb = 0; jb < cpw; jb += k1cBatch) {
     uint4 xv[k1cBatch][NT];
@@ -334,8 +405,14 @@ __global__ void __launch_bounds__(k1cWarps * 32) k_gemv1c_router(const RouterArg
     for (int i = 0; i < k1cBatch; ++i) {
       if (jb + i < cpw && w_ok) {
         const int c = warp + k1cWarps * (jb + i);
-        const uint4 wa = *reinterpret_cast<const uint4*>(w0 + c * 64);
-        const uint4 wb = *reinterpret_cast<const uint4*>(w1 + c * 64);
+        uint4 wa, wb;
+        if (FP4) {
+          wa = fp4_frag(*reinterpret_cast<const uint32_t*>(w0 + c * 16), sc0[2 * c], s_lut);
+          wb = fp4_frag(*reinterpret_cast<const uint32_t*>(w1 + c * 16), sc1[2 * c], s_lut);
+        } else {
+          wa = *reinterpret_cast<const uint4*>(w0 + c * 64);
+          wb = *reinterpret_cast<const uint4*>(w1 + c * 64);
+        }
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           mma_bf16_16816(acc[n], wa.x, wb.x, wa.y, wb.y, xv[i][n].x, xv[i][n].y);
@@ -353,17 +430,26 @@ __global__ void __launch_bounds__(k1cWarps * 32) k_gemv1c_router(const RouterArg
     s_part[warp][g + 8][n * 8 + 2 * t + 1] = acc[n][3];
   }
   __syncthreads();
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   // sum the warps' partials in a fixed order and push them into CTA 0
   for (int i = tid; i < 16 * M; i += k1cWarps * 32) {
     const int m = i >> 4, el = i & 15;
     float v = s_part[0][el][m];
 #pragma unroll
     for (int w = 1; w < k1cWarps; ++w) v += s_part[w][el][m];
+    if (FP4) v *= a.w_global;
     dsmem_st_f32(&s_all[m][e0 + el], 0u, v);
     if (a.logits) a.logits[(size_t)m * E + e0 + el] = v;
   }
-  cluster_sync_all();  // every logit is in CTA 0; no shared memory is read remotely after this
-  if (rank != 0) return;
+  __syncthreads();  // this CTA's pushes happen before its arrival (the release is cumulative)
+  if (tid == 0) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(smem_u32(&s_join)));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(r)
+                 : "memory");
+  }
+  if (rank != 0) return;  // nothing reads this CTA's shared memory
+  if (!mbar_wait_cluster(smem_u32(&s_join), 0, a.status)) return;
 
   const bool table = a.tbl_unique != nullptr;
   const int k = a.k;
@@ -487,16 +573,26 @@ cudaError_t gemv_dispatch(const RouterArgs& a, int CL, bool pdl, cudaStream_t s)
   return gemv_dispatch_vpl<8, SELECT>(a, CL, pdl, s);
 }
 
-int gemv1c_pitch(int H) { return 2 * H + ((2 * H) % 128 == 0 ? 64 : 0); }
+// Row pitch of the staged W rows: BF16 rows padded to 64 (mod 128) bytes and
+// NVFP4 rows to 16 (mod 32) bytes, which keeps the fragment loads free of
+// bank conflicts.
+int gemv1c_pitch(int H, bool fp4) {
+  if (fp4) return H / 2 + ((H / 2) % 32 == 16 ? 0 : 16);
+  return 2 * H + ((2 * H) % 128 == 0 ? 64 : 0);
+}
+
+size_t gemv1c_smem(int H, bool fp4) {
+  return (size_t)16 * gemv1c_pitch(H, fp4) + (fp4 ? (size_t)16 * (H / 16) : 0);
+}
 
 // Launches (or, with probe, only sizes) the single-cluster kernel.
-template <int NT, int VPL>
+template <int NT, int VPL, bool FP4>
 cudaError_t launch_1c_inst(const RouterArgs& a, bool pdl, cudaStream_t stream, bool probe,
                            bool* fits) {
-  auto kern = k_gemv1c_router<NT, VPL>;
+  auto kern = k_gemv1c_router<NT, VPL, FP4>;
   const int CL = a.E / 16;
-  const int pitch = gemv1c_pitch(a.H);
-  const size_t dsmem = (size_t)16 * pitch;
+  const int pitch = gemv1c_pitch(a.H, FP4);
+  const size_t dsmem = gemv1c_smem(a.H, FP4);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dsmem);
   if (e != cudaSuccess) return e;
@@ -527,33 +623,39 @@ cudaError_t launch_1c_inst(const RouterArgs& a, bool pdl, cudaStream_t stream, b
   return cudaLaunchKernelEx(&cfg, kern, a, pitch);
 }
 
-template <int NT>
+template <int NT, bool FP4>
 cudaError_t launch_1c_vpl(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe, bool* fits) {
-  if (a.E <= 128) return launch_1c_inst<NT, 4>(a, pdl, s, probe, fits);
-  return launch_1c_inst<NT, 8>(a, pdl, s, probe, fits);
+  if (a.E <= 128) return launch_1c_inst<NT, 4, FP4>(a, pdl, s, probe, fits);
+  return launch_1c_inst<NT, 8, FP4>(a, pdl, s, probe, fits);
 }
 
 cudaError_t launch_1c(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe, bool* fits) {
-  if (a.M <= 8) return launch_1c_vpl<1>(a, pdl, s, probe, fits);
-  return launch_1c_vpl<2>(a, pdl, s, probe, fits);
+  const bool fp4 = a.w_dtype == DT_NVFP4;
+  if (a.M <= 8)
+    return fp4 ? launch_1c_vpl<1, true>(a, pdl, s, probe, fits)
+               : launch_1c_vpl<1, false>(a, pdl, s, probe, fits);
+  return fp4 ? launch_1c_vpl<2, true>(a, pdl, s, probe, fits)
+             : launch_1c_vpl<2, false>(a, pdl, s, probe, fits);
 }
 
 }  // namespace
 
-bool gemv1c_eligible(int M, int H, int E) {
-  if (M < 1 || M > 16 || E % 16 != 0 || E < 16 || E > 256 || H % 32 != 0) return false;
-  if ((size_t)16 * gemv1c_pitch(H) > (size_t)200 * 1024) return false;
+bool gemv1c_eligible(int M, int H, int E, bool fp4) {
+  if (M < 1 || M > 16 || E % 16 != 0 || E < 16 || E > 256 || H % (fp4 ? 256 : 32) != 0)
+    return false;
+  if (gemv1c_smem(H, fp4) > (size_t)200 * 1024) return false;
   // the cluster must be schedulable with this much shared memory per CTA
   static std::mutex mu;
   static std::map<std::tuple<int, int, int, int>, bool> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  const auto key = std::make_tuple(dev, M <= 8 ? 1 : 2, E, gemv1c_pitch(H));
+  const auto key = std::make_tuple(dev, (M <= 8 ? 1 : 2) + (fp4 ? 2 : 0), E, gemv1c_pitch(H, fp4));
   std::lock_guard<std::mutex> lk(mu);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
   RouterArgs probe_args{};
   probe_args.M = M, probe_args.H = H, probe_args.E = E;
+  probe_args.w_dtype = fp4 ? DT_NVFP4 : DT_BF16;
   bool fits = false;
   if (launch_1c(probe_args, true, 0, true, &fits) != cudaSuccess) fits = false;
   cache[key] = fits;

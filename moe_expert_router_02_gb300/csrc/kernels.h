@@ -19,7 +19,7 @@ int gemv_cluster_size(int H);
 cudaError_t launch_gemv(const RouterArgs& a, bool select, bool pdl, cudaStream_t stream);
 
 // Small-M single-cluster router (M <= 16, E <= 256, W_gate in shared memory).
-bool gemv1c_eligible(int M, int H, int E);
+bool gemv1c_eligible(int M, int H, int E, bool fp4);
 cudaError_t launch_gemv1c(const RouterArgs& a, bool pdl, cudaStream_t stream);
 
 // Row-per-CTA router for any dtype and shape.

@@ -180,11 +180,22 @@ def test_single_cluster_hidden_limits(H):
     check_case(synth.make_case(cfg, M=4, seed=H))
 
 
-def test_nvfp4_weights_small_M():
-    case = synth.make_case(C["C2"], M=8, seed=4, w_dtype=synth.NVFP4)
-    check_case(case)
-    case = synth.make_case(C["C2"], M=2, seed=4, w_dtype=synth.NVFP4, nvfp4_global=0.5)
-    check_case(case)
+@pytest.mark.parametrize("M", [1, 2, 8, 16])
+def test_nvfp4_weights_small_M(M):
+    case = synth.make_case(C["C2"], M=M, seed=4 + M, w_dtype=synth.NVFP4)
+    check_case(case, expect_regime=R.GBR_REGIME_GEMV1C)
+    case = synth.make_case(C["C2"], M=M, seed=4, w_dtype=synth.NVFP4, nvfp4_global=0.5)
+    check_case(case, table=(M % 2 == 0))
+    softmax = dict(C["C1"], H=2048)
+    check_case(synth.make_case(softmax, M=M, seed=M, w_dtype=synth.NVFP4))
+
+
+def test_nvfp4_small_M_other_paths():
+    # 16 < M <= 64 and H not a multiple of 256 take the generic kernel
+    check_case(synth.make_case(C["C2"], M=33, seed=1, w_dtype=synth.NVFP4),
+               expect_regime=R.GBR_REGIME_GENERIC)
+    check_case(synth.make_case(dict(C["C2"], H=1056), M=4, seed=2, w_dtype=synth.NVFP4),
+               expect_regime=R.GBR_REGIME_GENERIC)
 
 
 def test_repeated_calls_reuse_workspace_and_ticket():
