@@ -64,6 +64,8 @@ size_t workspace_for(const Shape& s, int regime) {
   // workspace sized on one device also fits a device where it is not chosen.
   if (regime == GBR_REGIME_GEMV || regime == GBR_REGIME_GEMV1C || regime == GBR_REGIME_UNFUSED)
     return kTicketBytes + round_up((size_t)s.M * s.E * 4, 256);
+  // the prefill kernel decodes NVFP4 W once per launch into the workspace
+  if (regime == GBR_REGIME_TC) return gbr::tc_workspace(s.H, s.E, s.w_dtype);
   return 0;
 }
 
@@ -213,6 +215,7 @@ int router_forward_ex(const void* x, const void* W_gate, const float* bias, int 
       break;
     }
     case GBR_REGIME_TC:
+      a.ticket = static_cast<uint32_t*>(ws);
       err = gbr::launch_tc(a, pdl, stream);
       break;
     default:

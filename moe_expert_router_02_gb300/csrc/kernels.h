@@ -28,6 +28,9 @@ cudaError_t launch_generic(const RouterArgs& a, bool pdl, cudaStream_t stream);
 // tcgen05 prefill router.
 bool tc_eligible(int M, int H, int E, int k, int x_dtype, int w_dtype);
 cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream);
+// Workspace the prefill router needs (NVFP4 W: flags and the decoded copy);
+// launch_tc takes it as RouterArgs::ticket.
+size_t tc_workspace(int H, int E, int w_dtype);
 int tc_read_status(int clear);  // 0 ok, 1 a bounded wait expired, -1 query failed
 unsigned* status_word();        // device address of that status word (current device)
 

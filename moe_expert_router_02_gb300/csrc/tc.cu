@@ -139,6 +139,39 @@ __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
       : "memory");
 }
 
+// 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait for a flag in global memory to take the value want.
+__device__ __forceinline__ bool wait_flag(const unsigned* f, unsigned want) {
+  if (ld_acquire_u32(f) == want) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t ns = 32;
+  while (ld_acquire_u32(f) != want) {
+    __nanosleep(ns);
+    if (ns < 256) ns <<= 1;
+    if (globaltimer() - t0 > kWaitNs) {
+      atomicOr(&g_tc_status, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -333,6 +366,11 @@ struct TcParams {
   uint32_t stage_bytes, a_bytes, b_bytes;
   int tmem_cols;
   int mc;  // CTAs per cluster sharing each W tile through TMA multicast (1 or 2)
+  // NVFP4 only, both in the workspace: W decoded to BF16 (one swizzled
+  // [E x 64] tile per k-step), and [0] claim counter, [1] epoch, [2 + kb]
+  // flag of tile kb
+  uint8_t* wdec;
+  unsigned* wsync;
 };
 
 // Serial unique-route table for one pair of rows (the thread owning the
@@ -376,6 +414,8 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
                 const __grid_constant__ CUtensorMap tmap_w, const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t s_lut[256];  // NVFP4: byte of two E2M1 codes -> two BF16 values
+  __shared__ __align__(8) uint64_t s_wready;  // NVFP4: s_epoch is set
+  __shared__ unsigned s_epoch, s_claim;
   __shared__ float s_bias[256];    // the selection bias (sqrt-softplus)
   const RouterArgs& a = p.a;
   const int S = p.stages;
@@ -398,10 +438,11 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&full[s]), FP4 ? 1 + kEpiWarps * 32 : 1);
+      mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), (uint32_t)p.mc);  // one release per CTA using the stage
     }
     mbar_init(smem_u32(accf), 1);
+    if (FP4) mbar_init(smem_u32(&s_wready), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == mma_warp) {
@@ -426,15 +467,26 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
                      : "memory");
       pdl_wait();
       int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
+      unsigned want = 0u;  // NVFP4: the flag value of a tile decoded by this launch
+      bool go = true;
+      if (FP4) {
+        go = mbar_wait(smem_u32(&s_wready), 0);
+        want = *reinterpret_cast<volatile unsigned*>(&s_epoch) + 1u;
+      }
+      for (int kb = 0; kb < nk && go; ++kb) {
         const int s = kb % S;
         const uint32_t ph = (uint32_t)(kb / S) & 1u;
         if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) break;
         uint8_t* st = tiles + (size_t)s * p.stage_bytes;
         const uint32_t fb = smem_u32(&full[s]);
-        mbar_expect_tx(fb, FP4 ? p.a_bytes : p.a_bytes + p.b_bytes);
+        mbar_expect_tx(fb, p.a_bytes + p.b_bytes);
         tma_load_2d(smem_u32(st), &tmap_x, kb * BK, m0, fb);
-        if (!FP4) {
+        ++issued;
+        if (FP4) {
+          if (!wait_flag(p.wsync + 2 + kb, want)) break;
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          bulk_load(smem_u32(st + p.a_bytes), p.wdec + (size_t)kb * p.b_bytes, p.b_bytes, fb);
+        } else {
           if (p.mc == 1) {
             tma_load_2d(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, 0, fb);
           } else {
@@ -444,7 +496,6 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
                            crank * rows, fb, (uint16_t)((1u << p.mc) - 1u));
           }
         }
-        ++issued;
       }
       // let copies still in flight land before the CTA can exit
       for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
@@ -500,77 +551,74 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       for (int e = lane; e < E; e += 32) s_bias[e] = __ldg(a.bias + e);
     asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
     if (FP4) {
-      // During the main loop these warps decode W: thread t owns row t of
-      // every E x 64 BF16 tile; the packed bytes and scales of k-step kb + 2
-      // are loaded while kb is decoded.
+      // NVFP4: W is decoded once per launch, not once per CTA. The CTAs claim
+      // k-step tiles from a counter in the workspace; the 256 threads of a
+      // claim decode the tile (thread r owns row r) into the exact BF16
+      // [E x 64] layout the MMA reads, 128-byte swizzle included, and flag
+      // it with this launch's epoch; producers copy flagged tiles as they are.
+      // Claims never wait, so no CTA needs another to be resident. Each CTA
+      // makes one failing claim; the last of them (ticket nk + grid - 1)
+      // resets the counter and advances the epoch for the next launch.
       const int r = threadIdx.x;  // 0..255
       for (int b = r; b < 256; b += kEpiWarps * 32) {
         const uint32_t lo = __float_as_uint(e2m1_to_f32(b & 15u)) >> 16;
         const uint32_t hi = __float_as_uint(e2m1_to_f32((uint32_t)b >> 4)) >> 16;
         s_lut[b] = lo | (hi << 16);
       }
-      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+      pdl_wait();  // the decoded copy is read by the preceding launch until here
+      if (r == 0) {
+        s_epoch = ld_acquire_u32(p.wsync + 1);
+        mbar_arrive(smem_u32(&s_wready));
+      }
       const uint8_t* qp = static_cast<const uint8_t*>(a.w);
       const int Hb = a.H / 2, Hs = a.H / 16;
-      const bool has_row = r < E;
-      uint4 pq[2][2];  // [slot][half of the 32 packed bytes]
-      uint32_t ps[2];  // [slot] four E4M3 scales
-#define GBR_FP4_LOAD(slot, kbl)                                                                  \
-  do {                                                                                           \
-    if ((kbl) < nk && has_row) {                                                                 \
-      const uint4* src = reinterpret_cast<const uint4*>(qp + (size_t)r * Hb + (kbl) * (BK / 2)); \
-      pq[slot][0] = __ldg(src);                                                                  \
-      pq[slot][1] = __ldg(src + 1);                                                              \
-      ps[slot] = __ldg(                                                                          \
-          reinterpret_cast<const uint32_t*>(a.w_scales + (size_t)r * Hs + (kbl) * (BK / 16)));   \
-    }                                                                                            \
-  } while (0)
-      GBR_FP4_LOAD(0, 0);
-      GBR_FP4_LOAD(1, 1);
-      bool dec_ok = true;
-      for (int kb2 = 0; kb2 < nk && dec_ok; kb2 += 2) {
-#pragma unroll
-        for (int slot = 0; slot < 2; ++slot) {  // unrolled so the register slots are static
-          const int kb = kb2 + slot;
-          if (kb >= nk) break;
-          const int s = kb % S;
-          const uint32_t ph = (uint32_t)(kb / S) & 1u;
-          if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1u)) {
-            dec_ok = false;
-            break;
+      const unsigned nclaim = (unsigned)nk + gridDim.x;
+      for (;;) {
+        if (r == 0) {
+          const unsigned t = atomicAdd(p.wsync, 1u);
+          if (t == nclaim - 1u) {  // every claim of this launch is in
+            asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(p.wsync) : "memory");
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.wsync + 1) : "memory");
           }
-          if (has_row) {
-            uint8_t* bt = tiles + (size_t)s * p.stage_bytes + p.a_bytes;
-            const uint32_t qw[8] = {pq[slot][0].x, pq[slot][0].y, pq[slot][0].z, pq[slot][0].w,
-                                    pq[slot][1].x, pq[slot][1].y, pq[slot][1].z, pq[slot][1].w};
-            const uint32_t sc = ps[slot];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {  // 16-byte chunk c = elements 8c..8c+7
-              // the scale in BF16 (exact: at most 4 significant bits), twice
-              const uint32_t sb16 =
-                  __float_as_uint(e4m3_to_f32((sc >> (8 * (c >> 1))) & 0xffu)) >> 16;
-              const __nv_bfloat162 scale2 =
-                  __halves2bfloat162(__ushort_as_bfloat16((unsigned short)sb16),
-                                     __ushort_as_bfloat16((unsigned short)sb16));
-              uint32_t outw[4];
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                const uint32_t pair = s_lut[(qw[c] >> (8 * jj)) & 0xffu];
-                __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pair);
-                v = __hmul2(v, scale2);  // exact: the product has at most 6 significant bits
-                outw[jj] = *reinterpret_cast<const uint32_t*>(&v);
-              }
-              const int phys = c ^ (r & 7);  // 128-byte swizzle: chunk index XOR row mod 8
-              *reinterpret_cast<uint4*>(bt + (size_t)r * 128 + phys * 16) =
-                  make_uint4(outw[0], outw[1], outw[2], outw[3]);
-            }
-          }
-          GBR_FP4_LOAD(slot, kb + 2);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arrive(smem_u32(&full[s]));
+          s_claim = t;
         }
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+        const unsigned t = *reinterpret_cast<volatile unsigned*>(&s_claim);
+        const unsigned want = *reinterpret_cast<volatile unsigned*>(&s_epoch) + 1u;
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+        if (t >= (unsigned)nk) break;
+        if (r < E) {
+          const uint4* src = reinterpret_cast<const uint4*>(qp + (size_t)r * Hb + t * (BK / 2));
+          const uint4 q0 = __ldg(src), q1 = __ldg(src + 1);
+          const uint32_t sc =
+              __ldg(reinterpret_cast<const uint32_t*>(a.w_scales + (size_t)r * Hs + t * (BK / 16)));
+          const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          uint8_t* dst = p.wdec + (size_t)t * p.b_bytes + (size_t)r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {  // 16-byte chunk c = elements 8c..8c+7
+            // the block scale in BF16 (exact: at most 4 significant bits), twice
+            const uint32_t sb16 = __float_as_uint(e4m3_to_f32((sc >> (8 * (c >> 1))) & 0xffu)) >> 16;
+            const __nv_bfloat162 scale2 = __halves2bfloat162(
+                __ushort_as_bfloat16((unsigned short)sb16), __ushort_as_bfloat16((unsigned short)sb16));
+            uint32_t outw[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const uint32_t pair = s_lut[(qw[c] >> (8 * jj)) & 0xffu];
+              __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pair);
+              v = __hmul2(v, scale2);  // exact: the product has at most 6 significant bits
+              outw[jj] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+            const int phys = c ^ (r & 7);  // 128-byte swizzle: chunk index XOR row mod 8
+            *reinterpret_cast<uint4*>(dst + phys * 16) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+          }
+        }
+        // the producers read the tile through the async proxy
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+        if (r == 0)
+          asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.wsync + 2 + t), "r"(want)
+                       : "memory");
       }
-#undef GBR_FP4_LOAD
     }
     const bool ok = mbar_wait_warp(smem_u32(accf), 0);
     tc_fence_after();
@@ -761,24 +809,67 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       // most `band` need an FP64 key; the others keep their FP32 key, which
       // orders them correctly against everything more than `band` away.
       bool in_list = false;
+      double kd[KC];
+      uint32_t need = 0u;  // list entries that take an FP64 key
+#pragma unroll
+      for (int j = 0; j < KC; ++j) kd[j] = (double)float_of_ord(top.o[j]);
       if (close) {
         const double lo = thr - band;
-        in_list = top.o[KC - 1] == 0u || (double)float_of_ord(top.o[KC - 1]) < lo;
+        in_list = top.o[KC - 1] == 0u || kd[KC - 1] < lo;
         if (in_list) {
-          double kd[KC];
 #pragma unroll
-          for (int j = 0; j < KC; ++j) kd[j] = (double)float_of_ord(top.o[j]);
+          for (int j = 0; j < KC; ++j) {
+            const bool nr = top.o[j] != 0u && kd[j] >= lo &&
+                            ((j > 0 && kd[j - 1] - kd[j] <= band) ||
+                             (j + 1 < KC && top.o[j + 1] != 0u && kd[j] - kd[j + 1] <= band));
+            need |= (nr ? 1u : 0u) << j;
+          }
+        }
+      }
+      // The FP64 keys are slow on this part (~3400 cycles each), so the warp
+      // pools the entries its rows need and evaluates them one per lane;
+      // each owner then gathers its keys back with shuffles.
+      const int nneed = __popc(need);
+      int qoff = nneed;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(kFull, qoff, d);
+        if (lane >= d) qoff += t;
+      }
+      const int qtotal = __shfl_sync(kFull, qoff, 31);
+      qoff -= nneed;
+      if (qtotal > 0) {
+        uint32_t* wl = reinterpret_cast<uint32_t*>(tiles + kCandOffset + (size_t)E * BM * 4) +
+                       warp * kListCap;  // this warp's candidate list is spent
+        {
+          int q = qoff;
+#pragma unroll
+          for (int j = 0; j < KC; ++j)
+            if ((need >> j) & 1u)
+              wl[q++] = ((uint32_t)top.i[j] << 16) | ((uint32_t)lane << 5) | (uint32_t)j;
+        }
+        __syncwarp();
+        for (int base = 0; base < qtotal; base += 32) {
+          double key = 0.0;
+          if (base + lane < qtotal) {
+            const uint32_t item = wl[base + lane];
+            const int e = (int)(item >> 16);
+            key = key64(zbuf[e * BM + quad * 32 + (int)((item >> 5) & 31u)], a.bias, e);
+          }
+#pragma unroll
+          for (int j = 0; j < KC; ++j) {
+            const int qj = qoff + __popc(need & ((1u << j) - 1u));
+            const bool mine = ((need >> j) & 1u) && qj >= base && qj < base + 32;
+            const double kv = __shfl_sync(kFull, key, mine ? qj - base : lane);
+            if (mine) kd[j] = kv;
+          }
+        }
+        if (need != 0u) {
           TopList64<KC> t64;
           t64.init();
 #pragma unroll
-          for (int j = 0; j < KC; ++j) {
-            if (top.o[j] == 0u) continue;
-            const bool nr = kd[j] >= lo && ((j > 0 && kd[j - 1] - kd[j] <= band) ||
-                                            (j + 1 < KC && top.o[j + 1] != 0u &&
-                                             kd[j] - kd[j + 1] <= band));
-            const double key = nr ? key64(zbuf[top.i[j] * BM + row], a.bias, top.i[j]) : kd[j];
-            t64.push(key, top.i[j], top.z[j]);
-          }
+          for (int j = 0; j < KC; ++j)
+            if (top.o[j] != 0u) t64.push(kd[j], top.i[j], top.z[j]);
 #pragma unroll
           for (int j = 0; j < KC; ++j) {
             top.i[j] = t64.i[j];
@@ -933,10 +1024,26 @@ bool tc_eligible(int M, int H, int E, int k, int x_dtype, int w_dtype) {
          E % 16 == 0 && E >= 16 && E <= 256 && H % BK == 0 && k <= kMaxK;
 }
 
+// NVFP4 workspace: the tile flags (after the claim counter and the epoch),
+// then the decoded W at a 256-byte boundary.
+static size_t tc_flag_bytes(int H) {
+  return ((size_t)(2 + H / BK) * 4 + 255) / 256 * 256;
+}
+
+size_t tc_workspace(int H, int E, int w_dtype) {
+  if (w_dtype != DT_NVFP4) return 0;
+  return tc_flag_bytes(H) + (size_t)E * H * 2;
+}
+
 cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
   const bool fp4 = a.w_dtype == DT_NVFP4;
   TcParams p{};
   p.a = a;
+  if (fp4) {
+    if (!a.ticket) return cudaErrorInvalidValue;
+    p.wsync = a.ticket;
+    p.wdec = reinterpret_cast<uint8_t*>(a.ticket) + tc_flag_bytes(a.H);
+  }
   p.a_bytes = BM * BK * 2;
   p.b_bytes = (uint32_t)a.E * BK * 2;
   p.stage_bytes = p.a_bytes + p.b_bytes;
@@ -966,7 +1073,7 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
   CUtensorMap mx, mw;
   if (!make_map(&mx, a.x, a.M, a.H, BM)) return cudaErrorInvalidValue;
   if (fp4) {
-    mw = mx;  // unused: W tiles are decoded by the kernel
+    mw = mx;  // unused: the decoded W tiles arrive by 1-D bulk copies
   } else if (!make_map(&mw, a.w, a.E, a.H, a.E / p.mc)) {
     return cudaErrorInvalidValue;
   }

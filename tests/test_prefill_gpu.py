@@ -47,6 +47,32 @@ def test_nvfp4_weights(glob):
     check_case(case, expect_regime=R.GBR_REGIME_TC)
 
 
+def test_nvfp4_decode_claims_reset_across_launches():
+    """NVFP4 W is decoded once per launch into the workspace, in k-step tiles
+    claimed from a counter and flagged with a per-launch epoch. One caller
+    workspace serves launches of different grid sizes, hidden sizes and
+    weights back to back: a stale tile or a counter left over from the
+    previous launch would route against the wrong W."""
+    import torch
+    from tests.helpers import empty_outputs
+    cases = [small_prefill(M, H=H, seed=20 + M, w_dtype=synth.NVFP4)
+             for M, H in ((300, 1024), (1000, 1024), (130, 2048), (129, 512), (2000, 1024))]
+    probe = R.make_opts(w_dtype=synth.NVFP4, w_scales=1)
+    need = max(R.router_workspace_size(c["M"], c["H"], c["E"], c["k"], probe) for c in cases)
+    assert need >= 2048 * 256 * 2
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for c in cases:
+        t = upload(c)
+        idx, w = empty_outputs(c["M"], c["k"])
+        opts = R.make_opts(x_dtype=c["x_dtype"], w_dtype=c["w_dtype"], w_scales=t["scales"],
+                           w_global_scale=c["g"], workspace=ws, workspace_bytes=need)
+        R.router_forward_ex(t["x"], t["W"], t["bias"], c["M"], c["H"], c["E"], c["k"], c["act"],
+                            idx, w, opts)
+        torch.cuda.synchronize()
+        ref = oracle.router(c)
+        check_routes(idx.cpu().numpy(), w.cpu().numpy(), ref["idx"], ref["w"], ref["keys"], c["k"])
+
+
 def test_fused_table():
     check_case(small_prefill(256, k=6, seed=9), table=True)
 
