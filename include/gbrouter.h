@@ -155,6 +155,20 @@ int router_select(const float* logits, const float* bias, int M, int E, int k, i
                   int32_t* out_idx, float* out_w, cudaStream_t stream);
 
 /*
+ * router_near_tie_keys — the key the selection re-ranks near ties with
+ * (sqrt-softplus + bias only): key[i] = sqrt(softplus(z[i])) + bias[i]
+ * (bias nullable: 0) returned as an unevaluated sum key_hi[i] + key_lo[i]
+ * of two floats with |lo| <= ulp(hi)/2, from FP32 arithmetic only
+ * (double-float evaluation, relative error near 2^-42; |z| > 30 goes
+ * through FP64). Step 2 of the router as the guard-band refine evaluates
+ * it; exposed so that its error can be measured against an FP64
+ * definition. z, bias, key_hi, key_lo: device FP32 [n]. Errors: GBR_EINVAL
+ * for n < 0 or null z / key pointers (n == 0: no launch).
+ */
+int router_near_tie_keys(const float* z, const float* bias, int n, float* key_hi, float* key_lo,
+                         cudaStream_t stream);
+
+/*
  * route_table — step 5 alone for `groups` groups of T = tokens_per_group
  * rows (1 <= T <= 8), k slots each (1 <= k <= 16):
  *   idx        int32 [groups, T, k]  expert ids (expected >= 0)

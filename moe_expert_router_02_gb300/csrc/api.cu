@@ -243,6 +243,15 @@ int router_select(const float* logits, const float* bias, int M, int E, int k, i
              : GBR_ECUDA;
 }
 
+int router_near_tie_keys(const float* z, const float* bias, int n, float* key_hi, float* key_lo,
+                         cudaStream_t stream) {
+  if (n < 0) return GBR_EINVAL;
+  if (n == 0) return GBR_OK;
+  if (!z || !key_hi || !key_lo) return GBR_EINVAL;
+  return gbr::launch_near_tie_keys(z, bias, n, key_hi, key_lo, stream) == cudaSuccess ? GBR_OK
+                                                                                       : GBR_ECUDA;
+}
+
 int route_table(const int32_t* idx, int groups, int tokens_per_group, int k, int32_t* out_unique,
                 uint8_t* out_mask, uint8_t* out_map, int32_t* out_count, cudaStream_t stream) {
   if (groups < 0 || tokens_per_group < 1 || tokens_per_group > 8 || k < 1 || k > gbr::kMaxK)

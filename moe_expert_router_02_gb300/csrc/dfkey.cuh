@@ -1,0 +1,224 @@
+// Near-tie keys in double-float ("float-float") arithmetic.
+//
+// The selection re-ranks experts whose FP32 keys sqrt(softplus(z)) + b lie
+// within the FP32 error band of the k-th (the FP64 guard band). FP64
+// transcendentals run at a small fraction of the FP32 rate on this part
+// (one FP64 sqrt(softplus) costs a warp some 24,000 cycles), so the key is
+// evaluated as an unevaluated sum hi + lo of two floats with a relative
+// error near 2^-42, from FP32 operations only. A pair of keys closer than
+// the bound kDfRel allows (and not computed from identical inputs) still
+// goes to FP64 (key64 in the callers): the double-float keys only decide
+// the orders that FP64 would decide the same way.
+//
+// Methods: error-free sum and product (Knuth's TwoSum, Dekker's Fast2Sum,
+// the FMA product residual) and Dekker's double-length multiplication;
+// exp by Cody and Waite's argument reduction with ln 2 split in three
+// parts, a short Taylor series of expm1 in double-float on x / 16 and four
+// doublings expm1(2y) = expm1(y) (expm1(y) + 2); log1p by one Newton step
+// on e^y - 1 - u from the FP32 log1pf; sqrt by one Newton (Heron) step.
+// The constants are ln 2 and 1/k! rounded to float: C1 is ln 2 to 15
+// significant bits (n * C1 is exact for n < 2^8), C2 and C3 the next
+// float-rounded parts (C1 + C2 + C3 - ln 2 = -1.3e-21).
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace gbr {
+
+struct df32 {
+  float hi, lo;
+};
+
+__device__ __forceinline__ df32 two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+
+// |a| >= |b| (or a == 0)
+__device__ __forceinline__ df32 fast_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ df32 two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return {p, __fmaf_rn(a, b, -p)};
+}
+
+__device__ __forceinline__ df32 df_add(df32 x, df32 y) {
+  df32 s = two_sum(x.hi, y.hi);
+  const df32 t = two_sum(x.lo, y.lo);
+  s.lo = __fadd_rn(s.lo, t.hi);
+  s = fast_two_sum(s.hi, s.lo);
+  s.lo = __fadd_rn(s.lo, t.lo);
+  return fast_two_sum(s.hi, s.lo);
+}
+
+__device__ __forceinline__ df32 df_add_f(df32 x, float b) {
+  df32 s = two_sum(x.hi, b);
+  s.lo = __fadd_rn(s.lo, x.lo);
+  return fast_two_sum(s.hi, s.lo);
+}
+
+__device__ __forceinline__ df32 df_mul(df32 x, df32 y) {
+  df32 p = two_prod(x.hi, y.hi);
+  p.lo = __fmaf_rn(x.hi, y.lo, p.lo);
+  p.lo = __fmaf_rn(x.lo, y.hi, p.lo);
+  return fast_two_sum(p.hi, p.lo);
+}
+
+__device__ __forceinline__ df32 df_scale(df32 x, float pow2) {  // exact for powers of two
+  return {__fmul_rn(x.hi, pow2), __fmul_rn(x.lo, pow2)};
+}
+
+// expm1(x) for |x| <= 0.75, relative error about 2^-43. Out of line: the
+// two calls in sqrt_softplus_df share one copy.
+static __device__ __noinline__ df32 expm1_df(df32 x) {
+  const df32 y = df_scale(x, 0x1p-4f);  // |y| <= 0.047
+  const df32 y2 = df_mul(y, y);
+  const df32 y3 = df_mul(y2, y);
+  const df32 y4 = df_mul(y2, y2);
+  // y^5 / 5! .. y^8 / 8! in FP32: at most 3e-8 of the result, so their
+  // rounding stays near 2^-47 of it; the first dropped term is 3e-17 of it
+  const float t = y.hi;
+  float tail = __fmaf_rn(t, 0x1.a01a02p-16f, 0x1.a01a02p-13f);
+  tail = __fmaf_rn(t, tail, 0x1.6c16c2p-10f);
+  tail = __fmaf_rn(t, tail, 0x1.111112p-7f);
+  tail = __fmul_rn(tail, __fmul_rn(y4.hi, t));
+  df32 e = df_add_f(df_mul(y4, df32{0x1.555556p-5f, -0x1.555556p-30f}), tail);  // + y^4 / 24
+  e = df_add(e, df_mul(y3, df32{0x1.555556p-3f, -0x1.555556p-28f}));           // + y^3 / 6
+  e = df_add(e, df_scale(y2, 0.5f));                                            // + y^2 / 2
+  e = df_add(e, y);                                                             // + y
+#pragma unroll
+  for (int i = 0; i < 4; ++i) e = df_mul(e, df_add_f(e, 2.0f));  // expm1(2v) from expm1(v)
+  return e;
+}
+
+// Largest |z| the double-float path takes; beyond it the callers use FP64.
+constexpr float kDfMaxAbsZ = 30.0f;
+// Bound used to call two double-float keys distinct: |key_a - key_b| must
+// exceed kDfRel * (s_a + |key_a| + s_b + |key_b|). The evaluation error is
+// near 2^-42 relative; the margin is 64x.
+constexpr float kDfRel = 0x1p-36f;
+
+// sqrt(softplus(z)) with softplus(z) = max(z, 0) + log1p(exp(-|z|)), for
+// |z| <= kDfMaxAbsZ.
+__device__ __forceinline__ df32 sqrt_softplus_df(float z) {
+  const float a = fabsf(z);
+  const float n = rintf(__fmul_rn(a, 0x1.715476p+0f));  // 0 .. 44
+  // r = a - n ln 2 (Cody and Waite): a - n*C1 is exact, n*C2 is exact as a
+  // product pair, n*C3 is below 2^-38
+  const float r0 = __fmaf_rn(-n, 0x1.62e4p-1f, a);
+  const df32 nc2 = two_prod(n, 0x1.7f7d1cp-20f);
+  df32 r = df_add(df32{r0, 0.0f}, df32{-nc2.hi, -nc2.lo});
+  r = df_add_f(r, -__fmul_rn(n, 0x1.ef357ap-45f));
+  // u = exp(-a) = 2^-n (1 + expm1(-r))
+  const df32 em = expm1_df(df32{-r.hi, -r.lo});
+  df32 u = df_add_f(em, 1.0f);
+  u = df_scale(u, __int_as_float((127 - (int)n) << 23));  // 2^-n, n in 0..44
+  // log1p(u): y0 from FP32, one Newton step y1 = y0 + (u - expm1(y0)) / (1 + expm1(y0))
+  const float y0 = log1pf(u.hi);
+  const df32 e1 = expm1_df(df32{y0, 0.0f});
+  const df32 d = df_add(u, df32{-e1.hi, -e1.lo});
+  const float delta = __fdiv_rn(__fadd_rn(d.hi, d.lo), __fadd_rn(1.0f, e1.hi));
+  df32 sp = fast_two_sum(y0, delta);
+  if (z > 0.0f) sp = df_add_f(sp, z);
+  // sqrt: s0 = RN(sqrt(sp.hi)); s = s0 + (sp - s0^2) / (2 s0), s0^2 exact as a product pair
+  const float s0 = __fsqrt_rn(sp.hi);
+  const df32 sq = two_prod(s0, s0);
+  const float res = __fadd_rn(__fsub_rn(__fsub_rn(sp.hi, sq.hi), sq.lo), sp.lo);
+  return fast_two_sum(s0, __fdiv_rn(res, __fmul_rn(2.0f, s0)));
+}
+
+// Upper bound on |key32 - key| for FP32 keys whose largest activation is
+// amax and largest |key| is kabs: 2^-23 (2.25 amax + 0.5 kabs) + 2^-60,
+// every step rounded up.
+__device__ __forceinline__ float key_err_bound(float amax, float kabs) {
+  return __fadd_ru(__fmul_ru(__fmaf_ru(2.25f, amax, __fmul_ru(0.5f, kabs)), 0x1p-23f), 0x1p-60f);
+}
+
+// A near-tie key: sqrt(softplus(z)) + b as a double-float, with the scale
+// s + |key| its distinctness test uses. Beyond the double-float range of z
+// the activation comes from FP64.
+struct NearKey {
+  float hi, lo, scale;
+};
+
+// FP64 activation split into two floats; out of line, so that no FP64
+// instruction is issued (not even predicated off) unless |z| is large.
+static __device__ __noinline__ df32 sqrt_softplus_split64(float z) {
+  const double v = sqrt_softplus_f64((double)z);
+  df32 s;
+  s.hi = (float)v;
+  s.lo = isfinite(s.hi) ? (float)(v - (double)s.hi) : 0.0f;
+  return s;
+}
+
+__device__ __forceinline__ NearKey near_key(float z, float b) {
+  const df32 s = fabsf(z) <= kDfMaxAbsZ ? sqrt_softplus_df(z) : sqrt_softplus_split64(z);
+  const df32 key = df_add_f(s, b);
+  return {key.hi, isfinite(key.hi) ? key.lo : 0.0f, __fadd_ru(fabsf(s.hi), fabsf(key.hi))};
+}
+
+// near_key out of line: its callers run on cold paths, where one shared
+// copy of the code costs fewer instruction fetches.
+static __device__ __noinline__ NearKey near_key_ool(float z, float b) { return near_key(z, b); }
+
+// True when two near-tie keys are far enough apart that their double-float
+// order is the order FP64 gives.
+__device__ __forceinline__ bool near_distinct(float ah, float al, float asc, float bh, float bl,
+                                              float bsc) {
+  const float d = fabsf(__fadd_rn(__fsub_rn(ah, bh), __fsub_rn(al, bl)));
+  return d > kDfRel * __fadd_ru(asc, bsc);
+}
+
+// (hi, lo) ordering of normalised double-float keys.
+__device__ __forceinline__ bool df_gt(float ah, float al, float bh, float bl) {
+  return ah > bh || (ah == bh && al > bl);
+}
+
+// Row-local top list of double-float keys, sorted by (key desc, index asc),
+// with FP32 comparisons only.
+template <int KC>
+struct TopListDF {
+  float h[KC], l[KC];
+  int i[KC];
+  float z[KC];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      h[j] = -INFINITY;
+      l[j] = 0.0f;
+      i[j] = 0x7fffffff;
+      z[j] = 0.0f;
+    }
+  }
+  __device__ __forceinline__ static bool ahead(float kh, float kl, int idx, float vh, float vl,
+                                               int vi) {
+    return df_gt(kh, kl, vh, vl) || (kh == vh && kl == vl && idx < vi);
+  }
+  __device__ __forceinline__ void push(float kh, float kl, int idx, float zz) {
+#pragma unroll
+    for (int j = KC - 1; j > 0; --j) {
+      if (ahead(kh, kl, idx, h[j], l[j], i[j])) {
+        const bool up = ahead(kh, kl, idx, h[j - 1], l[j - 1], i[j - 1]);
+        h[j] = up ? h[j - 1] : kh;
+        l[j] = up ? l[j - 1] : kl;
+        i[j] = up ? i[j - 1] : idx;
+        z[j] = up ? z[j - 1] : zz;
+      }
+    }
+    if (ahead(kh, kl, idx, h[0], l[0], i[0])) {
+      h[0] = kh;
+      l[0] = kl;
+      i[0] = idx;
+      z[0] = zz;
+    }
+  }
+};
+
+}  // namespace gbr

@@ -36,7 +36,23 @@ __global__ void __launch_bounds__(kTblWarps * 32)
                    map + (size_t)g * n, count + g);
 }
 
+__global__ void k_near_tie_keys(const float* __restrict__ z, const float* __restrict__ bias, int n,
+                                float* __restrict__ hi, float* __restrict__ lo) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const NearKey k = near_key(z[i], bias ? bias[i] : 0.0f);
+    hi[i] = k.hi;
+    lo[i] = k.lo;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_near_tie_keys(const float* z, const float* bias, int n, float* hi, float* lo,
+                                 cudaStream_t stream) {
+  const int blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
+  k_near_tie_keys<<<blocks, 256, 0, stream>>>(z, bias, n, hi, lo);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_select(const float* logits, const float* bias, int M, int E, int k, int act,
                           int32_t* out_idx, float* out_w, cudaStream_t stream) {

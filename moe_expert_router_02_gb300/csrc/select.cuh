@@ -17,11 +17,14 @@
 // the three steps gives |key32 - key| <= 2^-23 (2.25 a + 0.5 |key|) plus a
 // tiny absolute term for subnormal softplus values. When two neighbouring
 // keys among the first k+1 are closer than four times that bound, the
-// candidates within the band of the k-th key are re-ranked with keys
-// recomputed in FP64, which decides the order the FP64 definition gives.
+// candidates within the band of the k-th key are re-ranked with
+// double-float keys (relative error near 2^-42, FP32 arithmetic only); a
+// pair of those still too close to call, from different inputs, is ranked
+// with FP64 keys, which decide the order the FP64 definition gives.
 #pragma once
 
 #include "common.cuh"
+#include "dfkey.cuh"
 
 namespace gbr {
 
@@ -51,6 +54,47 @@ __device__ __forceinline__ void sort_desc(uint64_t (&v)[VPL]) {
 #pragma unroll
     for (int j = pass & 1; j + 1 < VPL; j += 2) cas_desc(v[j], v[j + 1]);
   }
+}
+
+// The FP64 re-ranking of the candidates in cmask (k rounds of
+// (key desc, index asc)); returns this lane's pick (lane < k). Out of line:
+// FP64 is slow on this part and must not be issued on the common path.
+template <int VPL, class Ld>
+__device__ __noinline__ int select_fp64(const Ld ld, const float* __restrict__ bias, int k,
+                                        uint32_t cmask) {
+  const int lane = threadIdx.x & 31;
+  double k64[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    k64[j] = 0.0;
+    if ((cmask >> j) & 1u)
+      k64[j] = sqrt_softplus_f64((double)ld(e)) + (bias ? (double)__ldg(bias + e) : 0.0);
+  }
+  int pick = -1;
+  for (int r = 0; r < k; ++r) {
+    double bv = -INFINITY;
+    int bidx = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      if (((cmask >> j) & 1u) && (bidx == 0x7fffffff || k64[j] > bv)) {
+        bv = k64[j];
+        bidx = lane + 32 * j;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const double ov = __shfl_xor_sync(kFull, bv, off);
+      const int oi = __shfl_xor_sync(kFull, bidx, off);
+      if (ov > bv || (ov == bv && oi < bidx)) {
+        bv = ov;
+        bidx = oi;
+      }
+    }
+    if ((bidx & 31) == lane) cmask &= ~(1u << (bidx >> 5));
+    if (lane == r) pick = bidx;
+  }
+  return pick;
 }
 
 // One warp selects the top-k of one row of E <= 32*VPL logits.
@@ -110,50 +154,94 @@ __device__ __noinline__ void warp_select_row(const Ld ld, const float* __restric
     // FP32 key error bound; non-negative floats order like their bit patterns
     const float amax_w = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(amax)));
     const float kabs_w = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(kabs)));
-    const double err = 0x1p-23 * (2.25 * (double)amax_w + 0.5 * (double)kabs_w) + 0x1p-60;
-    const double band = 4.0 * err;
+    const float band = 4.0f * key_err_bound(amax_w, kabs_w);
     const float next_key = __shfl_down_sync(kFull, sel_key, 1);
-    const bool close = (lane < kk - 1) && ((double)sel_key - (double)next_key <= band);
+    // the difference rounded down: a gap of at most band is never missed
+    const bool close = (lane < kk - 1) && __fsub_rd(sel_key, next_key) <= band;
     if (__any_sync(kFull, close)) {
       // re-rank every expert whose FP32 key lies within the band of the k-th
-      const double thr = (double)__shfl_sync(kFull, sel_key, k - 1) - band;
-      double k64[VPL];
+      const float thr = __fsub_rd(__shfl_sync(kFull, sel_key, k - 1), band);
       uint32_t cmask = 0;
 #pragma unroll
       for (int j = 0; j < VPL; ++j) {
-        k64[j] = 0.0;
         const int e = lane + 32 * j;
         if (e < E) {
-          const float z = ld(e);
-          const float a = sqrt_softplus_f32(z);
+          const float a = sqrt_softplus_f32(ld(e));
           const float kv = bias ? a + __ldg(bias + e) : a;
-          if ((double)kv >= thr) {
-            cmask |= 1u << j;
-            k64[j] = sqrt_softplus_f64((double)z) + (bias ? (double)__ldg(bias + e) : 0.0);
-          }
+          if (kv >= thr) cmask |= 1u << j;
         }
       }
-      for (int r = 0; r < k; ++r) {
-        double bv = -INFINITY;
+      // double-float keys, one candidate per lane per round
+      float khi[VPL], klo[VPL], ksc[VPL];
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) khi[j] = klo[j] = ksc[j] = 0.0f;
+      uint32_t todo = cmask;
+      while (__any_sync(kFull, todo != 0u)) {
+        const bool has = todo != 0u;
+        const int j = has ? __ffs(todo) - 1 : 0;
+        const int e = lane + 32 * j;
+        const float z = has ? ld(e) : 0.0f;
+        const float b = (has && bias) ? __ldg(bias + e) : 0.0f;
+        const NearKey nk = near_key_ool(z, b);
+#pragma unroll
+        for (int jj = 0; jj < VPL; ++jj) {
+          if (has && jj == j) {
+            khi[jj] = nk.hi;
+            klo[jj] = nk.lo;
+            ksc[jj] = nk.scale;
+          }
+        }
+        todo &= todo - 1u;
+      }
+      // k+1 rounds of (key desc, index asc) over the candidates; a pair of
+      // consecutive picks too close for the double-float keys, from
+      // different inputs, sends the row to FP64
+      bool amb = false;
+      float ph = 0.0f, pl = 0.0f, psc = 0.0f, pz = 0.0f, pb = 0.0f;
+      int pick = -1;
+      uint32_t left = cmask;
+      for (int r = 0; r < kk; ++r) {
+        float bh = -INFINITY, bl = 0.0f, bsc = 0.0f;
         int bidx = 0x7fffffff;
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
-          if (((cmask >> j) & 1u) && (bidx == 0x7fffffff || k64[j] > bv)) {
-            bv = k64[j];
+          if (((left >> j) & 1u) && (bidx == 0x7fffffff || df_gt(khi[j], klo[j], bh, bl))) {
+            bh = khi[j];
+            bl = klo[j];
+            bsc = ksc[j];
             bidx = lane + 32 * j;
           }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-          const double ov = __shfl_xor_sync(kFull, bv, off);
+          const float oh = __shfl_xor_sync(kFull, bh, off);
+          const float ol = __shfl_xor_sync(kFull, bl, off);
+          const float os = __shfl_xor_sync(kFull, bsc, off);
           const int oi = __shfl_xor_sync(kFull, bidx, off);
-          if (ov > bv || (ov == bv && oi < bidx)) {
-            bv = ov;
+          const bool take = oi != 0x7fffffff &&
+                            (bidx == 0x7fffffff || df_gt(oh, ol, bh, bl) ||
+                             (oh == bh && ol == bl && oi < bidx));
+          if (take) {
+            bh = oh;
+            bl = ol;
+            bsc = os;
             bidx = oi;
           }
         }
-        if ((bidx & 31) == lane) cmask &= ~(1u << (bidx >> 5));
-        if (lane == r) sel_idx = bidx;
+        if (bidx == 0x7fffffff) break;  // fewer candidates than rounds
+        if ((bidx & 31) == lane) left &= ~(1u << (bidx >> 5));
+        const float wz = ld(bidx);
+        const float wb = bias ? __ldg(bias + bidx) : 0.0f;
+        if (r > 0 && !near_distinct(ph, pl, psc, bh, bl, bsc) && !(pz == wz && pb == wb))
+          amb = true;
+        ph = bh, pl = bl, psc = bsc, pz = wz, pb = wb;
+        if (lane == r) pick = bidx;
+      }
+      if (!amb) {
+        if (lane < k) sel_idx = pick;
+      } else {
+        const int pick64 = select_fp64<VPL>(ld, bias, k, cmask);
+        if (lane < k) sel_idx = pick64;
       }
     }
   }
@@ -164,8 +252,18 @@ __device__ __noinline__ void warp_select_row(const Ld ld, const float* __restric
     // the key is the logit (-0.0 read back as +0.0, which exp treats alike)
     const float z0 = __shfl_sync(kFull, sel_key, 0);
     if (lane < k) s = expf(sel_key - z0);
-  } else if (lane < k) {
-    s = sqrt_softplus_f32(ld(sel_idx));
+  } else {
+    if (lane < k) s = sqrt_softplus_f32(ld(sel_idx));
+    const float smax = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(s)));
+    if (!(smax >= 0x1p-50f)) {
+      // every chosen activation is tiny (FP32 keeps few or no bits of it):
+      // the ratios come from the log domain
+      const float la = lane < k ? log_sqrt_softplus(ld(sel_idx)) : -INFINITY;
+      float lm = la;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lm = fmaxf(lm, __shfl_xor_sync(kFull, lm, off));
+      s = (lane < k && lm > -INFINITY) ? expf(la - lm) : 0.0f;
+    }
   }
   float sum = 0.0f;
 #pragma unroll

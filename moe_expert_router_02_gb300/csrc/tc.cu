@@ -30,6 +30,7 @@
 #include <mutex>
 
 #include "kernels.h"
+#include "dfkey.cuh"
 #include "select.cuh"
 
 namespace gbr {
@@ -317,8 +318,8 @@ struct TopList64 {
 
 // FP64 key of one expert; out of line so that the FP64 work runs only for
 // the entries that need it.
-__device__ __noinline__ double key64(float z, const float* bias, int e) {
-  return sqrt_softplus_f64((double)z) + (bias ? (double)__ldg(bias + e) : 0.0);
+__device__ __noinline__ double key64(float z, float b) {
+  return sqrt_softplus_f64((double)z) + (double)b;
 }
 
 // FP64 re-ranking of one row (see select.cuh): every lane of the warp calls
@@ -327,7 +328,7 @@ __device__ __noinline__ double key64(float z, const float* bias, int e) {
 // stays in registers.
 template <int KC, bool FP4>
 __device__ __noinline__ void refine_row(uint32_t trow, int E, float g, const float* bias,
-                                        double thr, bool close, int* out_i, float* out_z) {
+                                        float thr, bool close, int* out_i, float* out_z) {
   // out_i / out_z: KC entries, BM apart (shared memory)
   TopList64<KC> t64;
   t64.init();
@@ -342,7 +343,7 @@ __device__ __noinline__ void refine_row(uint32_t trow, int E, float g, const flo
           const float z = FP4 ? v[j] * g : v[j];
           const float av = sqrt_softplus_f32(z);
           const float key = bias ? av + __ldg(bias + e) : av;
-          if ((double)key >= thr)
+          if (key >= thr)
             t64.push(sqrt_softplus_f64((double)z) + (bias ? (double)__ldg(bias + e) : 0.0), e, av);
         }
       }
@@ -355,6 +356,181 @@ __device__ __noinline__ void refine_row(uint32_t trow, int E, float g, const flo
       out_z[j * BM] = t64.z[j];
     }
   }
+}
+
+// The FP64 stage of refine_in_list (all lanes call): FP64 keys for every
+// pooled entry; rows with amb set re-rank their list (still as stored) with
+// them. Out of line: FP64 is slow on this part and must not be issued on
+// the common path.
+template <int KC>
+__device__ __noinline__ void refine_fp64(const uint32_t* l_o, int32_t* l_i, float* l_z,
+                                         uint32_t need, bool amb, int qoff, int qtotal,
+                                         const float* zq, const float* sb, const uint32_t* wl) {
+  const int lane = threadIdx.x & 31;
+  double kd[KC];
+#pragma unroll
+  for (int j = 0; j < KC; ++j) kd[j] = (double)float_of_ord(l_o[j * BM]);
+  for (int base = 0; base < qtotal; base += 32) {
+    double key = 0.0;
+    if (base + lane < qtotal) {
+      const uint32_t item = wl[base + lane];
+      const int e = (int)(item >> 16);
+      key = key64(zq[e * BM + (int)((item >> 5) & 31u)], sb ? sb[e] : 0.0f);
+    }
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      const int qj = qoff + __popc(need & ((1u << j) - 1u));
+      const bool mine = ((need >> j) & 1u) && qj >= base && qj < base + 32;
+      const double kv = __shfl_sync(kFull, key, mine ? qj - base : lane);
+      if (mine) kd[j] = kv;
+    }
+  }
+  if (amb) {
+    TopList64<KC> t64;
+    t64.init();
+#pragma unroll
+    for (int j = 0; j < KC; ++j)
+      if (l_o[j * BM] != 0u) t64.push(kd[j], l_i[j * BM], l_z[j * BM]);
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      l_i[j * BM] = t64.i[j];
+      l_z[j * BM] = t64.z[j];
+    }
+  }
+}
+
+// Near ties inside the merged list of one row (all 32 lanes call; lanes
+// with close == false take part in the pooled evaluations only). The list
+// (KC entries, BM apart in shared memory: order keys, experts, scores) is
+// re-ranked in place. When every key at or above the band below the k-th
+// is in the list, only entries next to a gap of at most `band` need a
+// better key; the others keep their FP32 key, which orders them correctly
+// against everything more than `band` away. Those keys are double-float
+// (dfkey.cuh); a pair still too close to call, from different inputs,
+// takes FP64 keys. The warp pools the entries its rows need and evaluates
+// them one per lane (zq: the warp's logit copy, [E][BM] from its first
+// row; sb: the bias in shared memory or null). Returns true when the near
+// ties reach past the list (the caller then re-ranks every column).
+// About one row in four thousand gets here, so this code is cold in the
+// instruction cache whenever it runs, and its cost is the instruction
+// fetches: it keeps to rolled loops over local arrays.
+template <int KC>
+__device__ __noinline__ bool refine_in_list(const uint32_t* l_o, int32_t* l_i, float* l_z,
+                                            bool close, float band, float thr, const float* zq,
+                                            const float* sb, uint32_t* wl) {
+  const int lane = threadIdx.x & 31;
+  float kh[KC], kl[KC], ks[KC], sc[KC];
+  int ii[KC];
+  bool rk[KC];
+  int n = 0;  // filled entries (empty ones sort last)
+#pragma unroll 1
+  for (int j = 0; j < KC; ++j) {
+    const uint32_t o = l_o[j * BM];
+    if (o != 0u) n = j + 1;
+    kh[j] = float_of_ord(o);
+    kl[j] = 0.0f;
+    ks[j] = 0.0f;
+    ii[j] = l_i[j * BM];
+    sc[j] = l_z[j * BM];
+    rk[j] = false;
+  }
+  bool in_list = false;
+  uint32_t need = 0u;
+  if (close) {
+    const float lo = __fsub_rd(thr, band);
+    in_list = n < KC || kh[KC - 1] < lo;
+    if (in_list) {
+#pragma unroll 1
+      for (int j = 0; j < n; ++j) {
+        const bool up = j > 0 && __fsub_rd(kh[j - 1], kh[j]) <= band;
+        const bool dn = j + 1 < n && __fsub_rd(kh[j], kh[j + 1]) <= band;
+        if (kh[j] >= lo && (up || dn)) need |= 1u << j;
+      }
+    }
+  }
+  // pool (expert, owner lane, slot) items of the needed entries
+  const int nneed = __popc(need);
+  int qoff = nneed;
+#pragma unroll 1
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(kFull, qoff, d);
+    if (lane >= d) qoff += t;
+  }
+  const int qtotal = __shfl_sync(kFull, qoff, 31);
+  qoff -= nneed;
+  if (qtotal == 0) return close && !in_list;
+  {
+    int q = qoff;
+#pragma unroll 1
+    for (int j = 0; j < KC; ++j)
+      if ((need >> j) & 1u) wl[q++] = ((uint32_t)ii[j] << 16) | ((uint32_t)lane << 5) | (uint32_t)j;
+  }
+  __syncwarp();
+  // double-float keys, one item per lane, handed back to the owners
+#pragma unroll 1
+  for (int base = 0; base < qtotal; base += 32) {
+    NearKey nk{0.0f, 0.0f, 0.0f};
+    if (base + lane < qtotal) {
+      const uint32_t item = wl[base + lane];
+      const int e = (int)(item >> 16);
+      nk = near_key_ool(zq[e * BM + (int)((item >> 5) & 31u)], sb ? sb[e] : 0.0f);
+    }
+#pragma unroll 1
+    for (int j = 0; j < KC; ++j) {
+      const int qj = qoff + __popc(need & ((1u << j) - 1u));
+      const bool mine = ((need >> j) & 1u) && qj >= base && qj < base + 32;
+      const int src = mine ? qj - base : lane;
+      const float h = __shfl_sync(kFull, nk.hi, src);
+      const float l = __shfl_sync(kFull, nk.lo, src);
+      const float c = __shfl_sync(kFull, nk.scale, src);
+      if (mine) {
+        kh[j] = h;
+        kl[j] = l;
+        ks[j] = c;
+        rk[j] = true;
+      }
+    }
+  }
+  // insertion sort by (key desc, index asc); then consecutive re-keyed
+  // entries must be distinct or come from identical inputs (a misordered
+  // pair always leaves such a consecutive pair, with nothing re-keyed or
+  // not between them)
+  bool amb = false;
+  if (need != 0u) {
+#pragma unroll 1
+    for (int j = 1; j < n; ++j) {
+      const float h = kh[j], l = kl[j], c = ks[j], z = sc[j];
+      const int i = ii[j];
+      const bool r = rk[j];
+      int p = j;
+      while (p > 0 && (df_gt(h, l, kh[p - 1], kl[p - 1]) ||
+                       (h == kh[p - 1] && l == kl[p - 1] && i < ii[p - 1]))) {
+        kh[p] = kh[p - 1], kl[p] = kl[p - 1], ks[p] = ks[p - 1], sc[p] = sc[p - 1];
+        ii[p] = ii[p - 1], rk[p] = rk[p - 1];
+        --p;
+      }
+      kh[p] = h, kl[p] = l, ks[p] = c, sc[p] = z, ii[p] = i, rk[p] = r;
+    }
+#pragma unroll 1
+    for (int j = 0; j + 1 < n; ++j) {
+      if (rk[j] && rk[j + 1] && !near_distinct(kh[j], kl[j], ks[j], kh[j + 1], kl[j + 1], ks[j + 1])) {
+        const bool same = zq[ii[j] * BM + lane] == zq[ii[j + 1] * BM + lane] &&
+                          (sb ? sb[ii[j]] == sb[ii[j + 1]] : true);
+        if (!same) amb = true;
+      }
+    }
+  }
+  // rare: FP64 keys decide the rows the double-float keys could not (it
+  // reads the list as still stored)
+  if (__any_sync(kFull, amb)) refine_fp64<KC>(l_o, l_i, l_z, need, amb, qoff, qtotal, zq, sb, wl);
+  if (need != 0u && !amb) {
+#pragma unroll 1
+    for (int j = 0; j < KC; ++j) {
+      l_i[j * BM] = ii[j];
+      l_z[j * BM] = sc[j];
+    }
+  }
+  return close && !in_list;
 }
 
 constexpr size_t kCandOffset = 32768;  // the logits copy starts after the exchange area
@@ -417,6 +593,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
   __shared__ __align__(8) uint64_t s_wready;  // NVFP4: s_epoch is set
   __shared__ unsigned s_epoch, s_claim;
   __shared__ float s_bias[256];    // the selection bias (sqrt-softplus)
+  __shared__ float s_gbmin[2][32];  // least bias per column group (sqrt-softplus)
   const RouterArgs& a = p.a;
   const int S = p.stages;
   // 1024-byte aligned tile ring, then barriers
@@ -549,6 +726,18 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
     }
     if (has_bias && warp == 0)
       for (int e = lane; e < E; e += 32) s_bias[e] = __ldg(a.bias + e);
+    if (sp && warp == 1) {
+      // least bias of each interleaved column group of each half (the
+      // groups of pass A: column c_lo + q + G t is in group q)
+      constexpr int G = KC <= 4 ? 4 : (KC <= 6 ? 8 : (KC <= 10 ? 16 : 32));
+      for (int hq = lane; hq < 2 * G; hq += 32) {
+        const int h = hq / G, q = hq % G;
+        const int lo = h * E2, hi = h ? E : min(E, E2);
+        float m = INFINITY;
+        for (int c = lo + q; c < hi; c += G) m = fminf(m, has_bias ? __ldg(a.bias + c) : 0.0f);
+        s_gbmin[h][q] = m;
+      }
+    }
     asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
     if (FP4) {
       // NVFP4: W is decoded once per launch, not once per CTA. The CTAs claim
@@ -634,12 +823,16 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
     top.init();
     float amax = 0.0f, kabs = 0.0f;
     if (all_ok) {
-      // Pass A: a lower bound L on this half's k-th largest logit, branch-free:
-      // the k-th largest of the maxima of G >= 2k interleaved column groups
-      // (k distinct experts are >= it). The half holds k experts with
-      // key >= a(L) + b_min, so an expert can reach the top k only if
-      // a(z) + b_max >= a(L) + b_min: z >= a^-1(a(L) - (b_max - b_min)).
-      // For softmax the key is the logit: z >= L.
+      // Pass A: a lower bound L on the row's k-th largest key, branch-free.
+      // Each half splits its columns into G interleaved groups and takes each
+      // group's largest logit z_q; that expert's key a(z_q) + b is at least
+      // LB_q = sqrt(max(z_q, 0)) + (least bias in the group), since
+      // a(z) >= sqrt(max(z, 0)) (rounded down: LB_q never exceeds it). The
+      // groups of both halves are 2G distinct experts, so the k-th largest
+      // LB_q over the row is at most the k-th largest key. An expert can
+      // then reach the top k (or the FP32 band below it) only if
+      // a(z) + b_max >= L - margin, i.e. z >= a^-1(L - margin - b_max).
+      // For softmax the key is the logit and LB_q = z_q, so z >= L.
       constexpr int G = KC <= 4 ? 4 : (KC <= 6 ? 8 : (KC <= 10 ? 16 : 32));  // >= 2 (KC - 2) >= 2k
       float gmax[G];
 #pragma unroll
@@ -656,37 +849,63 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
           }
         }
       }
-      // k-th largest of the G maxima: a sorted list of KC - 1 >= k values kept
-      // with min/max only (new[j] = max(old[j], min(old[j-1], x)))
+      // this half's KC - 1 >= k largest LB_q, sorted, kept with min/max only
+      // (new[j] = max(old[j], min(old[j-1], x)))
       float srt[KC - 1];
 #pragma unroll
       for (int j = 0; j < KC - 1; ++j) srt[j] = -INFINITY;
 #pragma unroll
       for (int q = 0; q < G; ++q) {
-        const float xq = gmax[q];
+        float xq = gmax[q];
+        if (sp) xq = xq > -INFINITY ? __fadd_rd(__fsqrt_rd(fmaxf(xq, 0.0f)), s_gbmin[half][q])
+                                    : -INFINITY;
 #pragma unroll
         for (int j = KC - 2; j > 0; --j) srt[j] = fmaxf(srt[j], fminf(srt[j - 1], xq));
         srt[0] = fmaxf(srt[0], xq);
       }
+      // merge with the other half's list (through the idle exchange area;
+      // the second barrier keeps it from being reused before both have read)
+      float* lbx = reinterpret_cast<float*>(tiles);  // [2][KC - 1][BM]
+#pragma unroll
+      for (int j = 0; j < KC - 1; ++j) lbx[(half * (KC - 1) + j) * BM + row] = srt[j];
+      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+#pragma unroll
+      for (int jo = 0; jo < KC - 1; ++jo) {
+        const float xq = lbx[((1 - half) * (KC - 1) + jo) * BM + row];
+#pragma unroll
+        for (int j = KC - 2; j > 0; --j) srt[j] = fmaxf(srt[j], fminf(srt[j - 1], xq));
+        srt[0] = fmaxf(srt[0], xq);
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
       float lz = INFINITY;
 #pragma unroll
       for (int j = 0; j < KC - 1; ++j)
         if (j < k) lz = fminf(lz, srt[j]);
-      // the threshold, rounded down with margins far above the FP32 errors of
-      // sqrt_softplus (<= 2.25 ulp), expm1f and logf (<= 1 ulp each)
+      // The threshold. Margins: the FP32 keys are within
+      // err = 2^-23 (2.25 a + 0.5 |key|) of the exact ones and the band the
+      // list must also hold reaches 8 err below the k-th FP32 key, so the
+      // exact keys to keep reach L - 10 err; with a <= A = (largest LB) -
+      // b_min + 0.84 (a(z) <= sqrt(max(z, 0)) + sqrt(ln 2)) the margin
+      // 2^-16 (4 A + |b|max + 1) covers that many times over. a^-1(y) =
+      // log(expm1(y^2)) is then taken on y shrunk by 2^-18 and the result
+      // lowered by 2^-16 (1 + |t|), far beyond the FP32 errors of expm1f and
+      // logf; above y^2 = 80, log(expm1(u)) = u - O(e^-80).
       float tz;
       if (!(lz > -INFINITY)) {
-        tz = -INFINITY;  // fewer than G experts in this half: keep them all
-      } else if (!sp || !has_bias) {
-        tz = lz;  // the key is increasing in the logit
+        tz = -INFINITY;  // fewer than k experts bounded: keep them all
+      } else if (!sp) {
+        tz = lz;  // softmax: the key is the logit, exactly
       } else {
-        const float ak = sqrt_softplus_f32(lz);
-        const float y = ak * (1.0f - 0x1p-20f) - (bmax - bmin) * (1.0f + 0x1p-20f) - 0x1p-40f;
+        const float A = srt[0] - bmin + 0.84f;
+        const float babs = fmaxf(fabsf(bmin), fabsf(bmax));
+        const float margin = 0x1p-16f * (4.0f * fabsf(A) + babs + 1.0f);
+        const float y = (lz - margin - bmax) * (1.0f - 0x1p-18f);
         if (!(y > 0.0f)) {
           tz = -INFINITY;
         } else {
-          const float t = logf(expm1f(y * y * (1.0f - 0x1p-21f)));
-          tz = t - 0x1p-18f * (1.0f + fabsf(t));
+          const float u = y * y;
+          const float t = u > 80.0f ? u : logf(expm1f(u));
+          tz = t - 0x1p-16f * (1.0f + fabsf(t));
         }
       }
       // Pass B: a bit per candidate column, branch-free (at most 4 chunks of 32)
@@ -784,17 +1003,16 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       for (int j = 0; j < KC; ++j) top.push(xo[j * BM + row], xi[j * BM + row], xz[j * BM + row]);
       amax = fmaxf(amax, xm[row]);
       kabs = fmaxf(kabs, xm[BM + row]);
-      // FP64 guard-band refine (see select.cuh)
+      // guard-band refine (see select.cuh); FP32 bounds, rounded outwards
       bool close = false;
-      double band = 0.0;
+      float band = 0.0f;
       if (sp) {
-        const double err = 0x1p-23 * (2.25 * (double)amax + 0.5 * (double)kabs) + 0x1p-60;
-        band = 4.0 * err;
+        band = 4.0f * key_err_bound(amax, kabs);
         const int kk = min(k + 1, E);
 #pragma unroll
         for (int j = 0; j + 1 < KC; ++j)
           if (j + 1 < kk &&
-              (double)float_of_ord(top.o[j]) - (double)float_of_ord(top.o[j + 1]) <= band)
+              __fsub_rd(float_of_ord(top.o[j]), float_of_ord(top.o[j + 1])) <= band)
             close = true;
       }
       // the k-th key is the smallest of the first k (the list is sorted);
@@ -803,81 +1021,29 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
 #pragma unroll
       for (int j = 0; j < KC; ++j)
         if (j < k) kth = min(kth, top.o[j]);
-      const double thr = (double)float_of_ord(kth) - band;
-      // Near ties inside the merged list: when every key at or above the band
-      // below the k-th is in the list, only list entries next to a gap of at
-      // most `band` need an FP64 key; the others keep their FP32 key, which
-      // orders them correctly against everything more than `band` away.
-      bool in_list = false;
-      double kd[KC];
-      uint32_t need = 0u;  // list entries that take an FP64 key
+      const float thr = __fsub_rd(float_of_ord(kth), band);
+      bool slow = false;
+      if (__any_sync(kFull, close)) {
+        // the list goes through the exchange area (free after the merge), so
+        // the rare refine runs out of line without holding it in registers
 #pragma unroll
-      for (int j = 0; j < KC; ++j) kd[j] = (double)float_of_ord(top.o[j]);
-      if (close) {
-        const double lo = thr - band;
-        in_list = top.o[KC - 1] == 0u || kd[KC - 1] < lo;
-        if (in_list) {
-#pragma unroll
-          for (int j = 0; j < KC; ++j) {
-            const bool nr = top.o[j] != 0u && kd[j] >= lo &&
-                            ((j > 0 && kd[j - 1] - kd[j] <= band) ||
-                             (j + 1 < KC && top.o[j + 1] != 0u && kd[j] - kd[j + 1] <= band));
-            need |= (nr ? 1u : 0u) << j;
-          }
+        for (int j = 0; j < KC; ++j) {
+          xo[j * BM + row] = top.o[j];
+          xi[j * BM + row] = top.i[j];
+          xz[j * BM + row] = top.z[j];
         }
-      }
-      // The FP64 keys are slow on this part (~3400 cycles each), so the warp
-      // pools the entries its rows need and evaluates them one per lane;
-      // each owner then gathers its keys back with shuffles.
-      const int nneed = __popc(need);
-      int qoff = nneed;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int t = __shfl_up_sync(kFull, qoff, d);
-        if (lane >= d) qoff += t;
-      }
-      const int qtotal = __shfl_sync(kFull, qoff, 31);
-      qoff -= nneed;
-      if (qtotal > 0) {
         uint32_t* wl = reinterpret_cast<uint32_t*>(tiles + kCandOffset + (size_t)E * BM * 4) +
                        warp * kListCap;  // this warp's candidate list is spent
-        {
-          int q = qoff;
-#pragma unroll
-          for (int j = 0; j < KC; ++j)
-            if ((need >> j) & 1u)
-              wl[q++] = ((uint32_t)top.i[j] << 16) | ((uint32_t)lane << 5) | (uint32_t)j;
-        }
-        __syncwarp();
-        for (int base = 0; base < qtotal; base += 32) {
-          double key = 0.0;
-          if (base + lane < qtotal) {
-            const uint32_t item = wl[base + lane];
-            const int e = (int)(item >> 16);
-            key = key64(zbuf[e * BM + quad * 32 + (int)((item >> 5) & 31u)], a.bias, e);
-          }
+        slow = refine_in_list<KC>(xo + row, xi + row, xz + row, close, band, thr,
+                                  zbuf + quad * 32, has_bias ? s_bias : nullptr, wl);
+        if (close) {
 #pragma unroll
           for (int j = 0; j < KC; ++j) {
-            const int qj = qoff + __popc(need & ((1u << j) - 1u));
-            const bool mine = ((need >> j) & 1u) && qj >= base && qj < base + 32;
-            const double kv = __shfl_sync(kFull, key, mine ? qj - base : lane);
-            if (mine) kd[j] = kv;
-          }
-        }
-        if (need != 0u) {
-          TopList64<KC> t64;
-          t64.init();
-#pragma unroll
-          for (int j = 0; j < KC; ++j)
-            if (top.o[j] != 0u) t64.push(kd[j], top.i[j], top.z[j]);
-#pragma unroll
-          for (int j = 0; j < KC; ++j) {
-            top.i[j] = t64.i[j];
-            top.z[j] = t64.z[j];
+            top.i[j] = xi[j * BM + row];
+            top.z[j] = xz[j * BM + row];
           }
         }
       }
-      const bool slow = close && !in_list;
       if (__any_sync(kFull, slow)) {  // near ties reaching past the list: every column
         refine_row<KC, FP4>(trow, E, g, a.bias, thr, slow, xi + row, xz + row);
         if (slow) {
@@ -895,6 +1061,28 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         for (int j = 0; j < KC; ++j) {
           sv[j] = sp ? top.z[j] : expf(top.z[j] - top.z[0]);  // the list keeps scores
           if (j < k) sum += sv[j];
+        }
+        if (sp) {
+          float smax = 0.0f;
+#pragma unroll
+          for (int j = 0; j < KC; ++j)
+            if (j < k) smax = fmaxf(smax, sv[j]);
+          if (!(smax >= 0x1p-50f)) {
+            // every chosen activation is tiny (FP32 keeps few or no bits of
+            // it): the ratios come from the log domain
+            float la[KC], lm = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < KC; ++j) {
+              la[j] = j < k ? log_sqrt_softplus(zbuf[top.i[j] * BM + row]) : -INFINITY;
+              lm = fmaxf(lm, la[j]);
+            }
+            sum = 0.0f;
+#pragma unroll
+            for (int j = 0; j < KC; ++j) {
+              sv[j] = lm > -INFINITY ? expf(la[j] - lm) : 0.0f;
+              if (j < k) sum += sv[j];
+            }
+          }
         }
 #pragma unroll
         for (int j = 0; j < KC; ++j) {
@@ -927,7 +1115,6 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       }
     }
   }
-
   tc_fence_before();
   __syncthreads();
   // the peer may still signal this CTA's barriers until it is done as well
@@ -1048,7 +1235,7 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
   p.b_bytes = (uint32_t)a.E * BK * 2;
   p.stage_bytes = p.a_bytes + p.b_bytes;
   const size_t extra = 1024 /*align*/ + 2 * 8 * 8 + 8 + 16 + BM * kMaxK * 4;
-  const size_t budget = 227 * 1024 - 2048;  // the rest holds the static NVFP4 table
+  const size_t budget = 227 * 1024 - 4096;  // the rest holds the static shared arrays
   int S = (int)((budget - extra) / p.stage_bytes);
   if (S > 6) S = 6;
   if (S < 2) return cudaErrorInvalidValue;

@@ -23,7 +23,7 @@ GBR_REGIME_GENERIC, GBR_REGIME_GEMV, GBR_REGIME_TC, GBR_REGIME_UNFUSED, GBR_REGI
 
 EXPORTS = ("router_forward", "router_forward_ex", "router_workspace_size", "router_regime",
            "router_select", "route_table", "router_strerror", "router_device_status",
-           "router_forward_noalloc")
+           "router_forward_noalloc", "router_near_tie_keys")
 
 
 class RouterError(RuntimeError):
@@ -62,11 +62,13 @@ def lib() -> ctypes.CDLL:
             L.router_select.argtypes = [P, P, I, I, I, I, P, P, P]
             L.route_table.argtypes = [P, I, I, I, P, P, P, P, P]
             L.router_forward_noalloc.argtypes = [P, P, P, I, I, I, I, I, P, P, P]
+            L.router_near_tie_keys.argtypes = [P, P, I, P, P, P]
             L.router_strerror.argtypes = [I]
             L.router_strerror.restype = ctypes.c_char_p
             L.router_device_status.argtypes = [I]
             for f in (L.router_forward, L.router_forward_ex, L.router_regime, L.router_select,
-                      L.route_table, L.router_device_status, L.router_forward_noalloc):
+                      L.route_table, L.router_device_status, L.router_forward_noalloc,
+                      L.router_near_tie_keys):
                 f.restype = I
             _lib = L
     return _lib
@@ -143,6 +145,11 @@ def router_regime(M, H, E, k, opts=None) -> int:
 def router_select(logits, bias, M, E, k, act, out_idx, out_w, stream=None):
     _check(lib().router_select(_ptr(logits), _ptr(bias), M, E, k, act, _ptr(out_idx),
                                _ptr(out_w), _stream(stream)), "router_select")
+
+
+def router_near_tie_keys(z, bias, n, key_hi, key_lo, stream=None):
+    _check(lib().router_near_tie_keys(_ptr(z), _ptr(bias), n, _ptr(key_hi), _ptr(key_lo),
+                                      _stream(stream)), "router_near_tie_keys")
 
 
 def route_table(idx, groups, tokens_per_group, k, out_unique, out_mask, out_map, out_count,
