@@ -13,7 +13,7 @@
 // Methods: error-free sum and product (Knuth's TwoSum, Dekker's Fast2Sum,
 // the FMA product residual) and Dekker's double-length multiplication;
 // exp by Cody and Waite's argument reduction with ln 2 split in three
-// parts, a short Taylor series of expm1 in double-float on x / 16 and four
+// parts, the Taylor series of expm1 in double-float on x / 16 and four
 // doublings expm1(2y) = expm1(y) (expm1(y) + 2); log1p by one Newton step
 // on e^y - 1 - u from the FP32 log1pf; sqrt by one Newton (Heron) step.
 // The constants are ln 2 and 1/k! rounded to float: C1 is ln 2 to 15
@@ -75,25 +75,30 @@ __device__ __forceinline__ df32 df_scale(df32 x, float pow2) {  // exact for pow
   return {__fmul_rn(x.hi, pow2), __fmul_rn(x.lo, pow2)};
 }
 
-// expm1(x) for |x| <= 0.75, relative error about 2^-43. Out of line: the
-// two calls in sqrt_softplus_df share one copy.
+// 1/k! for k = 1..9 as double-floats.
+static __constant__ float2 c_inv_fact[9] = {
+    {0x1p+0f, 0.0f},
+    {0x1p-1f, 0.0f},
+    {0x1.555556p-3f, -0x1.555556p-28f},
+    {0x1.555556p-5f, -0x1.555556p-30f},
+    {0x1.111112p-7f, -0x1.dddddep-32f},
+    {0x1.6c16c2p-10f, -0x1.27d27ep-35f},
+    {0x1.a01a02p-13f, -0x1.7f97fap-39f},
+    {0x1.a01a02p-16f, -0x1.7f97fap-42f},
+    {0x1.71de3ap-19f, 0x1.55b1ccp-45f}};
+
+// expm1(x) for |x| <= 0.75, relative error about 2^-44: the Taylor series
+// to degree 9 on y = x / 16 (the first dropped term is below 2^-55 of the
+// result), then four doublings. This path only runs for near ties, so its
+// code is cold whenever it runs: the loops stay rolled and the function
+// out of line, which keeps the instruction fetches few.
 static __device__ __noinline__ df32 expm1_df(df32 x) {
   const df32 y = df_scale(x, 0x1p-4f);  // |y| <= 0.047
-  const df32 y2 = df_mul(y, y);
-  const df32 y3 = df_mul(y2, y);
-  const df32 y4 = df_mul(y2, y2);
-  // y^5 / 5! .. y^8 / 8! in FP32: at most 3e-8 of the result, so their
-  // rounding stays near 2^-47 of it; the first dropped term is 3e-17 of it
-  const float t = y.hi;
-  float tail = __fmaf_rn(t, 0x1.a01a02p-16f, 0x1.a01a02p-13f);
-  tail = __fmaf_rn(t, tail, 0x1.6c16c2p-10f);
-  tail = __fmaf_rn(t, tail, 0x1.111112p-7f);
-  tail = __fmul_rn(tail, __fmul_rn(y4.hi, t));
-  df32 e = df_add_f(df_mul(y4, df32{0x1.555556p-5f, -0x1.555556p-30f}), tail);  // + y^4 / 24
-  e = df_add(e, df_mul(y3, df32{0x1.555556p-3f, -0x1.555556p-28f}));           // + y^3 / 6
-  e = df_add(e, df_scale(y2, 0.5f));                                            // + y^2 / 2
-  e = df_add(e, y);                                                             // + y
-#pragma unroll
+  df32 p = df32{c_inv_fact[8].x, c_inv_fact[8].y};
+#pragma unroll 1
+  for (int i = 7; i >= 0; --i) p = df_add(df_mul(p, y), df32{c_inv_fact[i].x, c_inv_fact[i].y});
+  df32 e = df_mul(p, y);
+#pragma unroll 1
   for (int i = 0; i < 4; ++i) e = df_mul(e, df_add_f(e, 2.0f));  // expm1(2v) from expm1(v)
   return e;
 }

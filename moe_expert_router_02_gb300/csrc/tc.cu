@@ -111,12 +111,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// L2 eviction policies: x streams through once (first to go), W_gate is
+// read by every CTA (last to go). Keeping the stream from flushing the
+// rest of L2 also keeps the kernel's own code there: the epilogue's rarely
+// run paths are otherwise fetched from DRAM.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // TMA load delivered to the same shared-memory offset (and mbarrier offset)
@@ -143,11 +158,11 @@ __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
 // 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned
 // addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
+                                          uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -411,40 +426,32 @@ __device__ __noinline__ void refine_fp64(const uint32_t* l_o, int32_t* l_i, floa
 // them one per lane (zq: the warp's logit copy, [E][BM] from its first
 // row; sb: the bias in shared memory or null). Returns true when the near
 // ties reach past the list (the caller then re-ranks every column).
-// About one row in four thousand gets here, so this code is cold in the
-// instruction cache whenever it runs, and its cost is the instruction
-// fetches: it keeps to rolled loops over local arrays.
+// This runs for about one row in four thousand, so its code is cold in the
+// instruction cache whenever it runs and every distinct instruction costs a
+// fetch: the loops stay rolled and work in shared memory (the row's list,
+// and the warp's spent candidate list wl for the pooled items).
 template <int KC>
 __device__ __noinline__ bool refine_in_list(const uint32_t* l_o, int32_t* l_i, float* l_z,
                                             bool close, float band, float thr, const float* zq,
                                             const float* sb, uint32_t* wl) {
   const int lane = threadIdx.x & 31;
-  float kh[KC], kl[KC], ks[KC], sc[KC];
-  int ii[KC];
-  bool rk[KC];
-  int n = 0;  // filled entries (empty ones sort last)
-#pragma unroll 1
-  for (int j = 0; j < KC; ++j) {
-    const uint32_t o = l_o[j * BM];
-    if (o != 0u) n = j + 1;
-    kh[j] = float_of_ord(o);
-    kl[j] = 0.0f;
-    ks[j] = 0.0f;
-    ii[j] = l_i[j * BM];
-    sc[j] = l_z[j * BM];
-    rk[j] = false;
-  }
   bool in_list = false;
   uint32_t need = 0u;
   if (close) {
     const float lo = __fsub_rd(thr, band);
-    in_list = n < KC || kh[KC - 1] < lo;
+    in_list = l_o[(KC - 1) * BM] == 0u || float_of_ord(l_o[(KC - 1) * BM]) < lo;
     if (in_list) {
+      float prev = INFINITY;
 #pragma unroll 1
-      for (int j = 0; j < n; ++j) {
-        const bool up = j > 0 && __fsub_rd(kh[j - 1], kh[j]) <= band;
-        const bool dn = j + 1 < n && __fsub_rd(kh[j], kh[j + 1]) <= band;
-        if (kh[j] >= lo && (up || dn)) need |= 1u << j;
+      for (int j = 0; j < KC; ++j) {
+        const uint32_t o = l_o[j * BM];
+        if (o == 0u) break;  // empty entries sort last
+        const float kj = float_of_ord(o);
+        const uint32_t on = j + 1 < KC ? l_o[(j + 1) * BM] : 0u;
+        const bool up = j > 0 && __fsub_rd(prev, kj) <= band;
+        const bool dn = on != 0u && __fsub_rd(kj, float_of_ord(on)) <= band;
+        if (kj >= lo && (up || dn)) need |= 1u << j;
+        prev = kj;
       }
     }
   }
@@ -459,75 +466,91 @@ __device__ __noinline__ bool refine_in_list(const uint32_t* l_o, int32_t* l_i, f
   const int qtotal = __shfl_sync(kFull, qoff, 31);
   qoff -= nneed;
   if (qtotal == 0) return close && !in_list;
+  // items in wl[0, 256), their double-float keys (hi, lo) and scales after
+  // them; more than 256 items (a warp full of near ties) go to FP64
+  const bool fits = qtotal <= 256;
+  uint32_t* it_e = wl;
+  float* it_h = reinterpret_cast<float*>(wl + 256);
+  float* it_l = reinterpret_cast<float*>(wl + 512);
+  float* it_s = reinterpret_cast<float*>(wl + 768);
   {
     int q = qoff;
 #pragma unroll 1
     for (int j = 0; j < KC; ++j)
-      if ((need >> j) & 1u) wl[q++] = ((uint32_t)ii[j] << 16) | ((uint32_t)lane << 5) | (uint32_t)j;
+      if ((need >> j) & 1u)
+        it_e[q++] = ((uint32_t)l_i[j * BM] << 16) | ((uint32_t)lane << 5) | (uint32_t)j;
   }
   __syncwarp();
-  // double-float keys, one item per lane, handed back to the owners
+  bool amb = !fits;
+  if (fits) {
+    // double-float keys, one item per lane
 #pragma unroll 1
-  for (int base = 0; base < qtotal; base += 32) {
-    NearKey nk{0.0f, 0.0f, 0.0f};
-    if (base + lane < qtotal) {
-      const uint32_t item = wl[base + lane];
+    for (int q = lane; q < qtotal; q += 32) {
+      const uint32_t item = it_e[q];
       const int e = (int)(item >> 16);
-      nk = near_key_ool(zq[e * BM + (int)((item >> 5) & 31u)], sb ? sb[e] : 0.0f);
+      const NearKey nk = near_key_ool(zq[e * BM + (int)((item >> 5) & 31u)], sb ? sb[e] : 0.0f);
+      it_h[q] = nk.hi;
+      it_l[q] = nk.lo;
+      it_s[q] = nk.scale;
     }
+    __syncwarp();
+    // Re-rank this row's items. Runs of consecutive needed entries lie more
+    // than `band` apart, beyond what the keys' errors can cross, so sorting
+    // all of the row's items by (key desc, expert asc) keeps every item in
+    // its run; they then refill the needed slots in order.
 #pragma unroll 1
-    for (int j = 0; j < KC; ++j) {
-      const int qj = qoff + __popc(need & ((1u << j) - 1u));
-      const bool mine = ((need >> j) & 1u) && qj >= base && qj < base + 32;
-      const int src = mine ? qj - base : lane;
-      const float h = __shfl_sync(kFull, nk.hi, src);
-      const float l = __shfl_sync(kFull, nk.lo, src);
-      const float c = __shfl_sync(kFull, nk.scale, src);
-      if (mine) {
-        kh[j] = h;
-        kl[j] = l;
-        ks[j] = c;
-        rk[j] = true;
-      }
-    }
-  }
-  // insertion sort by (key desc, index asc); then consecutive re-keyed
-  // entries must be distinct or come from identical inputs (a misordered
-  // pair always leaves such a consecutive pair, with nothing re-keyed or
-  // not between them)
-  bool amb = false;
-  if (need != 0u) {
+    for (int q = qoff + 1; q < qoff + nneed; ++q) {
+      const uint32_t ie = it_e[q];
+      const float h = it_h[q], l = it_l[q], c = it_s[q];
+      int p = q;
 #pragma unroll 1
-    for (int j = 1; j < n; ++j) {
-      const float h = kh[j], l = kl[j], c = ks[j], z = sc[j];
-      const int i = ii[j];
-      const bool r = rk[j];
-      int p = j;
-      while (p > 0 && (df_gt(h, l, kh[p - 1], kl[p - 1]) ||
-                       (h == kh[p - 1] && l == kl[p - 1] && i < ii[p - 1]))) {
-        kh[p] = kh[p - 1], kl[p] = kl[p - 1], ks[p] = ks[p - 1], sc[p] = sc[p - 1];
-        ii[p] = ii[p - 1], rk[p] = rk[p - 1];
+      while (p > qoff) {
+        const float ph = it_h[p - 1], pl = it_l[p - 1];
+        const bool ahead = df_gt(h, l, ph, pl) ||
+                           (h == ph && l == pl && (ie >> 16) < (it_e[p - 1] >> 16));
+        if (!ahead) break;
+        it_e[p] = it_e[p - 1], it_h[p] = ph, it_l[p] = pl, it_s[p] = it_s[p - 1];
         --p;
       }
-      kh[p] = h, kl[p] = l, ks[p] = c, sc[p] = z, ii[p] = i, rk[p] = r;
+      it_e[p] = ie, it_h[p] = h, it_l[p] = l, it_s[p] = c;
     }
+    // consecutive items must be distinct or come from identical inputs (a
+    // misordered pair always leaves such a consecutive pair)
 #pragma unroll 1
-    for (int j = 0; j + 1 < n; ++j) {
-      if (rk[j] && rk[j + 1] && !near_distinct(kh[j], kl[j], ks[j], kh[j + 1], kl[j + 1], ks[j + 1])) {
-        const bool same = zq[ii[j] * BM + lane] == zq[ii[j + 1] * BM + lane] &&
-                          (sb ? sb[ii[j]] == sb[ii[j + 1]] : true);
+    for (int q = qoff; q + 1 < qoff + nneed; ++q) {
+      if (!near_distinct(it_h[q], it_l[q], it_s[q], it_h[q + 1], it_l[q + 1], it_s[q + 1])) {
+        const int e0 = (int)(it_e[q] >> 16), e1 = (int)(it_e[q + 1] >> 16);
+        const bool same = zq[e0 * BM + lane] == zq[e1 * BM + lane] && (sb ? sb[e0] == sb[e1] : true);
         if (!same) amb = true;
       }
     }
   }
   // rare: FP64 keys decide the rows the double-float keys could not (it
-  // reads the list as still stored)
-  if (__any_sync(kFull, amb)) refine_fp64<KC>(l_o, l_i, l_z, need, amb, qoff, qtotal, zq, sb, wl);
+  // reads the list as still stored and pools its own items)
+  if (__any_sync(kFull, amb)) {
+    __syncwarp();
+    if (amb) {  // back to slot order (the other rows keep their sorted items)
+      int q = qoff;
+#pragma unroll 1
+      for (int j = 0; j < KC; ++j)
+        if ((need >> j) & 1u)
+          wl[q++] = ((uint32_t)l_i[j * BM] << 16) | ((uint32_t)lane << 5) | (uint32_t)j;
+    }
+    __syncwarp();
+    refine_fp64<KC>(l_o, l_i, l_z, need, amb, qoff, qtotal, zq, sb, wl);
+  }
   if (need != 0u && !amb) {
+    // the sorted items' scores (from their original slots), then the refill
+#pragma unroll 1
+    for (int q = qoff; q < qoff + nneed; ++q) it_s[q] = l_z[(int)(it_e[q] & 31u) * BM];
+    int q = qoff;
 #pragma unroll 1
     for (int j = 0; j < KC; ++j) {
-      l_i[j * BM] = ii[j];
-      l_z[j * BM] = sc[j];
+      if ((need >> j) & 1u) {
+        l_i[j * BM] = (int)(it_e[q] >> 16);
+        l_z[j * BM] = it_s[q];
+        ++q;
+      }
     }
   }
   return close && !in_list;
@@ -643,6 +666,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w))
                      : "memory");
       pdl_wait();
+      const uint64_t pol_x = policy_evict_first(), pol_w = policy_evict_last();
       int issued = 0;
       unsigned want = 0u;  // NVFP4: the flag value of a tile decoded by this launch
       bool go = true;
@@ -657,15 +681,15 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         uint8_t* st = tiles + (size_t)s * p.stage_bytes;
         const uint32_t fb = smem_u32(&full[s]);
         mbar_expect_tx(fb, p.a_bytes + p.b_bytes);
-        tma_load_2d(smem_u32(st), &tmap_x, kb * BK, m0, fb);
+        tma_load_2d(smem_u32(st), &tmap_x, kb * BK, m0, fb, pol_x);
         ++issued;
         if (FP4) {
           if (!wait_flag(p.wsync + 2 + kb, want)) break;
           asm volatile("fence.proxy.async.global;" ::: "memory");
-          bulk_load(smem_u32(st + p.a_bytes), p.wdec + (size_t)kb * p.b_bytes, p.b_bytes, fb);
+          bulk_load(smem_u32(st + p.a_bytes), p.wdec + (size_t)kb * p.b_bytes, p.b_bytes, fb, pol_w);
         } else {
           if (p.mc == 1) {
-            tma_load_2d(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, 0, fb);
+            tma_load_2d(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, 0, fb, pol_w);
           } else {
             // this CTA's share of the W tile, written into every CTA of the pair
             const int rows = E / p.mc;
