@@ -119,6 +119,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The CTA-pair form: the completion goes to the mbarrier at `bar`, a
+// shared::cluster address that may lie in the other CTA of the pair (both
+// CTAs load their own operand halves and signal the even CTA's barrier).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0,
+                                                 int c1, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // L2 eviction policies: x streams through once (first to go), W_gate is
 // read by every CTA (last to go). Keeping the stream from flushing the
 // rest of L2 also keeps the kernel's own code there: the epilogue's rarely
@@ -152,17 +164,6 @@ __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(bar),
       "h"(cta_mask)
-      : "memory");
-}
-
-// 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned
-// addresses, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -213,8 +214,8 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 
 // Instruction descriptor, kind::f16: FP32 accumulator, BF16 A and B, both
 // K-major, N = E, M = 128.
-__host__ __device__ constexpr uint32_t idesc_bf16(int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_bf16(int N, int M = BM) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
@@ -225,6 +226,34 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// A CTA pair's MMA (M = 256: each CTA's 128 rows of A, each CTA's half of
+// the N rows of B, D in each CTA's tensor memory), issued by the even CTA.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the mbarrier at this offset in both CTAs of the pair once the
+// pair MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -565,9 +594,9 @@ struct TcParams {
   uint32_t stage_bytes, a_bytes, b_bytes;
   int tmem_cols;
   int mc;  // CTAs per cluster sharing each W tile through TMA multicast (1 or 2)
-  // NVFP4 only, both in the workspace: W decoded to BF16 (one swizzled
-  // [E x 64] tile per k-step), and [0] claim counter, [1] epoch, [2 + kb]
-  // flag of tile kb
+  int pair;  // CTA pairs run M = 256 MMAs, each CTA holding half of every W tile
+  // NVFP4 only, both in the workspace: W decoded to a BF16 [E, H] copy,
+  // and [0] claim counter, [1] epoch, [2 + kb] flag of column block kb
   uint8_t* wdec;
   unsigned* wsync;
 };
@@ -607,7 +636,7 @@ __device__ void pair_table(const int32_t* r0, const int32_t* r1, int k, int32_t*
   *count = n;
 }
 
-template <int KC, bool FP4>
+template <int KC, bool FP4, bool PAIR>
 __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
     k_tc_router(const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_w, const TcParams p) {
@@ -632,7 +661,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int producer_warp = kEpiWarps, mma_warp = kEpiWarps + 1;
   const int m0 = blockIdx.x * BM;
-  const int crank = p.mc > 1 ? (int)cluster_rank() : 0;
+  const int crank = (PAIR || p.mc > 1) ? (int)cluster_rank() : 0;
   const int nk = a.H / BK;
   const int E = a.E;
 
@@ -646,25 +675,42 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == mma_warp) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(p.tmem_cols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (PAIR) {
+      // both CTAs of the pair allocate; the MMAs use the even CTA's address
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(p.tmem_cols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(p.tmem_cols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // the pair's barriers are initialised and its allocations made before
+  // either CTA signals the other
+  if (PAIR) cluster_sync_tc();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_own = *tmem_slot;
+  uint32_t tmem = tmem_own;
+  if (PAIR) {
+    asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                 : "=r"(tmem)
+                 : "r"(mapa_u32(smem_u32(tmem_slot), 0u))
+                 : "memory");
+  }
 
   pdl_launch_dependents();
 
   if (warp == producer_warp) {
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x)) : "memory");
-      if (!FP4)
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w))
-                     : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
       pdl_wait();
       const uint64_t pol_x = policy_evict_first(), pol_w = policy_evict_last();
       int issued = 0;
@@ -680,14 +726,27 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) break;
         uint8_t* st = tiles + (size_t)s * p.stage_bytes;
         const uint32_t fb = smem_u32(&full[s]);
+        if (PAIR) {
+          // both CTAs' halves land on the even CTA's barrier
+          const uint32_t fb0 = mapa_u32(fb, 0u);
+          if (crank == 0) mbar_expect_tx(fb, 2u * (p.a_bytes + p.b_bytes));
+          tma_load_2d_pair(smem_u32(st), &tmap_x, kb * BK, m0, fb0, pol_x);
+          ++issued;
+          if (FP4) {
+            if (!wait_flag(p.wsync + 2 + kb, want)) break;
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
+          tma_load_2d_pair(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, crank * (E / 2), fb0, pol_w);
+          continue;
+        }
         mbar_expect_tx(fb, p.a_bytes + p.b_bytes);
         tma_load_2d(smem_u32(st), &tmap_x, kb * BK, m0, fb, pol_x);
         ++issued;
-        if (FP4) {
+        if (FP4) {  // the decoded copy: wait for this k-step's columns
           if (!wait_flag(p.wsync + 2 + kb, want)) break;
           asm volatile("fence.proxy.async.global;" ::: "memory");
-          bulk_load(smem_u32(st + p.a_bytes), p.wdec + (size_t)kb * p.b_bytes, p.b_bytes, fb, pol_w);
-        } else {
+        }
+        {
           if (p.mc == 1) {
             tma_load_2d(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, 0, fb, pol_w);
           } else {
@@ -698,12 +757,30 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
           }
         }
       }
-      // let copies still in flight land before the CTA can exit
-      for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
-        mbar_wait(smem_u32(&full[kb % S]), (uint32_t)(kb / S) & 1u);
+      // let copies still in flight land before the CTA can exit (a pair's
+      // odd CTA cannot see them: its exit waits for the pair's last MMA)
+      if (!PAIR || crank == 0)
+        for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
+          mbar_wait(smem_u32(&full[kb % S]), (uint32_t)(kb / S) & 1u);
     }
   } else if (warp == mma_warp) {
-    if (lane == 0) {
+    if (PAIR && lane == 0 && crank == 0) {
+      const uint32_t idesc = idesc_bf16(E, 2 * BM);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % S;
+        const uint32_t ph = (uint32_t)(kb / S) & 1u;
+        if (!mbar_wait(smem_u32(&full[s]), ph)) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(tiles + (size_t)s * p.stage_bytes);
+        const uint32_t sb = sa + p.a_bytes;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16_pair(tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32), idesc,
+                        (kb > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_pair(smem_u32(&empty[s]));
+      }
+      mma_commit_pair(smem_u32(accf));
+    } else if (!PAIR && lane == 0) {
       const uint32_t idesc = idesc_bf16(E);
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % S;
@@ -765,10 +842,10 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
     asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
     if (FP4) {
       // NVFP4: W is decoded once per launch, not once per CTA. The CTAs claim
-      // k-step tiles from a counter in the workspace; the 256 threads of a
-      // claim decode the tile (thread r owns row r) into the exact BF16
-      // [E x 64] layout the MMA reads, 128-byte swizzle included, and flag
-      // it with this launch's epoch; producers copy flagged tiles as they are.
+      // k-step column blocks from a counter in the workspace; the 256 threads
+      // of a claim decode the E x 64 block (thread r owns row r) into a BF16
+      // [E, H] copy and flag it with this launch's epoch; producers load
+      // flagged blocks with the same TMA tiles as BF16 weights.
       // Claims never wait, so no CTA needs another to be resident. Each CTA
       // makes one failing claim; the last of them (ticket nk + grid - 1)
       // resets the counter and advances the epoch for the next launch.
@@ -806,7 +883,8 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
           const uint32_t sc =
               __ldg(reinterpret_cast<const uint32_t*>(a.w_scales + (size_t)r * Hs + t * (BK / 16)));
           const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-          uint8_t* dst = p.wdec + (size_t)t * p.b_bytes + (size_t)r * 128;
+          // row r, elements 64t..64t+63 of the decoded [E, H] BF16 copy
+          uint8_t* dst = p.wdec + ((size_t)r * a.H + (size_t)t * BK) * 2;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {  // 16-byte chunk c = elements 8c..8c+7
             // the block scale in BF16 (exact: at most 4 significant bits), twice
@@ -821,8 +899,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
               v = __hmul2(v, scale2);  // exact: the product has at most 6 significant bits
               outw[jj] = *reinterpret_cast<const uint32_t*>(&v);
             }
-            const int phys = c ^ (r & 7);  // 128-byte swizzle: chunk index XOR row mod 8
-            *reinterpret_cast<uint4*>(dst + phys * 16) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+            *reinterpret_cast<uint4*>(dst + c * 16) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
           }
         }
         // the producers read the tile through the async proxy
@@ -1141,13 +1218,19 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // the peer may still signal this CTA's barriers until it is done as well
-  if (p.mc > 1) cluster_sync_tc();
+  // the peer may still signal this CTA's barriers (or read its tensor
+  // memory) until it is done as well
+  if (PAIR || p.mc > 1) cluster_sync_tc();
   if (warp == mma_warp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(p.tmem_cols)
-                 : "memory");
+    if (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_own),
+                   "r"(p.tmem_cols)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_own),
+                   "r"(p.tmem_cols)
+                   : "memory");
   }
 }
 
@@ -1184,23 +1267,24 @@ bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows)
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KC, bool FP4>
+template <int KC, bool FP4, bool PAIR>
 cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcParams& p,
                       size_t smem, bool pdl, cudaStream_t stream) {
-  auto kern = k_tc_router<KC, FP4>;
+  auto kern = k_tc_router<KC, FP4, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   const int tiles = (p.a.M + BM - 1) / BM;
-  cfg.gridDim = dim3((tiles + p.mc - 1) / p.mc * p.mc);
+  const int cl = PAIR ? 2 : p.mc;
+  cfg.gridDim = dim3((tiles + cl - 1) / cl * cl);
   cfg.blockDim = dim3((kEpiWarps + 2) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int na = 0;
-  if (p.mc > 1) {
+  if (cl > 1) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = p.mc;
+    attr[na].val.clusterDim.x = cl;
     attr[na].val.clusterDim.y = 1;
     attr[na].val.clusterDim.z = 1;
     ++na;
@@ -1215,17 +1299,17 @@ cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcPara
   return cudaLaunchKernelEx(&cfg, kern, mx, mw, p);
 }
 
-template <bool FP4>
+template <bool FP4, bool PAIR>
 cudaError_t dispatch_k(const CUtensorMap& mx, const CUtensorMap& mw, const TcParams& p,
                        size_t smem, bool pdl, cudaStream_t s) {
   // KC >= k + 2: the list keeps one key past the (k+1)-th, so a near tie at
   // the k / k+1 boundary can be settled inside the list
   const int k = p.a.k;
-  if (k <= 2) return launch_kc<4, FP4>(mx, mw, p, smem, pdl, s);
-  if (k <= 4) return launch_kc<6, FP4>(mx, mw, p, smem, pdl, s);
-  if (k <= 6) return launch_kc<8, FP4>(mx, mw, p, smem, pdl, s);
-  if (k <= 8) return launch_kc<10, FP4>(mx, mw, p, smem, pdl, s);
-  return launch_kc<18, FP4>(mx, mw, p, smem, pdl, s);
+  if (k <= 2) return launch_kc<4, FP4, PAIR>(mx, mw, p, smem, pdl, s);
+  if (k <= 4) return launch_kc<6, FP4, PAIR>(mx, mw, p, smem, pdl, s);
+  if (k <= 6) return launch_kc<8, FP4, PAIR>(mx, mw, p, smem, pdl, s);
+  if (k <= 8) return launch_kc<10, FP4, PAIR>(mx, mw, p, smem, pdl, s);
+  return launch_kc<18, FP4, PAIR>(mx, mw, p, smem, pdl, s);
 }
 
 }  // namespace
@@ -1255,8 +1339,17 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
     p.wsync = a.ticket;
     p.wdec = reinterpret_cast<uint8_t*>(a.ticket) + tc_flag_bytes(a.H);
   }
+  // CTA pairs (the default; GBR_TC_PAIR=0 turns them off): each CTA stages
+  // its 128 rows of x and half of the W tile, and the even CTA issues
+  // M = 256 MMAs for both, so each SM's shared memory carries a third less
+  // traffic per k-step
+  static const bool pair_env = [] {
+    const char* v = getenv("GBR_TC_PAIR");
+    return !(v && v[0] == '0');
+  }();
+  p.pair = pair_env && a.E % 32 == 0;
   p.a_bytes = BM * BK * 2;
-  p.b_bytes = (uint32_t)a.E * BK * 2;
+  p.b_bytes = (uint32_t)(p.pair ? a.E / 2 : a.E) * BK * 2;
   p.stage_bytes = p.a_bytes + p.b_bytes;
   const size_t extra = 1024 /*align*/ + 2 * 8 * 8 + 8 + 16 + BM * kMaxK * 4;
   const size_t budget = 227 * 1024 - 4096;  // the rest holds the static shared arrays
@@ -1280,16 +1373,18 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
     const char* v = getenv("GBR_TC_MULTICAST");
     return (v && v[0] == '1') ? 2 : 1;
   }();
-  p.mc = (!fp4 && a.E % 16 == 0) ? mc_env : 1;
+  p.mc = (!fp4 && !p.pair && a.E % 16 == 0) ? mc_env : 1;
   CUtensorMap mx, mw;
   if (!make_map(&mx, a.x, a.M, a.H, BM)) return cudaErrorInvalidValue;
-  if (fp4) {
-    mw = mx;  // unused: the decoded W tiles arrive by 1-D bulk copies
-  } else if (!make_map(&mw, a.w, a.E, a.H, a.E / p.mc)) {
+  // NVFP4: the kernel decodes W into the workspace as a BF16 [E, H] copy
+  if (!make_map(&mw, fp4 ? static_cast<const void*>(p.wdec) : a.w, a.E, a.H,
+                p.pair ? a.E / 2 : a.E / p.mc))
     return cudaErrorInvalidValue;
-  }
-  return fp4 ? dispatch_k<true>(mx, mw, p, smem, pdl, stream)
-             : dispatch_k<false>(mx, mw, p, smem, pdl, stream);
+  if (p.pair)
+    return fp4 ? dispatch_k<true, true>(mx, mw, p, smem, pdl, stream)
+               : dispatch_k<false, true>(mx, mw, p, smem, pdl, stream);
+  return fp4 ? dispatch_k<true, false>(mx, mw, p, smem, pdl, stream)
+             : dispatch_k<false, false>(mx, mw, p, smem, pdl, stream);
 }
 
 unsigned* status_word() {

@@ -106,3 +106,23 @@ def test_full_prefill_sampled_rows(w_dtype):
 
 def test_no_timeout_recorded():
     assert R.router_device_status(clear=True) == R.GBR_OK
+
+
+def test_single_cta_variant():
+    """The prefill kernel runs CTA pairs by default; GBR_TC_PAIR=0 selects
+    the single-CTA form (one CTA stages the whole W tile and issues M = 128
+    MMAs). The setting is read once per process, so a child checks it."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("from tests.test_prefill_gpu import small_prefill, check_case; "
+            "from moe_expert_router_02_gb300 import router as R, synth; "
+            "check_case(small_prefill(300, seed=31), expect_regime=R.GBR_REGIME_TC); "
+            "check_case(small_prefill(200, E=96, k=6, seed=32)); "
+            "check_case(small_prefill(320, H=1024, seed=33, w_dtype=synth.NVFP4)); "
+            "assert R.router_device_status(clear=True) == R.GBR_OK")
+    env = dict(os.environ, GBR_TC_PAIR="0")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
