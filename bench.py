@@ -419,6 +419,9 @@ def run_detail(args, peaks):
     record("C1_softmax_M8_unfused", RouterSet(C["C1"], 8, LAYERS, flags=R.GBR_FLAG_UNFUSED))
     for M in (1, 16, 64):
         record(f"C2_sqrtsoftplus_bias_M{M}", RouterSet(C["C2"], M, LAYERS))
+    for M in (1, 16):  # the same router with NVFP4 W_gate (decoded in the kernel)
+        record(f"C2_sqrtsoftplus_bias_M{M}_nvfp4",
+               RouterSet(C["C2"], M, LAYERS, w_dtype=synth.NVFP4))
     record("C4_M2_router_table", RouterSet(C["C4"], 2, LAYERS, table=True))
     record("C4_M2_router_no_table", RouterSet(C["C4"], 2, LAYERS))
     if "C4_M2_router_table" in out:

@@ -97,6 +97,102 @@ __device__ __noinline__ int select_fp64(const Ld ld, const float* __restrict__ b
   return pick;
 }
 
+// The near-tie re-ranking of one row (all lanes call): every expert whose
+// FP32 key lies within `band` of the k-th is re-keyed; returns this lane's
+// pick (lane < k). Out of line: it runs rarely, and the common path's
+// instructions stay contiguous.
+template <int VPL, class Ld>
+__device__ __noinline__ int refine_near_ties(const Ld ld, const float* __restrict__ bias, int E,
+                                             int k, int kk, float sel_key, int sel_idx,
+                                             float band) {
+  const int lane = threadIdx.x & 31;
+  // re-rank every expert whose FP32 key lies within the band of the k-th
+  const float thr = __fsub_rd(__shfl_sync(kFull, sel_key, k - 1), band);
+  uint32_t cmask = 0;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    if (e < E) {
+      const float a = sqrt_softplus_f32(ld(e));
+      const float kv = bias ? a + __ldg(bias + e) : a;
+      if (kv >= thr) cmask |= 1u << j;
+    }
+  }
+  // double-float keys, one candidate per lane per round
+  float khi[VPL], klo[VPL], ksc[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) khi[j] = klo[j] = ksc[j] = 0.0f;
+  uint32_t todo = cmask;
+  while (__any_sync(kFull, todo != 0u)) {
+    const bool has = todo != 0u;
+    const int j = has ? __ffs(todo) - 1 : 0;
+    const int e = lane + 32 * j;
+    const float z = has ? ld(e) : 0.0f;
+    const float b = (has && bias) ? __ldg(bias + e) : 0.0f;
+    const NearKey nk = near_key_ool(z, b);
+#pragma unroll
+    for (int jj = 0; jj < VPL; ++jj) {
+      if (has && jj == j) {
+        khi[jj] = nk.hi;
+        klo[jj] = nk.lo;
+        ksc[jj] = nk.scale;
+      }
+    }
+    todo &= todo - 1u;
+  }
+  // k+1 rounds of (key desc, index asc) over the candidates; a pair of
+  // consecutive picks too close for the double-float keys, from
+  // different inputs, sends the row to FP64
+  bool amb = false;
+  float ph = 0.0f, pl = 0.0f, psc = 0.0f, pz = 0.0f, pb = 0.0f;
+  int pick = -1;
+  uint32_t left = cmask;
+  for (int r = 0; r < kk; ++r) {
+    float bh = -INFINITY, bl = 0.0f, bsc = 0.0f;
+    int bidx = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      if (((left >> j) & 1u) && (bidx == 0x7fffffff || df_gt(khi[j], klo[j], bh, bl))) {
+        bh = khi[j];
+        bl = klo[j];
+        bsc = ksc[j];
+        bidx = lane + 32 * j;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float oh = __shfl_xor_sync(kFull, bh, off);
+      const float ol = __shfl_xor_sync(kFull, bl, off);
+      const float os = __shfl_xor_sync(kFull, bsc, off);
+      const int oi = __shfl_xor_sync(kFull, bidx, off);
+      const bool take = oi != 0x7fffffff &&
+                        (bidx == 0x7fffffff || df_gt(oh, ol, bh, bl) ||
+                         (oh == bh && ol == bl && oi < bidx));
+      if (take) {
+        bh = oh;
+        bl = ol;
+        bsc = os;
+        bidx = oi;
+      }
+    }
+    if (bidx == 0x7fffffff) break;  // fewer candidates than rounds
+    if ((bidx & 31) == lane) left &= ~(1u << (bidx >> 5));
+    const float wz = ld(bidx);
+    const float wb = bias ? __ldg(bias + bidx) : 0.0f;
+    if (r > 0 && !near_distinct(ph, pl, psc, bh, bl, bsc) && !(pz == wz && pb == wb))
+      amb = true;
+    ph = bh, pl = bl, psc = bsc, pz = wz, pb = wb;
+    if (lane == r) pick = bidx;
+  }
+  if (!amb) {
+    if (lane < k) sel_idx = pick;
+  } else {
+    const int pick64 = select_fp64<VPL>(ld, bias, k, cmask);
+    if (lane < k) sel_idx = pick64;
+  }
+  return sel_idx;
+}
+
 // One warp selects the top-k of one row of E <= 32*VPL logits.
 // Lane r < k writes slot r of out_idx / out_w and, if sel_out is not null,
 // sel_out[r] (for a route table). All 32 lanes must call.
@@ -105,10 +201,12 @@ __device__ __noinline__ int select_fp64(const Ld ld, const float* __restrict__ b
 // sorts them once; a round takes the warp maximum key (redux.sync), then
 // the lowest index among the lanes holding it (redux.sync), and the winning
 // lane shifts its sorted list by one. Scores are read back once at the end.
-template <int VPL, class Ld>
-__device__ __noinline__ void warp_select_row(const Ld ld, const float* __restrict__ bias, int E,
-                                             int k, int act, int32_t* __restrict__ out_idx,
-                                             float* __restrict__ out_w, int32_t* sel_out) {
+// One copy per activation: the kernels run it once per row and call, so the
+// instruction fetches of code for the other activation would be paid cold.
+template <int VPL, int act, class Ld>
+__device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __restrict__ bias,
+                                                 int E, int k, int32_t* __restrict__ out_idx,
+                                                 float* __restrict__ out_w, int32_t* sel_out) {
   const int lane = threadIdx.x & 31;
   uint64_t pk[VPL];  // (key << 32) | (0xffffffff - expert); 0 = empty
   float amax = 0.0f, kabs = 0.0f;
@@ -158,92 +256,8 @@ __device__ __noinline__ void warp_select_row(const Ld ld, const float* __restric
     const float next_key = __shfl_down_sync(kFull, sel_key, 1);
     // the difference rounded down: a gap of at most band is never missed
     const bool close = (lane < kk - 1) && __fsub_rd(sel_key, next_key) <= band;
-    if (__any_sync(kFull, close)) {
-      // re-rank every expert whose FP32 key lies within the band of the k-th
-      const float thr = __fsub_rd(__shfl_sync(kFull, sel_key, k - 1), band);
-      uint32_t cmask = 0;
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E) {
-          const float a = sqrt_softplus_f32(ld(e));
-          const float kv = bias ? a + __ldg(bias + e) : a;
-          if (kv >= thr) cmask |= 1u << j;
-        }
-      }
-      // double-float keys, one candidate per lane per round
-      float khi[VPL], klo[VPL], ksc[VPL];
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) khi[j] = klo[j] = ksc[j] = 0.0f;
-      uint32_t todo = cmask;
-      while (__any_sync(kFull, todo != 0u)) {
-        const bool has = todo != 0u;
-        const int j = has ? __ffs(todo) - 1 : 0;
-        const int e = lane + 32 * j;
-        const float z = has ? ld(e) : 0.0f;
-        const float b = (has && bias) ? __ldg(bias + e) : 0.0f;
-        const NearKey nk = near_key_ool(z, b);
-#pragma unroll
-        for (int jj = 0; jj < VPL; ++jj) {
-          if (has && jj == j) {
-            khi[jj] = nk.hi;
-            klo[jj] = nk.lo;
-            ksc[jj] = nk.scale;
-          }
-        }
-        todo &= todo - 1u;
-      }
-      // k+1 rounds of (key desc, index asc) over the candidates; a pair of
-      // consecutive picks too close for the double-float keys, from
-      // different inputs, sends the row to FP64
-      bool amb = false;
-      float ph = 0.0f, pl = 0.0f, psc = 0.0f, pz = 0.0f, pb = 0.0f;
-      int pick = -1;
-      uint32_t left = cmask;
-      for (int r = 0; r < kk; ++r) {
-        float bh = -INFINITY, bl = 0.0f, bsc = 0.0f;
-        int bidx = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-          if (((left >> j) & 1u) && (bidx == 0x7fffffff || df_gt(khi[j], klo[j], bh, bl))) {
-            bh = khi[j];
-            bl = klo[j];
-            bsc = ksc[j];
-            bidx = lane + 32 * j;
-          }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float oh = __shfl_xor_sync(kFull, bh, off);
-          const float ol = __shfl_xor_sync(kFull, bl, off);
-          const float os = __shfl_xor_sync(kFull, bsc, off);
-          const int oi = __shfl_xor_sync(kFull, bidx, off);
-          const bool take = oi != 0x7fffffff &&
-                            (bidx == 0x7fffffff || df_gt(oh, ol, bh, bl) ||
-                             (oh == bh && ol == bl && oi < bidx));
-          if (take) {
-            bh = oh;
-            bl = ol;
-            bsc = os;
-            bidx = oi;
-          }
-        }
-        if (bidx == 0x7fffffff) break;  // fewer candidates than rounds
-        if ((bidx & 31) == lane) left &= ~(1u << (bidx >> 5));
-        const float wz = ld(bidx);
-        const float wb = bias ? __ldg(bias + bidx) : 0.0f;
-        if (r > 0 && !near_distinct(ph, pl, psc, bh, bl, bsc) && !(pz == wz && pb == wb))
-          amb = true;
-        ph = bh, pl = bl, psc = bsc, pz = wz, pb = wb;
-        if (lane == r) pick = bidx;
-      }
-      if (!amb) {
-        if (lane < k) sel_idx = pick;
-      } else {
-        const int pick64 = select_fp64<VPL>(ld, bias, k, cmask);
-        if (lane < k) sel_idx = pick64;
-      }
-    }
+    if (__any_sync(kFull, close))
+      sel_idx = refine_near_ties<VPL>(ld, bias, E, k, kk, sel_key, sel_idx, band);
   }
 
   // weights over the chosen k, summed in slot order
@@ -276,6 +290,16 @@ __device__ __noinline__ void warp_select_row(const Ld ld, const float* __restric
     out_w[lane] = (sum > 0.0f) ? s / sum : 1.0f / (float)k;
     if (sel_out) sel_out[lane] = sel_idx;
   }
+}
+
+template <int VPL, class Ld>
+__device__ __forceinline__ void warp_select_row(const Ld ld, const float* __restrict__ bias, int E,
+                                                int k, int act, int32_t* __restrict__ out_idx,
+                                                float* __restrict__ out_w, int32_t* sel_out) {
+  if (act == ACT_SOFTMAX)
+    warp_select_row_act<VPL, ACT_SOFTMAX>(ld, bias, E, k, out_idx, out_w, sel_out);
+  else
+    warp_select_row_act<VPL, ACT_SQRT_SOFTPLUS>(ld, bias, E, k, out_idx, out_w, sel_out);
 }
 
 // One warp emits the unique-route table of one group of T tokens x k slots
