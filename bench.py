@@ -422,6 +422,8 @@ def run_detail(args, peaks):
     for M in (1, 16):  # the same router with NVFP4 W_gate (decoded in the kernel)
         record(f"C2_sqrtsoftplus_bias_M{M}_nvfp4",
                RouterSet(C["C2"], M, LAYERS, w_dtype=synth.NVFP4))
+    for M in (1, 16):  # the sigmoid score with the same selection bias
+        record(f"C2_sigmoid_bias_M{M}", RouterSet(dict(C["C2"], act=synth.SIGMOID), M, LAYERS))
     record("C4_M2_router_table", RouterSet(C["C4"], 2, LAYERS, table=True))
     record("C4_M2_router_no_table", RouterSet(C["C4"], 2, LAYERS))
     if "C4_M2_router_table" in out:
@@ -441,8 +443,10 @@ def run_detail(args, peaks):
     # prefill
     cfg3 = C["C3"]
     flops = 2 * cfg3["M"] * cfg3["H"] * cfg3["E"]
-    for name, wd in (("C3_prefill_bf16", synth.BF16), ("C3_prefill_nvfp4", synth.NVFP4)):
-        rs = RouterSet(cfg3, cfg3["M"], 1, w_dtype=wd, pool_bytes=0)
+    for name, wd, act in (("C3_prefill_bf16", synth.BF16, cfg3["act"]),
+                          ("C3_prefill_nvfp4", synth.NVFP4, cfg3["act"]),
+                          ("C3_prefill_bf16_sigmoid", synth.BF16, synth.SIGMOID)):
+        rs = RouterSet(dict(cfg3, act=act), cfg3["M"], 1, w_dtype=wd, pool_bytes=0)
         record(name, rs, steps=10, flops=flops)
     return out
 

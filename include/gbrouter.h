@@ -8,11 +8,13 @@
  *      gateLogits[E], "one kernel producing inds/scores directly from
  *      postNorm", logits held on chip instead of round-tripping);
  *   2. the score: softmax over E, or a = sqrt(softplus(logit)) with the
- *      stable softplus max(z,0) + log1p(exp(-|z|)) and a per-expert bias
- *      added for selection only
+ *      stable softplus max(z,0) + log1p(exp(-|z|)), or a = sigmoid(logit) =
+ *      1 / (1 + exp(-logit)); with the last two a per-expert bias is added
+ *      for selection only
  *      (dense_router_decode commit page, "DenseRouterDecodeKernel: BF16 GEMM
  *      + sqrt(softplus) + bias + top-k", "Numerically stable softplus", heap
- *      of "(score, index, unbiased act)");
+ *      of "(score, index, unbiased act)"; the sigmoid score is this
+ *      library's widening of the same biased-score contract);
  *   3. top-k under the fixed comparison: higher key first, an equal key goes
  *      to the lower expert index; slots are returned in that order
  *      (qwisp issue #145, "Bit-exactness": the tie-break order is part of
@@ -62,7 +64,7 @@ enum {
 };
 
 /* score activation */
-enum { GBR_ACT_SOFTMAX = 0, GBR_ACT_SQRT_SOFTPLUS = 1 };
+enum { GBR_ACT_SOFTMAX = 0, GBR_ACT_SQRT_SOFTPLUS = 1, GBR_ACT_SIGMOID = 2 };
 
 /* element types. NVFP4 is for W_gate only: packed E2M1 codes [E, H/2]
  * (element 2j in the low nibble of byte j, 2j+1 in the high nibble), one
@@ -156,17 +158,18 @@ int router_select(const float* logits, const float* bias, int M, int E, int k, i
 
 /*
  * router_near_tie_keys — the key the selection re-ranks near ties with
- * (sqrt-softplus + bias only): key[i] = sqrt(softplus(z[i])) + bias[i]
- * (bias nullable: 0) returned as an unevaluated sum key_hi[i] + key_lo[i]
- * of two floats with |lo| <= ulp(hi)/2, from FP32 arithmetic only
- * (double-float evaluation, relative error near 2^-42; |z| > 30 goes
- * through FP64). Step 2 of the router as the guard-band refine evaluates
- * it; exposed so that its error can be measured against an FP64
- * definition. z, bias, key_hi, key_lo: device FP32 [n]. Errors: GBR_EINVAL
- * for n < 0 or null z / key pointers (n == 0: no launch).
+ * (the biased activations): key[i] = a(z[i]) + bias[i], a = sqrt-softplus
+ * (act = GBR_ACT_SQRT_SOFTPLUS) or sigmoid (GBR_ACT_SIGMOID), bias nullable
+ * (0), returned as an unevaluated sum key_hi[i] + key_lo[i] of two floats
+ * with |lo| <= ulp(hi)/2, from FP32 arithmetic only (double-float
+ * evaluation, relative error near 2^-42; |z| > 30 goes through FP64).
+ * Step 2 of the router as the guard-band refine evaluates it; exposed so
+ * that its error can be measured against an FP64 definition. z, bias,
+ * key_hi, key_lo: device FP32 [n]. Errors: GBR_EINVAL for n < 0, another
+ * act, or null z / key pointers (n == 0: no launch).
  */
-int router_near_tie_keys(const float* z, const float* bias, int n, float* key_hi, float* key_lo,
-                         cudaStream_t stream);
+int router_near_tie_keys(const float* z, const float* bias, int n, int act, float* key_hi,
+                         float* key_lo, cudaStream_t stream);
 
 /*
  * route_table — step 5 alone for `groups` groups of T = tokens_per_group

@@ -24,7 +24,8 @@ struct Shape {
 // Argument checks that need no pointer values beyond null-ness.
 int check_shape(const Shape& s) {
   if (s.M < 0 || s.H < 1 || s.E < 1 || s.k < 1 || s.k > s.E) return GBR_EINVAL;
-  if (s.act != GBR_ACT_SOFTMAX && s.act != GBR_ACT_SQRT_SOFTPLUS) return GBR_EINVAL;
+  if (s.act != GBR_ACT_SOFTMAX && s.act != GBR_ACT_SQRT_SOFTPLUS && s.act != GBR_ACT_SIGMOID)
+    return GBR_EINVAL;
   if (s.act == GBR_ACT_SOFTMAX && s.has_bias) return GBR_EINVAL;
   if (s.x_dtype != GBR_F32 && s.x_dtype != GBR_BF16) return GBR_EINVAL;
   if (s.w_dtype != GBR_F32 && s.w_dtype != GBR_BF16 && s.w_dtype != GBR_NVFP4) return GBR_EINVAL;
@@ -233,7 +234,8 @@ int router_forward(const void* x, const void* W_gate, const float* bias, int M, 
 int router_select(const float* logits, const float* bias, int M, int E, int k, int act,
                   int32_t* out_idx, float* out_w, cudaStream_t stream) {
   if (M < 0 || E < 1 || k < 1 || k > E) return GBR_EINVAL;
-  if (act != GBR_ACT_SOFTMAX && act != GBR_ACT_SQRT_SOFTPLUS) return GBR_EINVAL;
+  if (act != GBR_ACT_SOFTMAX && act != GBR_ACT_SQRT_SOFTPLUS && act != GBR_ACT_SIGMOID)
+    return GBR_EINVAL;
   if (act == GBR_ACT_SOFTMAX && bias) return GBR_EINVAL;
   if (E > gbr::kMaxE || k > gbr::kMaxK) return GBR_EUNSUPPORTED;
   if (M == 0) return GBR_OK;
@@ -243,13 +245,14 @@ int router_select(const float* logits, const float* bias, int M, int E, int k, i
              : GBR_ECUDA;
 }
 
-int router_near_tie_keys(const float* z, const float* bias, int n, float* key_hi, float* key_lo,
-                         cudaStream_t stream) {
-  if (n < 0) return GBR_EINVAL;
+int router_near_tie_keys(const float* z, const float* bias, int n, int act, float* key_hi,
+                         float* key_lo, cudaStream_t stream) {
+  if (n < 0 || (act != GBR_ACT_SQRT_SOFTPLUS && act != GBR_ACT_SIGMOID)) return GBR_EINVAL;
   if (n == 0) return GBR_OK;
   if (!z || !key_hi || !key_lo) return GBR_EINVAL;
-  return gbr::launch_near_tie_keys(z, bias, n, key_hi, key_lo, stream) == cudaSuccess ? GBR_OK
-                                                                                       : GBR_ECUDA;
+  return gbr::launch_near_tie_keys(z, bias, n, act, key_hi, key_lo, stream) == cudaSuccess
+             ? GBR_OK
+             : GBR_ECUDA;
 }
 
 int route_table(const int32_t* idx, int groups, int tokens_per_group, int k, int32_t* out_unique,

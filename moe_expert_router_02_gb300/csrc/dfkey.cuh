@@ -139,39 +139,63 @@ __device__ __forceinline__ df32 sqrt_softplus_df(float z) {
   return fast_two_sum(s0, __fdiv_rn(res, __fmul_rn(2.0f, s0)));
 }
 
+// sigmoid(z) = 1 / (1 + exp(-z)) for |z| <= kDfMaxAbsZ: u = exp(-|z|) as
+// above, 1 / (1 + u) by one Newton step on the FP32 reciprocal, times u
+// when z < 0 (sigmoid(z) = u / (1 + u) there).
+__device__ __forceinline__ df32 sigmoid_df(float z) {
+  const float a = fabsf(z);
+  const float n = rintf(__fmul_rn(a, 0x1.715476p+0f));
+  const float r0 = __fmaf_rn(-n, 0x1.62e4p-1f, a);
+  const df32 nc2 = two_prod(n, 0x1.7f7d1cp-20f);
+  df32 r = df_add(df32{r0, 0.0f}, df32{-nc2.hi, -nc2.lo});
+  r = df_add_f(r, -__fmul_rn(n, 0x1.ef357ap-45f));
+  df32 u = df_add_f(expm1_df(df32{-r.hi, -r.lo}), 1.0f);
+  u = df_scale(u, __int_as_float((127 - (int)n) << 23));
+  const df32 s = df_add_f(u, 1.0f);  // 1 + u in [1, 2]
+  const float q0 = __fdiv_rn(1.0f, s.hi);
+  const df32 sq = two_prod(s.hi, q0);
+  const float res = __fsub_rn(__fsub_rn(__fsub_rn(1.0f, sq.hi), sq.lo), __fmul_rn(s.lo, q0));
+  const df32 inv = fast_two_sum(q0, __fmul_rn(q0, res));
+  return z >= 0.0f ? inv : df_mul(u, inv);
+}
+
 // Upper bound on |key32 - key| for FP32 keys whose largest activation is
 // amax and largest |key| is kabs: 2^-23 (2.25 amax + 0.5 kabs) + 2^-60,
 // every step rounded up.
-__device__ __forceinline__ float key_err_bound(float amax, float kabs) {
-  return __fadd_ru(__fmul_ru(__fmaf_ru(2.25f, amax, __fmul_ru(0.5f, kabs)), 0x1p-23f), 0x1p-60f);
+__device__ __forceinline__ float key_err_bound(float amax, float kabs, float coef = 2.25f) {
+  return __fadd_ru(__fmul_ru(__fmaf_ru(coef, amax, __fmul_ru(0.5f, kabs)), 0x1p-23f), 0x1p-60f);
 }
 
-// A near-tie key: sqrt(softplus(z)) + b as a double-float, with the scale
-// s + |key| its distinctness test uses. Beyond the double-float range of z
-// the activation comes from FP64.
+// A near-tie key: a(z) + b as a double-float (a = sqrt-softplus or sigmoid),
+// with the scale a + |key| its distinctness test uses. Beyond the
+// double-float range of z the activation comes from FP64.
 struct NearKey {
   float hi, lo, scale;
 };
 
 // FP64 activation split into two floats; out of line, so that no FP64
 // instruction is issued (not even predicated off) unless |z| is large.
-static __device__ __noinline__ df32 sqrt_softplus_split64(float z) {
-  const double v = sqrt_softplus_f64((double)z);
+static __device__ __noinline__ df32 act_split64(int act, float z) {
+  const double v = act_f64(act, (double)z);
   df32 s;
   s.hi = (float)v;
   s.lo = isfinite(s.hi) ? (float)(v - (double)s.hi) : 0.0f;
   return s;
 }
 
-__device__ __forceinline__ NearKey near_key(float z, float b) {
-  const df32 s = fabsf(z) <= kDfMaxAbsZ ? sqrt_softplus_df(z) : sqrt_softplus_split64(z);
+__device__ __forceinline__ NearKey near_key(int act, float z, float b) {
+  const df32 s = fabsf(z) <= kDfMaxAbsZ
+                     ? (act == ACT_SIGMOID ? sigmoid_df(z) : sqrt_softplus_df(z))
+                     : act_split64(act, z);
   const df32 key = df_add_f(s, b);
   return {key.hi, isfinite(key.hi) ? key.lo : 0.0f, __fadd_ru(fabsf(s.hi), fabsf(key.hi))};
 }
 
 // near_key out of line: its callers run on cold paths, where one shared
 // copy of the code costs fewer instruction fetches.
-static __device__ __noinline__ NearKey near_key_ool(float z, float b) { return near_key(z, b); }
+static __device__ __noinline__ NearKey near_key_ool(int act, float z, float b) {
+  return near_key(act, z, b);
+}
 
 // True when two near-tie keys are far enough apart that their double-float
 // order is the order FP64 gives.

@@ -10,9 +10,9 @@ namespace gbr {
 cudaError_t launch_select(const float* logits, const float* bias, int M, int E, int k, int act,
                           int32_t* out_idx, float* out_w, cudaStream_t stream);
 
-// Near-tie keys (double-float sqrt-softplus + bias) for n logits.
-cudaError_t launch_near_tie_keys(const float* z, const float* bias, int n, float* hi, float* lo,
-                                 cudaStream_t stream);
+// Near-tie keys (double-float activation + bias) for n logits.
+cudaError_t launch_near_tie_keys(const float* z, const float* bias, int n, int act, float* hi,
+                                 float* lo, cudaStream_t stream);
 
 cudaError_t launch_route_table(const int32_t* idx, int groups, int T, int k, int32_t* unique,
                                uint8_t* mask, uint8_t* map, int32_t* count, cudaStream_t stream);

@@ -55,7 +55,8 @@ extern "C" int router_forward_noalloc(const void* x, const void* W_gate, const f
                                       int H, int E, int k, int act, int32_t* out_idx,
                                       float* out_w, cudaStream_t stream) {
   if (M < 0 || H < 1 || E < 1 || k < 1 || k > E) return GBR_EINVAL;
-  if (act != GBR_ACT_SOFTMAX && act != GBR_ACT_SQRT_SOFTPLUS) return GBR_EINVAL;
+  if (act != GBR_ACT_SOFTMAX && act != GBR_ACT_SQRT_SOFTPLUS && act != GBR_ACT_SIGMOID)
+    return GBR_EINVAL;
   if (act == GBR_ACT_SOFTMAX && bias) return GBR_EINVAL;
   if (E > gbr::kMaxE || k > gbr::kMaxK) return GBR_EUNSUPPORTED;
   if (M > kNoAllocMaxM || E > kNoAllocMaxE) return GBR_EWORKSPACE;  // beyond the static scratch

@@ -37,9 +37,9 @@ __global__ void __launch_bounds__(kTblWarps * 32)
 }
 
 __global__ void k_near_tie_keys(const float* __restrict__ z, const float* __restrict__ bias, int n,
-                                float* __restrict__ hi, float* __restrict__ lo) {
+                                int act, float* __restrict__ hi, float* __restrict__ lo) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    const NearKey k = near_key(z[i], bias ? bias[i] : 0.0f);
+    const NearKey k = near_key(act, z[i], bias ? bias[i] : 0.0f);
     hi[i] = k.hi;
     lo[i] = k.lo;
   }
@@ -47,10 +47,10 @@ __global__ void k_near_tie_keys(const float* __restrict__ z, const float* __rest
 
 }  // namespace
 
-cudaError_t launch_near_tie_keys(const float* z, const float* bias, int n, float* hi, float* lo,
-                                 cudaStream_t stream) {
+cudaError_t launch_near_tie_keys(const float* z, const float* bias, int n, int act, float* hi,
+                                 float* lo, cudaStream_t stream) {
   const int blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
-  k_near_tie_keys<<<blocks, 256, 0, stream>>>(z, bias, n, hi, lo);
+  k_near_tie_keys<<<blocks, 256, 0, stream>>>(z, bias, n, act, hi, lo);
   return cudaGetLastError();
 }
 

@@ -9,13 +9,15 @@
 //                 chosen experts: w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0).
 //   sqrt-softplus a = sqrt(max(z,0) + log1p(exp(-|z|))), key = a + bias;
 //                 the weights use the unbiased a: w_j = a_j / sum_i a_i.
+//   sigmoid       a = 1 / (1 + exp(-z)), key = a + bias, weights as above
+//                 (the biased sigmoid score of the same page's routing).
 // Order (qwisp issue #145, "Bit-exactness"): higher key first, an equal key
 // goes to the lower expert index; -0.0 equals +0.0.
 //
-// Exactness of the sqrt-softplus ranking. FP32 keys carry a bounded error
-// (CUDA documents expf <= 2 ulp, log1pf <= 1 ulp, IEEE sqrtf): following
-// the three steps gives |key32 - key| <= 2^-23 (2.25 a + 0.5 |key|) plus a
-// tiny absolute term for subnormal softplus values. When two neighbouring
+// Exactness of the biased rankings. FP32 keys carry a bounded error (CUDA
+// documents expf <= 2 ulp, log1pf <= 1 ulp, IEEE sqrtf and division):
+// following the steps gives |key32 - key| <= 2^-23 (c a + 0.5 |key|) plus a
+// tiny absolute term, c = 2.25 for sqrt-softplus and 3 for sigmoid. When two neighbouring
 // keys among the first k+1 are closer than four times that bound, the
 // candidates within the band of the k-th key are re-ranked with
 // double-float keys (relative error near 2^-42, FP32 arithmetic only); a
@@ -60,7 +62,7 @@ __device__ __forceinline__ void sort_desc(uint64_t (&v)[VPL]) {
 // (key desc, index asc)); returns this lane's pick (lane < k). Out of line:
 // FP64 is slow on this part and must not be issued on the common path.
 template <int VPL, class Ld>
-__device__ __noinline__ int select_fp64(const Ld ld, const float* __restrict__ bias, int k,
+__device__ __noinline__ int select_fp64(const Ld ld, const float* __restrict__ bias, int act, int k,
                                         uint32_t cmask) {
   const int lane = threadIdx.x & 31;
   double k64[VPL];
@@ -69,7 +71,7 @@ __device__ __noinline__ int select_fp64(const Ld ld, const float* __restrict__ b
     const int e = lane + 32 * j;
     k64[j] = 0.0;
     if ((cmask >> j) & 1u)
-      k64[j] = sqrt_softplus_f64((double)ld(e)) + (bias ? (double)__ldg(bias + e) : 0.0);
+      k64[j] = act_f64(act, (double)ld(e)) + (bias ? (double)__ldg(bias + e) : 0.0);
   }
   int pick = -1;
   for (int r = 0; r < k; ++r) {
@@ -102,7 +104,7 @@ __device__ __noinline__ int select_fp64(const Ld ld, const float* __restrict__ b
 // pick (lane < k). Out of line: it runs rarely, and the common path's
 // instructions stay contiguous.
 template <int VPL, class Ld>
-__device__ __noinline__ int refine_near_ties(const Ld ld, const float* __restrict__ bias, int E,
+__device__ __noinline__ int refine_near_ties(const Ld ld, const float* __restrict__ bias, int act, int E,
                                              int k, int kk, float sel_key, int sel_idx,
                                              float band) {
   const int lane = threadIdx.x & 31;
@@ -113,7 +115,7 @@ __device__ __noinline__ int refine_near_ties(const Ld ld, const float* __restric
   for (int j = 0; j < VPL; ++j) {
     const int e = lane + 32 * j;
     if (e < E) {
-      const float a = sqrt_softplus_f32(ld(e));
+      const float a = act_f32(act, ld(e));
       const float kv = bias ? a + __ldg(bias + e) : a;
       if (kv >= thr) cmask |= 1u << j;
     }
@@ -129,7 +131,7 @@ __device__ __noinline__ int refine_near_ties(const Ld ld, const float* __restric
     const int e = lane + 32 * j;
     const float z = has ? ld(e) : 0.0f;
     const float b = (has && bias) ? __ldg(bias + e) : 0.0f;
-    const NearKey nk = near_key_ool(z, b);
+    const NearKey nk = near_key_ool(act, z, b);
 #pragma unroll
     for (int jj = 0; jj < VPL; ++jj) {
       if (has && jj == j) {
@@ -187,7 +189,7 @@ __device__ __noinline__ int refine_near_ties(const Ld ld, const float* __restric
   if (!amb) {
     if (lane < k) sel_idx = pick;
   } else {
-    const int pick64 = select_fp64<VPL>(ld, bias, k, cmask);
+    const int pick64 = select_fp64<VPL>(ld, bias, act, k, cmask);
     if (lane < k) sel_idx = pick64;
   }
   return sel_idx;
@@ -218,7 +220,7 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
       const float z = ld(e);
       float key = z;
       if (act != ACT_SOFTMAX) {
-        const float a = sqrt_softplus_f32(z);
+        const float a = act_f32(act, z);
         key = bias ? a + __ldg(bias + e) : a;
         amax = fmaxf(amax, a);
         kabs = fmaxf(kabs, fabsf(key));
@@ -248,16 +250,16 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
     }
   }
 
-  if (act == ACT_SQRT_SOFTPLUS) {
+  if (act != ACT_SOFTMAX) {
     // FP32 key error bound; non-negative floats order like their bit patterns
     const float amax_w = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(amax)));
     const float kabs_w = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(kabs)));
-    const float band = 4.0f * key_err_bound(amax_w, kabs_w);
+    const float band = 4.0f * key_err_bound(amax_w, kabs_w, act_err_coef(act));
     const float next_key = __shfl_down_sync(kFull, sel_key, 1);
     // the difference rounded down: a gap of at most band is never missed
     const bool close = (lane < kk - 1) && __fsub_rd(sel_key, next_key) <= band;
     if (__any_sync(kFull, close))
-      sel_idx = refine_near_ties<VPL>(ld, bias, E, k, kk, sel_key, sel_idx, band);
+      sel_idx = refine_near_ties<VPL>(ld, bias, act, E, k, kk, sel_key, sel_idx, band);
   }
 
   // weights over the chosen k, summed in slot order
@@ -267,12 +269,12 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
     const float z0 = __shfl_sync(kFull, sel_key, 0);
     if (lane < k) s = expf(sel_key - z0);
   } else {
-    if (lane < k) s = sqrt_softplus_f32(ld(sel_idx));
+    if (lane < k) s = act_f32(act, ld(sel_idx));
     const float smax = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(s)));
     if (!(smax >= 0x1p-50f)) {
       // every chosen activation is tiny (FP32 keeps few or no bits of it):
       // the ratios come from the log domain
-      const float la = lane < k ? log_sqrt_softplus(ld(sel_idx)) : -INFINITY;
+      const float la = lane < k ? log_act(act, ld(sel_idx)) : -INFINITY;
       float lm = la;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) lm = fmaxf(lm, __shfl_xor_sync(kFull, lm, off));
@@ -298,6 +300,8 @@ __device__ __forceinline__ void warp_select_row(const Ld ld, const float* __rest
                                                 float* __restrict__ out_w, int32_t* sel_out) {
   if (act == ACT_SOFTMAX)
     warp_select_row_act<VPL, ACT_SOFTMAX>(ld, bias, E, k, out_idx, out_w, sel_out);
+  else if (act == ACT_SIGMOID)
+    warp_select_row_act<VPL, ACT_SIGMOID>(ld, bias, E, k, out_idx, out_w, sel_out);
   else
     warp_select_row_act<VPL, ACT_SQRT_SOFTPLUS>(ld, bias, E, k, out_idx, out_w, sel_out);
 }

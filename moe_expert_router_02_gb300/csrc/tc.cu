@@ -362,8 +362,8 @@ struct TopList64 {
 
 // FP64 key of one expert; out of line so that the FP64 work runs only for
 // the entries that need it.
-__device__ __noinline__ double key64(float z, float b) {
-  return sqrt_softplus_f64((double)z) + (double)b;
+__device__ __noinline__ double key64(int act, float z, float b) {
+  return act_f64(act, (double)z) + (double)b;
 }
 
 // FP64 re-ranking of one row (see select.cuh): every lane of the warp calls
@@ -371,7 +371,7 @@ __device__ __noinline__ double key64(float z, float b) {
 // take part in the loads. Kept out of line so the common path's top list
 // stays in registers.
 template <int KC, bool FP4>
-__device__ __noinline__ void refine_row(uint32_t trow, int E, float g, const float* bias,
+__device__ __noinline__ void refine_row(uint32_t trow, int E, float g, const float* bias, int act,
                                         float thr, bool close, int* out_i, float* out_z) {
   // out_i / out_z: KC entries, BM apart (shared memory)
   TopList64<KC> t64;
@@ -385,10 +385,10 @@ __device__ __noinline__ void refine_row(uint32_t trow, int E, float g, const flo
         const int e = c0 + j;
         if (e < E) {
           const float z = FP4 ? v[j] * g : v[j];
-          const float av = sqrt_softplus_f32(z);
+          const float av = act_f32(act, z);
           const float key = bias ? av + __ldg(bias + e) : av;
           if (key >= thr)
-            t64.push(sqrt_softplus_f64((double)z) + (bias ? (double)__ldg(bias + e) : 0.0), e, av);
+            t64.push(act_f64(act, (double)z) + (bias ? (double)__ldg(bias + e) : 0.0), e, av);
         }
       }
     }
@@ -407,7 +407,7 @@ __device__ __noinline__ void refine_row(uint32_t trow, int E, float g, const flo
 // them. Out of line: FP64 is slow on this part and must not be issued on
 // the common path.
 template <int KC>
-__device__ __noinline__ void refine_fp64(const uint32_t* l_o, int32_t* l_i, float* l_z,
+__device__ __noinline__ void refine_fp64(int act, const uint32_t* l_o, int32_t* l_i, float* l_z,
                                          uint32_t need, bool amb, int qoff, int qtotal,
                                          const float* zq, const float* sb, const uint32_t* wl) {
   const int lane = threadIdx.x & 31;
@@ -419,7 +419,7 @@ __device__ __noinline__ void refine_fp64(const uint32_t* l_o, int32_t* l_i, floa
     if (base + lane < qtotal) {
       const uint32_t item = wl[base + lane];
       const int e = (int)(item >> 16);
-      key = key64(zq[e * BM + (int)((item >> 5) & 31u)], sb ? sb[e] : 0.0f);
+      key = key64(act, zq[e * BM + (int)((item >> 5) & 31u)], sb ? sb[e] : 0.0f);
     }
 #pragma unroll
     for (int j = 0; j < KC; ++j) {
@@ -460,7 +460,7 @@ __device__ __noinline__ void refine_fp64(const uint32_t* l_o, int32_t* l_i, floa
 // fetch: the loops stay rolled and work in shared memory (the row's list,
 // and the warp's spent candidate list wl for the pooled items).
 template <int KC>
-__device__ __noinline__ bool refine_in_list(const uint32_t* l_o, int32_t* l_i, float* l_z,
+__device__ __noinline__ bool refine_in_list(int act, const uint32_t* l_o, int32_t* l_i, float* l_z,
                                             bool close, float band, float thr, const float* zq,
                                             const float* sb, uint32_t* wl) {
   const int lane = threadIdx.x & 31;
@@ -517,7 +517,7 @@ __device__ __noinline__ bool refine_in_list(const uint32_t* l_o, int32_t* l_i, f
     for (int q = lane; q < qtotal; q += 32) {
       const uint32_t item = it_e[q];
       const int e = (int)(item >> 16);
-      const NearKey nk = near_key_ool(zq[e * BM + (int)((item >> 5) & 31u)], sb ? sb[e] : 0.0f);
+      const NearKey nk = near_key_ool(act, zq[e * BM + (int)((item >> 5) & 31u)], sb ? sb[e] : 0.0f);
       it_h[q] = nk.hi;
       it_l[q] = nk.lo;
       it_s[q] = nk.scale;
@@ -566,7 +566,7 @@ __device__ __noinline__ bool refine_in_list(const uint32_t* l_o, int32_t* l_i, f
           wl[q++] = ((uint32_t)l_i[j * BM] << 16) | ((uint32_t)lane << 5) | (uint32_t)j;
     }
     __syncwarp();
-    refine_fp64<KC>(l_o, l_i, l_z, need, amb, qoff, qtotal, zq, sb, wl);
+    refine_fp64<KC>(act, l_o, l_i, l_z, need, amb, qoff, qtotal, zq, sb, wl);
   }
   if (need != 0u && !amb) {
     // the sorted items' scores (from their original slots), then the refill
@@ -807,7 +807,10 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
     const int c_lo = half * E2, c_hi = half ? E : min(E, E2);
     const float g = FP4 ? a.w_global : 1.0f;
     const int k = a.k;
-    const bool sp = a.act == ACT_SQRT_SOFTPLUS;
+    // sp: a biased activation (sqrt-softplus or sigmoid) rather than softmax
+    const int act = a.act;
+    const bool sp = act != ACT_SOFTMAX;
+    const bool sig = act == ACT_SIGMOID;
     const bool has_bias = sp && a.bias != nullptr;
     // range of the selection-only bias (read before the accumulator is ready)
     float bmin = 0.0f, bmax = 0.0f;
@@ -958,15 +961,23 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
 #pragma unroll
       for (int q = 0; q < G; ++q) {
         float xq = gmax[q];
-        if (sp) xq = xq > -INFINITY ? __fadd_rd(__fsqrt_rd(fmaxf(xq, 0.0f)), s_gbmin[half][q])
-                                    : -INFINITY;
+        if (sp) {
+          // a lower bound of a(z_q): sqrt(max(z,0)) rounded down, or the FP32
+          // sigmoid lowered by 2^-20 (its error is at most 3 * 2^-23)
+          const float lb = sig ? sigmoid_f32(xq) * (1.0f - 0x1p-20f) : __fsqrt_rd(fmaxf(xq, 0.0f));
+          xq = xq > -INFINITY ? __fadd_rd(lb, s_gbmin[half][q]) : -INFINITY;
+        }
 #pragma unroll
         for (int j = KC - 2; j > 0; --j) srt[j] = fmaxf(srt[j], fminf(srt[j - 1], xq));
         srt[0] = fmaxf(srt[0], xq);
       }
-      // merge with the other half's list (through the idle exchange area;
-      // the second barrier keeps it from being reused before both have read)
-      float* lbx = reinterpret_cast<float*>(tiles);  // [2][KC - 1][BM]
+      // merge with the other half's list through the idle tile ring: past
+      // the list exchange area when it fits below the logits copy (nothing
+      // else writes there), else over it, with a second barrier so it is
+      // not reused before both halves have read
+      constexpr int kLbxOff = (3 * KC + 3) * BM * 4;
+      constexpr bool kSepLbx = kLbxOff + 2 * (KC - 1) * BM * 4 <= (int)kCandOffset;
+      float* lbx = reinterpret_cast<float*>(tiles + (kSepLbx ? kLbxOff : 0));  // [2][KC - 1][BM]
 #pragma unroll
       for (int j = 0; j < KC - 1; ++j) lbx[(half * (KC - 1) + j) * BM + row] = srt[j];
       asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
@@ -977,7 +988,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         for (int j = KC - 2; j > 0; --j) srt[j] = fmaxf(srt[j], fminf(srt[j - 1], xq));
         srt[0] = fmaxf(srt[0], xq);
       }
-      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+      if (!kSepLbx) asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
       float lz = INFINITY;
 #pragma unroll
       for (int j = 0; j < KC - 1; ++j)
@@ -997,7 +1008,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       } else if (!sp) {
         tz = lz;  // softmax: the key is the logit, exactly
       } else {
-        const float A = srt[0] - bmin + 0.84f;
+        const float A = sig ? 1.0f : srt[0] - bmin + 0.84f;
         const float babs = fmaxf(fabsf(bmin), fabsf(bmax));
         const float margin = 0x1p-16f * (4.0f * fabsf(A) + babs + 1.0f);
         const float y = (lz - margin - bmax) * (1.0f - 0x1p-18f);
@@ -1005,7 +1016,9 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
           tz = -INFINITY;
         } else {
           const float u = y * y;
-          const float t = u > 80.0f ? u : logf(expm1f(u));
+          // a^-1(y): sqrt-softplus log(expm1(y^2)), sigmoid log(y / (1 - y));
+          // L never exceeds the k-th key, so y < 1 for the sigmoid
+          const float t = sig ? logf(y / (1.0f - y)) : (u > 80.0f ? u : logf(expm1f(u)));
           tz = t - 0x1p-16f * (1.0f + fabsf(t));
         }
       }
@@ -1056,7 +1069,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         for (int t = lane; t < total; t += 32) {  // each item becomes its score
           const uint32_t item = wl[t];
           const int zi = (int)(item & 255u) * BM + quad * 32 + (int)(item >> 8);
-          wl[t] = __float_as_uint(sqrt_softplus_f32(zbuf[zi]));
+          wl[t] = __float_as_uint(act_f32(act, zbuf[zi]));
         }
         __syncwarp();
       }
@@ -1075,7 +1088,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
           cm[3] = (!n0 && !n1 && !n2) ? rest : cm[3];
           const int e = c_lo + base + __ffs(mw) - 1;
           float sc = zbuf[e * BM + row];  // the score: the logit, or its activation
-          if (sp) sc = shared_act ? __uint_as_float(wl[off + i]) : sqrt_softplus_f32(sc);
+          if (sp) sc = shared_act ? __uint_as_float(wl[off + i]) : act_f32(act, sc);
           float key = sc;
           if (sp) {
             key = has_bias ? sc + s_bias[e] : sc;
@@ -1108,7 +1121,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       bool close = false;
       float band = 0.0f;
       if (sp) {
-        band = 4.0f * key_err_bound(amax, kabs);
+        band = 4.0f * key_err_bound(amax, kabs, act_err_coef(act));
         const int kk = min(k + 1, E);
 #pragma unroll
         for (int j = 0; j + 1 < KC; ++j)
@@ -1135,7 +1148,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         }
         uint32_t* wl = reinterpret_cast<uint32_t*>(tiles + kCandOffset + (size_t)E * BM * 4) +
                        warp * kListCap;  // this warp's candidate list is spent
-        slow = refine_in_list<KC>(xo + row, xi + row, xz + row, close, band, thr,
+        slow = refine_in_list<KC>(act, xo + row, xi + row, xz + row, close, band, thr,
                                   zbuf + quad * 32, has_bias ? s_bias : nullptr, wl);
         if (close) {
 #pragma unroll
@@ -1146,7 +1159,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         }
       }
       if (__any_sync(kFull, slow)) {  // near ties reaching past the list: every column
-        refine_row<KC, FP4>(trow, E, g, a.bias, thr, slow, xi + row, xz + row);
+        refine_row<KC, FP4>(trow, E, g, a.bias, act, thr, slow, xi + row, xz + row);
         if (slow) {
 #pragma unroll
           for (int j = 0; j < KC; ++j) {
@@ -1174,7 +1187,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
             float la[KC], lm = -INFINITY;
 #pragma unroll
             for (int j = 0; j < KC; ++j) {
-              la[j] = j < k ? log_sqrt_softplus(zbuf[top.i[j] * BM + row]) : -INFINITY;
+              la[j] = j < k ? log_act(act, zbuf[top.i[j] * BM + row]) : -INFINITY;
               lm = fmaxf(lm, la[j]);
             }
             sum = 0.0f;
@@ -1185,13 +1198,32 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
             }
           }
         }
+        const float inv = 1.0f / (float)k;
 #pragma unroll
-        for (int j = 0; j < KC; ++j) {
-          if (j < k) {
-            a.out_idx[(size_t)m * k + j] = top.i[j];
-            a.out_w[(size_t)m * k + j] = sum > 0.0f ? sv[j] / sum : 1.0f / (float)k;
-            if (a.tbl_unique) s_sel[row * kMaxK + j] = top.i[j];
+        for (int j = 0; j < KC; ++j) sv[j] = sum > 0.0f ? sv[j] / sum : inv;
+        int32_t* oi = a.out_idx + (size_t)m * k;
+        float* ow = a.out_w + (size_t)m * k;
+        if ((k & 3) == 0 && ((reinterpret_cast<uintptr_t>(oi) | reinterpret_cast<uintptr_t>(ow)) & 15u) == 0) {
+#pragma unroll
+          for (int j = 0; j + 3 < KC; j += 4) {  // 16-byte stores
+            if (j < k) {
+              *reinterpret_cast<int4*>(oi + j) = make_int4(top.i[j], top.i[j + 1], top.i[j + 2], top.i[j + 3]);
+              *reinterpret_cast<float4*>(ow + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+            }
           }
+        } else {
+#pragma unroll
+          for (int j = 0; j < KC; ++j) {
+            if (j < k) {
+              oi[j] = top.i[j];
+              ow[j] = sv[j];
+            }
+          }
+        }
+        if (a.tbl_unique) {
+#pragma unroll
+          for (int j = 0; j < KC; ++j)
+            if (j < k) s_sel[row * kMaxK + j] = top.i[j];
         }
       }
       if (a.logits) {  // telemetry tap; the loads are warp-collective, the stores per row

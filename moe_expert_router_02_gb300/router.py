@@ -14,7 +14,7 @@ import threading
 from . import build as _build
 
 GBR_OK, GBR_EINVAL, GBR_EUNSUPPORTED, GBR_ECUDA, GBR_EWORKSPACE, GBR_ETIMEOUT = range(6)
-GBR_ACT_SOFTMAX, GBR_ACT_SQRT_SOFTPLUS = 0, 1
+GBR_ACT_SOFTMAX, GBR_ACT_SQRT_SOFTPLUS, GBR_ACT_SIGMOID = 0, 1, 2
 GBR_F32, GBR_BF16, GBR_NVFP4 = 0, 1, 2
 GBR_FLAG_NO_PDL, GBR_FLAG_FORCE_GENERIC, GBR_FLAG_FORCE_GEMV, GBR_FLAG_FORCE_TC, \
     GBR_FLAG_UNFUSED, GBR_FLAG_NO_SINGLE_CLUSTER = 1, 2, 4, 8, 16, 32
@@ -62,7 +62,7 @@ def lib() -> ctypes.CDLL:
             L.router_select.argtypes = [P, P, I, I, I, I, P, P, P]
             L.route_table.argtypes = [P, I, I, I, P, P, P, P, P]
             L.router_forward_noalloc.argtypes = [P, P, P, I, I, I, I, I, P, P, P]
-            L.router_near_tie_keys.argtypes = [P, P, I, P, P, P]
+            L.router_near_tie_keys.argtypes = [P, P, I, I, P, P, P]
             L.router_strerror.argtypes = [I]
             L.router_strerror.restype = ctypes.c_char_p
             L.router_device_status.argtypes = [I]
@@ -147,8 +147,8 @@ def router_select(logits, bias, M, E, k, act, out_idx, out_w, stream=None):
                                _ptr(out_w), _stream(stream)), "router_select")
 
 
-def router_near_tie_keys(z, bias, n, key_hi, key_lo, stream=None):
-    _check(lib().router_near_tie_keys(_ptr(z), _ptr(bias), n, _ptr(key_hi), _ptr(key_lo),
+def router_near_tie_keys(z, bias, n, key_hi, key_lo, act=GBR_ACT_SQRT_SOFTPLUS, stream=None):
+    _check(lib().router_near_tie_keys(_ptr(z), _ptr(bias), n, act, _ptr(key_hi), _ptr(key_lo),
                                       _stream(stream)), "router_near_tie_keys")
 
 

@@ -29,7 +29,7 @@ from __future__ import annotations
 import numpy as np
 
 F32, BF16, NVFP4 = 0, 1, 2
-SOFTMAX, SQRT_SOFTPLUS = 0, 1
+SOFTMAX, SQRT_SOFTPLUS, SIGMOID = 0, 1, 2
 
 
 def rng(seed: int) -> np.random.Generator:

@@ -46,6 +46,7 @@ def lib():
             L.orc_e2m1.argtypes, L.orc_e2m1.restype = [I], D
             L.orc_e4m3.argtypes, L.orc_e4m3.restype = [I], D
             L.orc_sqrt_softplus.argtypes, L.orc_sqrt_softplus.restype = [D], D
+            L.orc_sigmoid.argtypes, L.orc_sigmoid.restype = [D], D
             L.orc_logits.argtypes = [P, I, P, I, P, D, I, I, I, P]
             L.orc_select.argtypes = [P, P, I, I, I, I, I, P, P, P]
             L.orc_select_by_prob.argtypes = [P, I, I, I, P]
@@ -70,6 +71,10 @@ def e4m3(code: int) -> float:
 
 def sqrt_softplus(z: float) -> float:
     return lib().orc_sqrt_softplus(float(z))
+
+
+def sigmoid(z: float) -> float:
+    return lib().orc_sigmoid(float(z))
 
 
 def logits(x, x_dtype, W, w_dtype, M, H, E, scales=None, g=1.0) -> np.ndarray:

@@ -16,7 +16,9 @@
 //   * scores           softmax over all E; or a = sqrt(softplus(l)) with the
 //       stable softplus max(l,0) + log1p(exp(-|l|)) and key = a + bias
 //       (commit page, "Numerically stable softplus"; the bias only selects,
-//       the heap keeps "(score, index, unbiased act)").
+//       the heap keeps "(score, index, unbiased act)"); or a = sigmoid(l) =
+//       1 / (1 + exp(-l)) with key = a + bias in the same way (the same
+//       biased-score contract with the sigmoid as the score).
 //   * top-k            full stable sort of all E experts by (key desc, index
 //       asc): equal keys keep the lower expert index first
 //       (qwisp issue #145, "Bit-exactness": the tie-break order is part of
@@ -42,7 +44,7 @@
 namespace {
 
 constexpr int kF32 = 0, kBF16 = 1, kNVFP4 = 2;
-constexpr int kSoftmax = 0, kSqrtSoftplus = 1;
+constexpr int kSoftmax = 0, kSqrtSoftplus = 1, kSigmoid = 2;
 
 double from_bf16(uint16_t b) {
   uint32_t u = static_cast<uint32_t>(b) << 16;
@@ -73,6 +75,8 @@ double sqrt_softplus(double z) {
   return std::sqrt(sp);
 }
 
+double sigmoid(double z) { return 1.0 / (1.0 + std::exp(-z)); }
+
 }  // namespace
 
 extern "C" {
@@ -80,6 +84,7 @@ extern "C" {
 double orc_e2m1(int code) { return e2m1(code); }
 double orc_e4m3(int code) { return e4m3(code); }
 double orc_sqrt_softplus(double z) { return sqrt_softplus(z); }
+double orc_sigmoid(double z) { return sigmoid(z); }
 
 // Element h of row r of an [R, H] matrix of the given dtype, widened to FP64.
 // NVFP4 rows: packed bytes [R, H/2], scales [R, H/16]; the global scale is
@@ -121,7 +126,7 @@ int orc_logits(const void* x, int x_dtype, const void* W, int w_dtype,
 //   first kk = min(k+1, E) keys in sorted order (for the gap rule).
 int orc_select(const double* logits, const float* bias, int bias_per_row, int M, int E,
                int k, int act, int32_t* out_idx, double* out_w, double* out_keys) {
-  if (k < 1 || k > E || (act != kSoftmax && act != kSqrtSoftplus)) return -1;
+  if (k < 1 || k > E || (act != kSoftmax && act != kSqrtSoftplus && act != kSigmoid)) return -1;
   if (act == kSoftmax && bias) return -1;
   const int kk = std::min(k + 1, E);
   std::vector<double> key(E), score(E);
@@ -140,7 +145,7 @@ int orc_select(const double* logits, const float* bias, int bias_per_row, int M,
       }
     } else {
       for (int e = 0; e < E; ++e) {
-        score[e] = sqrt_softplus(l[e]);
+        score[e] = act == kSigmoid ? sigmoid(l[e]) : sqrt_softplus(l[e]);
         key[e] = score[e] + (b ? static_cast<double>(b[e]) : 0.0);
       }
     }

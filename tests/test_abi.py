@@ -45,7 +45,7 @@ def test_empty_calls_return_ok_without_launch():
 @pytest.mark.parametrize("args,expect", [
     ((1, 64, 16, 0, 0), R.GBR_EINVAL),      # k < 1
     ((1, 64, 16, 17, 0), R.GBR_EINVAL),     # k > E
-    ((1, 64, 16, 2, 2), R.GBR_EINVAL),      # bad act
+    ((1, 64, 16, 2, 3), R.GBR_EINVAL),      # bad act
     ((-1, 64, 16, 2, 0), R.GBR_EINVAL),     # M < 0
     ((1, 0, 16, 2, 0), R.GBR_EINVAL),       # H < 1
     ((1, 64, 1024, 2, 0), R.GBR_EUNSUPPORTED),  # E > 512

@@ -28,25 +28,27 @@ B_I, B_J = np.float32(0.0125), np.float32(-0.0375)
 GAPS = (1e-7, -1e-7, 1e-9, -1e-9, 3e-11, -3e-11, 1e-12, -1e-12, 2e-13, -2e-13)
 
 
-def near_keys(z, b):
+def near_keys(z, b, act=synth.SQRT_SOFTPLUS):
     import torch
     n = len(z)
     hi = torch.empty(n, dtype=torch.float32, device="cuda")
     lo = torch.empty(n, dtype=torch.float32, device="cuda")
-    R.router_near_tie_keys(dev(z), None if b is None else dev(b), n, hi, lo)
+    R.router_near_tie_keys(dev(z), None if b is None else dev(b), n, hi, lo, act=act)
     torch.cuda.synchronize()
     return hi.cpu().numpy(), lo.cpu().numpy()
 
 
-def test_near_tie_key_error_against_fp64():
+@pytest.mark.parametrize("act", [synth.SQRT_SOFTPLUS, synth.SIGMOID])
+def test_near_tie_key_error_against_fp64(act):
     gen = synth.rng(5)
     z = np.concatenate([gen.uniform(-30, 30, 6000), synth.normal(gen, 6000, 2.0),
                         np.array([0.0, -0.0, 1e-30, -1e-30, 1e-8, -1e-8, 30.0, -30.0,
                                   30.5, -30.5, 45.0, -45.0, 80.0, -80.0])]).astype(np.float32)
     b = np.where(np.arange(len(z)) % 3 == 0, 0.0, gen.uniform(-0.05, 0.05, len(z)))
     b = b.astype(np.float32)
-    hi, lo = near_keys(z, b)
-    s = np.array([oracle.sqrt_softplus(float(v)) for v in z])
+    hi, lo = near_keys(z, b, act)
+    f = oracle.sigmoid if act == synth.SIGMOID else oracle.sqrt_softplus
+    s = np.array([f(float(v)) for v in z])
     ref = s + b.astype(np.float64)
     got = hi.astype(np.float64) + lo.astype(np.float64)
     err = np.abs(got - ref) / (s + np.abs(ref))
@@ -186,7 +188,7 @@ def test_fused_cross_input_near_ties(M, flags, regimes):
 
 
 @pytest.mark.parametrize("act,with_bias", [(synth.SQRT_SOFTPLUS, True), (synth.SQRT_SOFTPLUS, False),
-                                           (synth.SOFTMAX, False)])
+                                           (synth.SOFTMAX, False), (synth.SIGMOID, True)])
 def test_prefill_extreme_logits(act, with_bias):
     """Logits far outside the usual range reach the prefill kernel exactly:
     its candidate threshold must hold where expm1f(y^2) overflows (large
@@ -224,8 +226,9 @@ def test_prefill_extreme_logits(act, with_bias):
     assert R.router_device_status(clear=True) == R.GBR_OK
 
 
+@pytest.mark.parametrize("act", [synth.SQRT_SOFTPLUS, synth.SIGMOID])
 @pytest.mark.parametrize("lo,hi", [(-201.0, -200.0), (-110.0, -95.0)])
-def test_select_underflowing_activations(lo, hi):
+def test_select_underflowing_activations(lo, hi, act):
     """Rows whose chosen sqrt-softplus activations are all below FP32's
     range: the weights are ratios of exp(z/2) and come from the log domain
     (to 2e-5 of the oracle's FP64 weights)."""
@@ -235,9 +238,8 @@ def test_select_underflowing_activations(lo, hi):
     Z = gen.uniform(lo, hi, (M, E)).astype(np.float32)
     for bias in (None, synth.make_bias(E, 3)):
         idx, w = empty_outputs(M, K)
-        R.router_select(dev(Z), None if bias is None else dev(bias), M, E, K, synth.SQRT_SOFTPLUS,
-                        idx, w)
+        R.router_select(dev(Z), None if bias is None else dev(bias), M, E, K, act, idx, w)
         torch.cuda.synchronize()
-        oi, ow, _ = oracle.select(Z.astype(np.float64), K, synth.SQRT_SOFTPLUS, bias=bias)
+        oi, ow, _ = oracle.select(Z.astype(np.float64), K, act, bias=bias)
         assert np.array_equal(idx.cpu().numpy(), oi)
         assert np.max(np.abs(w.cpu().numpy() - ow)) <= W_TOL

@@ -110,6 +110,44 @@ def test_sqrt_softplus_strictly_increasing():
     assert np.all(np.diff(a) > 0)
 
 
+def _dec_sigmoid(z):
+    """sigmoid(z) = 1 / (1 + e^-z) in 60-digit decimal."""
+    with decimal.localcontext() as c:
+        c.prec = 60 + int(abs(z) / 2.3)
+        return 1 / (1 + (-decimal.Decimal(float(z))).exp())
+
+
+@pytest.mark.parametrize("z", [0.0, 1e-8, -1e-8, 0.5, -0.5, 1.0, -1.0, 2.5, -3.0, 10.0,
+                               -10.0, 30.0, -30.0, 80.0, -80.0, 300.0, -300.0])
+def test_sigmoid_matches_60_digit_decimal(z):
+    ref = float(_dec_sigmoid(z))
+    assert oracle.sigmoid(z) == pytest.approx(ref, rel=4e-16, abs=0)
+
+
+def test_sigmoid_closed_forms_and_symmetry():
+    assert oracle.sigmoid(0.0) == 0.5
+    assert oracle.sigmoid(800.0) == 1.0 and oracle.sigmoid(-800.0) == 0.0
+    assert oracle.sigmoid(-60.0) == pytest.approx(math.exp(-60.0), rel=1e-15)
+    for z in np.linspace(-20, 20, 401):
+        assert oracle.sigmoid(z) + oracle.sigmoid(-z) == pytest.approx(1.0, abs=5e-16)
+    zs = np.linspace(-30, 30, 20001)
+    a = np.array([oracle.sigmoid(z) for z in zs])
+    assert np.all(np.diff(a) > 0)
+
+
+def test_constructed_sigmoid_bias_rows_against_decimal_brute_force():
+    E, k = 12, 3
+    rows, bias, kinds = synth.tie_rows_sqrt_softplus(30, E, k, seed=7, std=0.4)
+    idx, w, _ = oracle.select(rows.astype(np.float64), k, synth.SIGMOID, bias=bias)
+    for r in range(len(rows)):
+        a = [_dec_sigmoid(float(z)) for z in rows[r]]
+        keys = [a[e] + decimal.Decimal(float(bias[r, e])) for e in range(E)]
+        assert list(idx[r]) == _brute_topk(keys, k), kinds[r]
+        tot = sum(a[e] for e in idx[r])
+        for j, e in enumerate(idx[r]):
+            assert w[r, j] == pytest.approx(float(a[e] / tot), rel=1e-14)
+
+
 # ---------------------------------------------------------------- selection
 @pytest.mark.parametrize("E,k", [(4, 1), (5, 2), (6, 3), (7, 2), (7, 3)])
 def test_topk_matches_brute_force_with_ties(E, k):
@@ -191,7 +229,8 @@ def test_renormalisation_invariants():
     gen = synth.rng(9)
     lg = gen.normal(size=(300, 256)) * 0.9
     for act, bias in ((synth.SOFTMAX, None),
-                      (synth.SQRT_SOFTPLUS, synth.make_bias(256, 1))):
+                      (synth.SQRT_SOFTPLUS, synth.make_bias(256, 1)),
+                      (synth.SIGMOID, synth.make_bias(256, 2))):
         idx, w, keys = oracle.select(lg, 8, act, bias=bias)
         np.testing.assert_allclose(w.sum(axis=1), 1.0, atol=1e-12)
         assert all(len(set(r)) == 8 for r in idx)
