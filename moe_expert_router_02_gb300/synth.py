@@ -277,6 +277,19 @@ def table_pairs(G: int, k: int, E: int, seed: int) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- workloads
+def gather_inputs(G: int, k: int, D: int, seed: int, T: int = 2):
+    """Inputs of the table's consumer for G groups of T tokens: expert output
+    rows y BF16 bits [G, T*k, T, D] ~ N(0, 1), router weights w FP32
+    [G, T, k] (positive, each token's summing to 1), shared expert output
+    BF16 bits [G, T, D] ~ N(0, 1)."""
+    gen = rng(seed)
+    y = f32_to_bf16_bits(normal(gen, (G, T * k, T, D), 1.0))
+    w = gen.uniform(0.05, 1.0, size=(G, T, k))
+    w = (w / w.sum(axis=2, keepdims=True)).astype(np.float32)
+    shared = f32_to_bf16_bits(normal(gen, (G, T, D), 1.0))
+    return y, w, shared
+
+
 CONFIGS = {
     # tiny correctness case: FP32 x and W, softmax, top-2
     "C0": dict(M=4, H=256, E=16, k=2, act=SOFTMAX, x_dtype=F32, w_dtype=F32,

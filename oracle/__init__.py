@@ -51,7 +51,9 @@ def lib():
             L.orc_select.argtypes = [P, P, I, I, I, I, I, P, P, P]
             L.orc_select_by_prob.argtypes = [P, I, I, I, P]
             L.orc_route_table.argtypes = [P, I, I, I, P, P, P, P]
-            for f in (L.orc_logits, L.orc_select, L.orc_select_by_prob, L.orc_route_table):
+            L.orc_gather_add.argtypes = [P, P, P, P, I, I, I, I, P]
+            for f in (L.orc_logits, L.orc_select, L.orc_select_by_prob, L.orc_route_table,
+                      L.orc_gather_add):
                 f.restype = I
             _lib = L
     return _lib
@@ -136,6 +138,24 @@ def route_table(idx):
     if lib().orc_route_table(_p(idx), G, T, k, _p(unique), _p(mask), _p(mp), _p(count)) != 0:
         raise ValueError("oracle: bad route_table arguments")
     return unique, mask, mp, count
+
+
+def gather_add(y, mp, w, shared):
+    """The table's consumer: ``y`` BF16 bits ``[G, T*k, T, D]`` (row (u, t) =
+    unique expert u's output for token t), ``mp`` uint8 ``[G, T, k]``, ``w``
+    FP32 ``[G, T, k]``, ``shared`` BF16 bits ``[G, T, D]``. Returns the BF16
+    bits ``[G, T, D]`` of bf16(bf16(FP32 fma sum in slot order) + shared)."""
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    mp = np.ascontiguousarray(mp, dtype=np.uint8)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    shared = np.ascontiguousarray(shared, dtype=np.uint16)
+    G, T, k = mp.shape
+    D = shared.shape[-1]
+    assert y.shape == (G, T * k, T, D) and w.shape == (G, T, k) and shared.shape == (G, T, D)
+    out = np.empty((G, T, D), dtype=np.uint16)
+    if lib().orc_gather_add(_p(y), _p(mp), _p(w), _p(shared), G, T, k, D, _p(out)) != 0:
+        raise ValueError("oracle: bad gather_add arguments")
+    return out
 
 
 def router(case: dict):

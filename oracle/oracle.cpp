@@ -25,6 +25,9 @@
 //       the contract).
 //   * renormalise      w_j = s_j / sum_{i<k} s_i over the chosen k
 //       (commit page, "top-k + renorm").
+//   * gather + shared add (the table's consumer): FP32 fma accumulation of
+//       the routed rows in slot order -> BF16 -> + shared BF16 -> BF16
+//       (b70 lab note, "Exact arithmetic").
 //   * route table      serial walk over (token, slot) in row-major order;
 //       first sight of an expert appends it to the unique list
 //       (b70 lab note, "Unique-route router screen": encounter-ordered
@@ -215,6 +218,59 @@ int orc_route_table(const int32_t* idx, int G, int T, int k, int32_t* unique,
     for (int u = 0; u < n; ++u) {
       unique[(size_t)g * n + u] = u < (int)uq.size() ? uq[u] : -1;
       mask[(size_t)g * n + u] = u < (int)uq.size() ? mk[u] : 0;
+    }
+  }
+  return 0;
+}
+
+
+// Consumer side of the unique-route table (b70 lab note, "MTP1 M=2
+// gather/shared-add gate", "Exact arithmetic": FP32 routed accumulation ->
+// BF16 -> add shared BF16 -> BF16; "Real route-direct result": one expert
+// output row per unique (token, expert) route, reused by duplicate slots).
+//   y      BF16 [G, T*k, T, D]  row (u, t): unique expert u's output for token t
+//   map    [G, T, k]            unique position of slot s of token t (route_table)
+//   w      FP32 [G, T, k]       the router's weights
+//   shared BF16 [G, T, D]       the shared expert's output
+//   out    BF16 [G, T, D]
+// For each (g, t, d): acc = 0; for s = 0..k-1 in slot order,
+// acc = fma(w[t][s], y[map[t][s]][t][d], acc) in FP32 (one rounding each);
+// then out = bf16(float(bf16(acc)) + float(shared)), the add in FP32 and
+// both conversions round-to-nearest-even.
+static uint16_t to_bf16(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40u);  // quiet NaN
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+static float bf16_value(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+int orc_gather_add(const uint16_t* y, const uint8_t* map, const float* w, const uint16_t* shared,
+                   int G, int T, int k, int D, uint16_t* out) {
+  if (G < 0 || T < 1 || T > 8 || k < 1 || D < 1) return -1;
+  const int n = T * k;
+  for (int g = 0; g < G; ++g) {
+    for (int t = 0; t < T; ++t) {
+      const uint8_t* mp = map + ((size_t)g * T + t) * k;
+      const float* wt = w + ((size_t)g * T + t) * k;
+      for (int s = 0; s < k; ++s)
+        if (mp[s] >= n) return -1;
+      for (int d = 0; d < D; ++d) {
+        float acc = 0.0f;
+        for (int s = 0; s < k; ++s) {
+          const size_t row = ((size_t)g * n + mp[s]) * T + t;
+          acc = std::fmaf(wt[s], bf16_value(y[row * D + d]), acc);
+        }
+        const float sum = bf16_value(to_bf16(acc)) + bf16_value(shared[((size_t)g * T + t) * D + d]);
+        out[((size_t)g * T + t) * D + d] = to_bf16(sum);
+      }
     }
   }
   return 0;

@@ -380,3 +380,94 @@ def test_router_tiny_case_consistency():
     np.testing.assert_allclose(out["logits"], x @ W.T, rtol=1e-12, atol=1e-12)
     for r in range(case["M"]):
         assert list(out["idx"][r]) == _brute_topk(list(out["logits"][r]), case["k"])
+
+
+# ---------------------------------------------------------------- table consumer
+def _bits(v):
+    return synth.f32_to_bf16_bits(np.asarray(v, dtype=np.float32))
+
+
+def _val(b):
+    return synth.bf16_bits_to_f32(np.asarray(b, dtype=np.uint16))
+
+
+def test_gather_add_exact_integer_case_through_the_table():
+    """Integer expert outputs, weights 1 or 2 and integer shared outputs keep
+    every step exact, so the result must be the integer sum over the routes
+    read through idx directly; a wrong map (token and slot swapped, the wrong
+    unique row) changes it."""
+    G, k, D, E = 60, 6, 32, 256
+    gen = synth.rng(3)
+    idx = synth.table_pairs(G, k, E, seed=4)
+    unique, mask, mp, count = oracle.route_table(idx)
+    Y = gen.integers(-8, 9, size=(G, E, 2, D)).astype(np.float32)  # every expert's output
+    y = np.full((G, 2 * k, 2, D), np.nan, dtype=np.float32)          # unused rows: NaN
+    for g in range(G):
+        for u in range(count[g]):
+            for t in range(2):
+                if mask[g, u] >> t & 1:
+                    y[g, u, t] = Y[g, unique[g, u], t]
+    w = gen.choice([1.0, 2.0], size=(G, 2, k)).astype(np.float32)
+    sh = gen.integers(-8, 9, size=(G, 2, D)).astype(np.float32)
+    out = _val(oracle.gather_add(_bits(y), mp, w, _bits(sh)))
+    want = np.zeros((G, 2, D))
+    for g in range(G):
+        for t in range(2):
+            for s in range(k):
+                want[g, t] += w[g, t, s] * Y[g, idx[g, t, s], t]
+    np.testing.assert_array_equal(out, want + sh)
+
+
+def test_gather_add_rounding_chain_and_fma():
+    """Hand-worked values. Routed sum 1 + 2^-8 is a BF16 halfway case and
+    rounds to 1.0 (even) before the shared 2^-9 is added, so the chain gives
+    1.0 where one rounding of the whole sum would give 1 + 2^-7. Slots
+    -(1 + 2^-23) and (1 + 2^-23) times 1 + 2^-7 leave 2^-30 with FMA
+    accumulation (a separate multiply would round it away to 0)."""
+    y = np.zeros((1, 4, 2, 2), dtype=np.float32)
+    y[0, 0, 0, 0] = 1.0
+    y[0, 1, 0, 0] = 1.0
+    y[0, 0, 0, 1] = 1.0 + 2.0 ** -7
+    y[0, 1, 0, 1] = 1.0 + 2.0 ** -7
+    mp = np.array([[[0, 1], [2, 3]]], dtype=np.uint8)
+    w = np.zeros((1, 2, 2), dtype=np.float32)
+    sh = np.zeros((1, 2, 2), dtype=np.float32)
+    # column 0: weights 1 and 2^-8, shared 2^-9
+    # column 1 uses the same weights, so give column 1 its own case via token 1 below
+    w[0, 0] = [1.0, 2.0 ** -8]
+    sh[0, 0, 0] = 2.0 ** -9
+    out = _val(oracle.gather_add(_bits(y), mp, w, _bits(sh)))
+    assert out[0, 0, 0] == 1.0
+    # token 1: rows 2 and 3 hold 1 + 2^-7; weights -(1 + 2^-23), 1 + 2^-23
+    y[0, 2, 1, 0] = 1.0 + 2.0 ** -7
+    y[0, 3, 1, 0] = 1.0 + 2.0 ** -7
+    w[0, 1] = [-(1.0 + 2.0 ** -23), 1.0 + 2.0 ** -23]
+    out = _val(oracle.gather_add(_bits(y), mp, w, _bits(sh)))
+    assert out[0, 1, 0] == 2.0 ** -30
+
+
+def test_gather_add_within_rounding_of_exact_and_row_permutation():
+    G, k, D = 40, 6, 64
+    y, w, sh = synth.gather_inputs(G, k, D, seed=8)
+    idx = synth.table_pairs(G, k, 256, seed=9)
+    unique, mask, mp, count = oracle.route_table(idx)
+    out = _val(oracle.gather_add(y, mp, w, sh)).astype(np.float64)
+    yv = _val(y).astype(np.float64)
+    exact = np.zeros((G, 2, D))
+    mag = np.zeros((G, 2, D))
+    for g in range(G):
+        for t in range(2):
+            for s in range(k):
+                r = yv[g, mp[g, t, s], t]
+                exact[g, t] += w[g, t, s] * r
+                mag[g, t] += abs(w[g, t, s] * r)
+    exact += _val(sh)
+    # BF16 rounding twice (2^-9 relative each) plus FP32 accumulation error
+    bound = 2.0 ** -8 * (np.abs(exact) + mag) + 2.0 ** -20 * mag + 1e-30
+    assert np.all(np.abs(out - exact) <= bound)
+    # relabelling the unique rows consistently leaves the result unchanged
+    perm = synth.rng(10).permutation(2 * k)
+    inv = np.argsort(perm)
+    y2 = y[:, perm]
+    mp2 = inv[mp].astype(np.uint8)
+    np.testing.assert_array_equal(oracle.gather_add(y2, mp2, w, sh), oracle.gather_add(y, mp, w, sh))
