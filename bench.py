@@ -440,6 +440,26 @@ def run_detail(args, peaks):
     tbytes = G * (2 * k * 4 + 2 * k * 4 + 2 * k + 2 * k + 4)
     out["C4_table_only_1e5"] = {"us": ms * 1e3, "hbm_frac": tbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
                                 "algo_bytes": tbytes}
+    # the table's consumer: routed gather + shared-expert add over 10^3 groups
+    # (M=2, k=6, D=4096 BF16 rows; 131 MB of rows, more than L2)
+    Gg, kg, Dg = 1000, C["C4"]["k"], C["C4"]["H"]
+    yg, wg, sg = synth.gather_inputs(Gg, kg, Dg, seed=0)
+    tg = (torch.empty((Gg, 2 * kg), dtype=torch.int32, device="cuda"),
+          torch.empty((Gg, 2 * kg), dtype=torch.uint8, device="cuda"),
+          torch.empty((Gg, 2, kg), dtype=torch.uint8, device="cuda"),
+          torch.empty((Gg,), dtype=torch.int32, device="cuda"))
+    R.route_table(dev(synth.table_pairs(Gg, kg, 256, seed=1)), Gg, 2, kg, *tg)
+    md = tg[2]
+    mpg = md.cpu().numpy()
+    yd, wd_, sd = dev(yg.view(np.int16)), dev(wg), dev(sg.view(np.int16))
+    od = torch.empty((Gg, 2, Dg), dtype=torch.int16, device="cuda")
+    ms = time_graph(lambda: R.route_gather_add(yd, md, wd_, sd, Gg, 2, kg, Dg, od), 20)
+    rows_read = int(sum(len(set(mpg[g, t])) for g in range(Gg) for t in range(2)))
+    gbytes = rows_read * Dg * 2 + 2 * (Gg * 2 * Dg * 2) + Gg * 2 * kg * 5
+    out["C4_gather_add_1e3"] = {"us": ms * 1e3, "hbm_frac": gbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
+                                "algo_bytes": gbytes}
+    del yd, od
+    torch.cuda.empty_cache()
     # prefill
     cfg3 = C["C3"]
     flops = 2 * cfg3["M"] * cfg3["H"] * cfg3["E"]

@@ -210,6 +210,32 @@ int router_forward_noalloc(const void* x, const void* W_gate, const float* bias,
                            int E, int k, int act, int32_t* out_idx, float* out_w,
                            cudaStream_t stream);
 
+/*
+ * route_gather_add — the table's consumer (b70 lab note "MTP1 M=2
+ * gather/shared-add gate": "Exact arithmetic", "Real route-direct result").
+ * The experts ran once per unique (token, expert) route of each group; this
+ * combines their rows. For group g, token t < T = tokens_per_group and
+ * element d < D:
+ *   acc = 0; for s = 0..k-1: acc = fma(w[g][t][s], y[g][map[g][t][s]][t][d], acc)
+ *   out[g][t][d] = bf16(float(bf16(acc)) + float(shared[g][t][d]))
+ * FP32 fma accumulation in slot order, FP32 add, round-to-nearest-even to
+ * BF16 at both steps. Layouts (dense, row-major, device):
+ *   y      BF16 [groups, T*k, T, D]  row (u, t): unique expert u's output
+ *                                     for token t (rows no slot maps to are
+ *                                     not read)
+ *   map    uint8 [groups, T, k]      as route_table's out_map
+ *   w      FP32 [groups, T, k]       the router's weights
+ *   shared BF16 [groups, T, D]       the shared expert's output
+ *   out    BF16 [groups, T, D]
+ * A map entry >= T*k contributes nothing. 16-byte aligned y, shared and out
+ * with D % 8 == 0 take the vector path. Errors: GBR_EINVAL for groups < 0,
+ * T outside 1..8, k outside 1..16, D < 1, null pointers (groups == 0: no
+ * launch).
+ */
+int route_gather_add(const void* y, const uint8_t* map, const float* w, const void* shared,
+                     int groups, int tokens_per_group, int k, int D, void* out,
+                     cudaStream_t stream);
+
 /* Static text for a status code. */
 const char* router_strerror(int status);
 

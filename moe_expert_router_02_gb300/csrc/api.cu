@@ -255,6 +255,20 @@ int router_near_tie_keys(const float* z, const float* bias, int n, int act, floa
              : GBR_ECUDA;
 }
 
+int route_gather_add(const void* y, const uint8_t* map, const float* w, const void* shared,
+                     int groups, int tokens_per_group, int k, int D, void* out,
+                     cudaStream_t stream) {
+  if (groups < 0 || tokens_per_group < 1 || tokens_per_group > 8 || k < 1 || k > gbr::kMaxK ||
+      D < 1)
+    return GBR_EINVAL;
+  if (groups == 0) return GBR_OK;
+  if (!y || !map || !w || !shared || !out) return GBR_EINVAL;
+  return gbr::launch_gather_add(y, map, w, shared, groups, tokens_per_group, k, D, out, stream) ==
+                 cudaSuccess
+             ? GBR_OK
+             : GBR_ECUDA;
+}
+
 int route_table(const int32_t* idx, int groups, int tokens_per_group, int k, int32_t* out_unique,
                 uint8_t* out_mask, uint8_t* out_map, int32_t* out_count, cudaStream_t stream) {
   if (groups < 0 || tokens_per_group < 1 || tokens_per_group > 8 || k < 1 || k > gbr::kMaxK)

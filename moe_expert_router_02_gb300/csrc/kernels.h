@@ -14,6 +14,11 @@ cudaError_t launch_select(const float* logits, const float* bias, int M, int E, 
 cudaError_t launch_near_tie_keys(const float* z, const float* bias, int n, int act, float* hi,
                                  float* lo, cudaStream_t stream);
 
+// The table's consumer: routed gather + shared-expert add (BF16 rows).
+cudaError_t launch_gather_add(const void* y, const uint8_t* map, const float* w,
+                              const void* shared, int G, int T, int k, int D, void* out,
+                              cudaStream_t stream);
+
 cudaError_t launch_route_table(const int32_t* idx, int groups, int T, int k, int32_t* unique,
                                uint8_t* mask, uint8_t* map, int32_t* count, cudaStream_t stream);
 

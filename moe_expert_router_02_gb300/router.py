@@ -23,7 +23,7 @@ GBR_REGIME_GENERIC, GBR_REGIME_GEMV, GBR_REGIME_TC, GBR_REGIME_UNFUSED, GBR_REGI
 
 EXPORTS = ("router_forward", "router_forward_ex", "router_workspace_size", "router_regime",
            "router_select", "route_table", "router_strerror", "router_device_status",
-           "router_forward_noalloc", "router_near_tie_keys")
+           "router_forward_noalloc", "router_near_tie_keys", "route_gather_add")
 
 
 class RouterError(RuntimeError):
@@ -63,12 +63,13 @@ def lib() -> ctypes.CDLL:
             L.route_table.argtypes = [P, I, I, I, P, P, P, P, P]
             L.router_forward_noalloc.argtypes = [P, P, P, I, I, I, I, I, P, P, P]
             L.router_near_tie_keys.argtypes = [P, P, I, I, P, P, P]
+            L.route_gather_add.argtypes = [P, P, P, P, I, I, I, I, P, P]
             L.router_strerror.argtypes = [I]
             L.router_strerror.restype = ctypes.c_char_p
             L.router_device_status.argtypes = [I]
             for f in (L.router_forward, L.router_forward_ex, L.router_regime, L.router_select,
                       L.route_table, L.router_device_status, L.router_forward_noalloc,
-                      L.router_near_tie_keys):
+                      L.router_near_tie_keys, L.route_gather_add):
                 f.restype = I
             _lib = L
     return _lib
@@ -157,6 +158,12 @@ def route_table(idx, groups, tokens_per_group, k, out_unique, out_mask, out_map,
     _check(lib().route_table(_ptr(idx), groups, tokens_per_group, k, _ptr(out_unique),
                              _ptr(out_mask), _ptr(out_map), _ptr(out_count), _stream(stream)),
            "route_table")
+
+
+def route_gather_add(y, mp, w, shared, groups, tokens_per_group, k, D, out, stream=None):
+    _check(lib().route_gather_add(_ptr(y), _ptr(mp), _ptr(w), _ptr(shared), groups,
+                                  tokens_per_group, k, D, _ptr(out), _stream(stream)),
+           "route_gather_add")
 
 
 def router_device_status(clear: bool = False) -> int:
