@@ -65,8 +65,9 @@ size_t workspace_for(const Shape& s, int regime) {
   // workspace sized on one device also fits a device where it is not chosen.
   if (regime == GBR_REGIME_GEMV || regime == GBR_REGIME_GEMV1C || regime == GBR_REGIME_UNFUSED)
     return kTicketBytes + round_up((size_t)s.M * s.E * 4, 256);
-  // the prefill kernel decodes NVFP4 W once per launch into the workspace
-  if (regime == GBR_REGIME_TC) return gbr::tc_workspace(s.H, s.E, s.w_dtype);
+  // the prefill kernel keeps stream-K partial sums and the NVFP4 W it
+  // decodes once per launch in the workspace
+  if (regime == GBR_REGIME_TC) return gbr::tc_workspace(s.M, s.H, s.E, s.w_dtype);
   return 0;
 }
 
@@ -140,6 +141,24 @@ int router_regime(int M, int H, int E, int k, const gbr_opts* opt) {
   const Shape s = make_shape(M, H, E, k, GBR_ACT_SOFTMAX, nullptr, opt);
   if (check_shape(s) != GBR_OK) return -1;
   return regime_of(s);
+}
+
+int router_tc_groups(int M, int H, int E, int k, const gbr_opts* opt) {
+  const Shape s = make_shape(M, H, E, k, GBR_ACT_SOFTMAX, nullptr, opt);
+  if (check_shape(s) != GBR_OK) return -1;
+  if (regime_of(s) != GBR_REGIME_TC) return 0;
+  gbr::RouterArgs a{};
+  a.M = M, a.H = H, a.E = E, a.k = k, a.act = GBR_ACT_SOFTMAX;
+  a.x_dtype = s.x_dtype, a.w_dtype = s.w_dtype;
+  // the launch gets a workspace whenever workspace_for asks for one
+  static uint32_t dummy[4];
+  a.ticket = workspace_for(s, GBR_REGIME_TC) ? dummy : nullptr;
+  int groups = 0;
+  if (gbr::launch_tc(a, false, nullptr, &groups) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  return groups;
 }
 
 int router_forward_ex(const void* x, const void* W_gate, const float* bias, int M, int H, int E,

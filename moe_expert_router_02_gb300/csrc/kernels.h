@@ -36,10 +36,15 @@ cudaError_t launch_generic(const RouterArgs& a, bool pdl, cudaStream_t stream);
 
 // tcgen05 prefill router.
 bool tc_eligible(int M, int H, int E, int k, int x_dtype, int w_dtype);
-cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream);
-// Workspace the prefill router needs (NVFP4 W: flags and the decoded copy);
-// launch_tc takes it as RouterArgs::ticket.
-size_t tc_workspace(int H, int E, int w_dtype);
+// With query set nothing launches: *query receives the stream-K group count
+// the launch would use (0: one CTA or CTA pair per tile).
+cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream, int* query = nullptr);
+// The M <= 64 kernels' part of a workspace: the arrival ticket (256 bytes)
+// and FP32 logits [M, E] for M <= 64, E <= 512.
+constexpr size_t kSmallMScratchBytes = 256 + 64 * 512 * 4;
+// Workspace the prefill router needs (flags, stream-K partial accumulators
+// for M >= 4096, NVFP4 W decoded); launch_tc takes it as RouterArgs::ticket.
+size_t tc_workspace(int M, int H, int E, int w_dtype);
 int tc_read_status(int clear);  // 0 ok, 1 a bounded wait expired, -1 query failed
 unsigned* status_word();        // device address of that status word (current device)
 

@@ -1,33 +1,42 @@
 // Large-M (prefill) fused router on the 5th-generation tensor cores.
 //
-// One CTA owns 128 token rows and all E <= 256 experts, so a row's logits
+// A CTA owns 128 token rows and all E <= 256 experts, so a row's logits
 // never leave the SM: TMA streams x [128 x 64] and W_gate [E x 64] BF16
 // tiles (128-byte swizzle) into a shared-memory ring; one thread issues
-// tcgen05.mma (kind::f16, M=128, N=E, K=16) into an FP32 accumulator in
-// tensor memory; after the last k-step the four epilogue warps read their
-// rows back with tcgen05.ld (thread i of warp w owns row 32w+i) and run the
-// activation, top-k and renormalisation in registers. This is the
-// warp-specialised layout the dense_router_decode commit page sketches
+// tcgen05.mma (kind::f16, K=16) into an FP32 accumulator in tensor memory;
+// after the last k-step eight epilogue warps read the rows back with
+// tcgen05.ld (thread = row, two warps per TMEM lane quadrant, each half of
+// the columns) and run the activation, top-k and renormalisation. This is
+// the warp-specialised layout the dense_router_decode commit page sketches
 // ("Warp 5 (TMA) ... Warp 4 (MMA) ... Warps 0-3 (EPI)", "the heap
 // accumulates across subtiles, then merge+renorm+store once per row"),
 // written directly in PTX for sm_103a.
 //
+// By default two CTAs form a pair for 256 rows (M = 256 MMAs issued by the
+// even CTA, each CTA staging half of every W tile). When there are fewer
+// tiles than resident pairs the launch is stream-K: the tiles x k-steps
+// units are split evenly over one pair per two SMs, a pair publishes the
+// partial accumulator of the tile it starts in the workspace and finishes
+// the tile it ends in after adding the partials of the pairs before it.
+//
 // NVFP4 weights (the same page's "NVFP4 blockscaled GEMM"): x stays BF16,
-// and tcgen05 has no BF16 x FP4 kind, so four extra warps decode each W
-// tile exactly into the BF16 shared-memory layout the MMA reads:
-// e2m1 * e4m3 has at most 6 significant bits and fits BF16's exponent
-// range, so the decoded tile equals W / g bit for bit; the FP32 global
+// and tcgen05 has no BF16 x FP4 kind, so the CTAs decode W once per launch,
+// exactly, into a BF16 copy in the workspace that the producers load like
+// BF16 weights: e2m1 * e4m3 has at most 6 significant bits and fits BF16's
+// exponent range, so the copy equals W / g bit for bit; the FP32 global
 // scale g multiplies the accumulator in the epilogue.
 //
-// Every wait on an mbarrier gives up after about a second of
-// %globaltimer, records GBR_ETIMEOUT in a device status word and lets the
-// CTA unwind (free tensor memory, return) instead of hanging.
+// Every wait (mbarriers, flags in global memory) gives up after about a
+// second of %globaltimer, records GBR_ETIMEOUT in a device status word and
+// lets the CTA unwind (free tensor memory, return) instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdlib>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "kernels.h"
 #include "dfkey.cuh"
@@ -284,6 +293,43 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to this CTA's shared memory, completing on the mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void st_cg_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("st.global.cg.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+// Writes 32 consecutive FP32 columns of this thread's TMEM lane (the
+// caller waits with tcgen05.wait::st before the columns are read again).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
 }
 
 // Row-local top list of capacity KC (>= k+1), kept sorted by (key desc,
@@ -599,7 +645,57 @@ struct TcParams {
   // and [0] claim counter, [1] epoch, [2 + kb] flag of column block kb
   uint8_t* wdec;
   unsigned* wsync;
+  // Stream-K (sk = 1): the tiles x k-steps units are split evenly over
+  // `groups` work groups (one CTA, or one CTA pair, per group), so every SM
+  // runs the main loop even when there are fewer tiles than SMs. A group's
+  // range covers at most the tail of one tile (which it finishes) and the
+  // head of the next (whose partial accumulator it publishes); the second
+  // accumulator sits `acc2` columns into tensor memory.
+  int sk, groups, tiles, acc2;
+  float* sk_part;     // [grid CTAs][E/4][BM][4] partial accumulators
+  unsigned* sk_flag;  // [grid CTAs] this launch's epoch + 1 once the partial is out
 };
+
+// One group's work: up to two segments of k-steps, the partial one first
+// (other groups wait for it), then the one that finishes its tile. Scalar
+// fields with select accessors keep the plan in registers.
+struct TcPlan {
+  int nseg;
+  int t0, a0, b0, t1, a1, b1;  // segment s: tile t_s, k-steps [a_s, b_s)
+  bool f0, f1;                 // segment s finishes its tile
+  int p0;  // first group holding a partial of the finished tile (== group: none)
+  __device__ __forceinline__ int t(int s) const { return s ? t1 : t0; }
+  __device__ __forceinline__ int kb0(int s) const { return s ? a1 : a0; }
+  __device__ __forceinline__ int kb1(int s) const { return s ? b1 : b0; }
+  __device__ __forceinline__ bool fin(int s) const { return s ? f1 : f0; }
+};
+
+__device__ __forceinline__ TcPlan tc_plan(const TcParams& p, int grp, int nk) {
+  TcPlan s;
+  s.nseg = 1;
+  s.t0 = grp, s.a0 = 0, s.b0 = nk, s.f0 = true;
+  s.t1 = 0, s.a1 = 0, s.b1 = 0, s.f1 = false;
+  s.p0 = grp;
+  if (!p.sk) return s;
+  const long long U = (long long)p.tiles * nk, G = p.groups;
+  const long long u0 = U * grp / G, u1 = U * (grp + 1) / G;
+  const int t0 = (int)(u0 / nk);
+  const long long te = (long long)(t0 + 1) * nk;
+  const int a0 = (int)(u0 - (long long)t0 * nk);
+  // the group owning unit u is ceil((u + 1) G / U) - 1
+  s.p0 = (int)((((long long)t0 * nk + 1) * G + U - 1) / U - 1);
+  if (u1 > te) {
+    // the tail of tile t0 runs to its end; the head of t0 + 1 is shorter
+    // than a tile (a range spans at most nk units)
+    s.nseg = 2;
+    s.t0 = t0 + 1, s.a0 = 0, s.b0 = (int)(u1 - te), s.f0 = false;
+    s.t1 = t0, s.a1 = a0, s.b1 = nk, s.f1 = true;
+  } else {
+    s.t0 = t0, s.a0 = a0, s.b0 = (int)(u1 - (long long)t0 * nk);
+    s.f0 = s.b0 == nk;
+  }
+  return s;
+}
 
 // Serial unique-route table for one pair of rows (the thread owning the
 // even row of the pair builds it from ids in shared memory). The running
@@ -646,6 +742,8 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
   __shared__ unsigned s_epoch, s_claim;
   __shared__ float s_bias[256];    // the selection bias (sqrt-softplus)
   __shared__ float s_gbmin[2][32];  // least bias per column group (sqrt-softplus)
+  __shared__ __align__(8) uint64_t s_pbar;  // stream-K: a partial has landed
+  __shared__ int s_go;                      // stream-K: prefetch the next partial
   const RouterArgs& a = p.a;
   const int S = p.stages;
   // 1024-byte aligned tile ring, then barriers
@@ -654,16 +752,23 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
   uint8_t* tiles = base;
   uint64_t* full = reinterpret_cast<uint64_t*>(tiles + (size_t)S * p.stage_bytes);
   uint64_t* empty = full + S;
-  uint64_t* accf = empty + S;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  uint64_t* accf = empty + S;  // the finishing accumulator is complete
+  uint64_t* accp = accf + 1;   // the partial accumulator is complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accp + 1);
   int32_t* s_sel = reinterpret_cast<int32_t*>(tmem_slot + 4);  // [BM][kMaxK] for tables
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int producer_warp = kEpiWarps, mma_warp = kEpiWarps + 1;
-  const int m0 = blockIdx.x * BM;
   const int crank = (PAIR || p.mc > 1) ? (int)cluster_rank() : 0;
   const int nk = a.H / BK;
   const int E = a.E;
+  const int grp = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const TcPlan plan = tc_plan(p, grp, nk);
+  const int tile_rows = PAIR ? 2 * BM : BM;
+  const bool has_fin = plan.f0 || plan.f1;
+  const bool has_part = !plan.f0;  // a partial segment always comes first
+  // first row of this CTA's 128 rows of the finished tile
+  const int m0 = (plan.f0 ? plan.t0 : plan.t1) * tile_rows + (PAIR ? crank * BM : 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -671,6 +776,8 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       mbar_init(smem_u32(&empty[s]), (uint32_t)p.mc);  // one release per CTA using the stage
     }
     mbar_init(smem_u32(accf), 1);
+    mbar_init(smem_u32(accp), 1);
+    mbar_init(smem_u32(&s_pbar), 1);
     if (FP4) mbar_init(smem_u32(&s_wready), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -720,33 +827,44 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         go = mbar_wait(smem_u32(&s_wready), 0);
         want = *reinterpret_cast<volatile unsigned*>(&s_epoch) + 1u;
       }
-      for (int kb = 0; kb < nk && go; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (uint32_t)(kb / S) & 1u;
-        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) break;
-        uint8_t* st = tiles + (size_t)s * p.stage_bytes;
-        const uint32_t fb = smem_u32(&full[s]);
-        if (PAIR) {
-          // both CTAs' halves land on the even CTA's barrier
-          const uint32_t fb0 = mapa_u32(fb, 0u);
-          if (crank == 0) mbar_expect_tx(fb, 2u * (p.a_bytes + p.b_bytes));
-          tma_load_2d_pair(smem_u32(st), &tmap_x, kb * BK, m0, fb0, pol_x);
+      for (int sg = 0; sg < plan.nseg && go; ++sg) {
+        const int mrow = plan.t(sg) * tile_rows + (PAIR ? crank * BM : 0);
+        for (int kb = plan.kb0(sg); kb < plan.kb1(sg); ++kb) {
+          const int s = issued % S;  // ring position: k-steps issued so far
+          const uint32_t ph = (uint32_t)(issued / S) & 1u;
+          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) {
+            go = false;
+            break;
+          }
+          uint8_t* st = tiles + (size_t)s * p.stage_bytes;
+          const uint32_t fb = smem_u32(&full[s]);
+          if (PAIR) {
+            // both CTAs' halves land on the even CTA's barrier
+            const uint32_t fb0 = mapa_u32(fb, 0u);
+            if (crank == 0) mbar_expect_tx(fb, 2u * (p.a_bytes + p.b_bytes));
+            tma_load_2d_pair(smem_u32(st), &tmap_x, kb * BK, mrow, fb0, pol_x);
+            ++issued;
+            if (FP4) {
+              if (!wait_flag(p.wsync + 2 + kb, want)) {
+                go = false;
+                break;
+              }
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            tma_load_2d_pair(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, crank * (E / 2), fb0,
+                             pol_w);
+            continue;
+          }
+          mbar_expect_tx(fb, p.a_bytes + p.b_bytes);
+          tma_load_2d(smem_u32(st), &tmap_x, kb * BK, mrow, fb, pol_x);
           ++issued;
-          if (FP4) {
-            if (!wait_flag(p.wsync + 2 + kb, want)) break;
+          if (FP4) {  // the decoded copy: wait for this k-step's columns
+            if (!wait_flag(p.wsync + 2 + kb, want)) {
+              go = false;
+              break;
+            }
             asm volatile("fence.proxy.async.global;" ::: "memory");
           }
-          tma_load_2d_pair(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, crank * (E / 2), fb0, pol_w);
-          continue;
-        }
-        mbar_expect_tx(fb, p.a_bytes + p.b_bytes);
-        tma_load_2d(smem_u32(st), &tmap_x, kb * BK, m0, fb, pol_x);
-        ++issued;
-        if (FP4) {  // the decoded copy: wait for this k-step's columns
-          if (!wait_flag(p.wsync + 2 + kb, want)) break;
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-        }
-        {
           if (p.mc == 1) {
             tma_load_2d(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, 0, fb, pol_w);
           } else {
@@ -760,43 +878,45 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       // let copies still in flight land before the CTA can exit (a pair's
       // odd CTA cannot see them: its exit waits for the pair's last MMA)
       if (!PAIR || crank == 0)
-        for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
-          mbar_wait(smem_u32(&full[kb % S]), (uint32_t)(kb / S) & 1u);
+        for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
+          mbar_wait(smem_u32(&full[i % S]), (uint32_t)(i / S) & 1u);
     }
   } else if (warp == mma_warp) {
-    if (PAIR && lane == 0 && crank == 0) {
-      const uint32_t idesc = idesc_bf16(E, 2 * BM);
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (uint32_t)(kb / S) & 1u;
-        if (!mbar_wait(smem_u32(&full[s]), ph)) break;
-        tc_fence_after();
-        const uint32_t sa = smem_u32(tiles + (size_t)s * p.stage_bytes);
-        const uint32_t sb = sa + p.a_bytes;
+    if (lane == 0 && (!PAIR || crank == 0)) {
+      // the even CTA of a pair issues M = 256 MMAs for both
+      const uint32_t idesc = PAIR ? idesc_bf16(E, 2 * BM) : idesc_bf16(E);
+      int it = 0;  // ring position
+      bool go = true;
+      for (int sg = 0; sg < plan.nseg && go; ++sg) {
+        const uint32_t acc = plan.fin(sg) ? tmem : tmem + (uint32_t)p.acc2;
+        for (int kb = plan.kb0(sg); kb < plan.kb1(sg); ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (uint32_t)(it / S) & 1u;
+          if (!mbar_wait(smem_u32(&full[s]), ph)) {
+            go = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(tiles + (size_t)s * p.stage_bytes);
+          const uint32_t sb = sa + p.a_bytes;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_bf16_pair(tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32), idesc,
-                        (kb > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_pair(smem_u32(&empty[s]));
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t accum = (kb > plan.kb0(sg) || kk > 0) ? 1u : 0u;
+            if (PAIR)
+              mma_bf16_pair(acc, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32),
+                            idesc, accum);
+            else
+              mma_bf16(acc, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32), idesc,
+                       accum);
+          }
+          if (PAIR) mma_commit_pair(smem_u32(&empty[s]));
+          else if (p.mc == 1) mma_commit(smem_u32(&empty[s]));
+          else mma_commit_mc(smem_u32(&empty[s]), (uint16_t)((1u << p.mc) - 1u));
+        }
+        const uint32_t done = smem_u32(plan.fin(sg) ? accf : accp);
+        if (PAIR) mma_commit_pair(done);
+        else mma_commit(done);
       }
-      mma_commit_pair(smem_u32(accf));
-    } else if (!PAIR && lane == 0) {
-      const uint32_t idesc = idesc_bf16(E);
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (uint32_t)(kb / S) & 1u;
-        if (!mbar_wait(smem_u32(&full[s]), ph)) break;
-        tc_fence_after();
-        const uint32_t sa = smem_u32(tiles + (size_t)s * p.stage_bytes);
-        const uint32_t sb = sa + p.a_bytes;
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_bf16(tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32), idesc,
-                   (kb > 0 || kk > 0) ? 1u : 0u);
-        if (p.mc == 1) mma_commit(smem_u32(&empty[s]));
-        else mma_commit_mc(smem_u32(&empty[s]), (uint16_t)((1u << p.mc) - 1u));
-      }
-      mma_commit(smem_u32(accf));
     }
   } else if (warp < kEpiWarps) {
     // epilogue: warp w reads TMEM lanes 32(w%4).. of columns half w/4
@@ -840,6 +960,18 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         float m = INFINITY;
         for (int c = lo + q; c < hi; c += G) m = fminf(m, has_bias ? __ldg(a.bias + c) : 0.0f);
         s_gbmin[h][q] = m;
+      }
+    }
+    if (!FP4 && p.sk && threadIdx.x == 0) {
+      // this launch's epoch (the flags it sets are epoch + 1): read after the
+      // previous launch has finished, then one arrival per CTA; the last
+      // arrival resets the counter and advances the epoch for the next launch
+      pdl_wait();
+      s_epoch = ld_acquire_u32(p.wsync + 1);
+      const unsigned t = atomicAdd(p.wsync, 1u);
+      if (t == gridDim.x - 1u) {
+        asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(p.wsync) : "memory");
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.wsync + 1) : "memory");
       }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
@@ -913,10 +1045,149 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
                        : "memory");
       }
     }
-    const bool ok = mbar_wait_warp(smem_u32(accf), 0);
-    tc_fence_after();
+    const unsigned sk_want = *reinterpret_cast<volatile unsigned*>(&s_epoch) + 1u;
     const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+    if (has_part) {
+      // publish the partial accumulator: this CTA's slot of the workspace,
+      // [E/4][BM][4] (a warp stores 512 contiguous bytes per 4 columns), then
+      // the flag; finishers fetch it with one bulk copy
+      const bool okp = mbar_wait_warp(smem_u32(accp), 0);
+      tc_fence_after();
+      if (okp) {
+        float* part = p.sk_part + (size_t)blockIdx.x * E * BM + row * 4;
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+          float v[32];
+          tmem_ld32(trow + (uint32_t)p.acc2 + c0, v);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)  // E % 16 == 0: a group of 4 is all in or all out
+            if (c0 + 4 * i < c_hi)
+              st_cg_v4(part + (size_t)(c0 / 4 + i) * BM * 4, v[4 * i], v[4 * i + 1],
+                       v[4 * i + 2], v[4 * i + 3]);
+        }
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // read by bulk copies
+      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+      if (threadIdx.x == 0) {
+        __threadfence();
+        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.sk_flag + blockIdx.x),
+                     "r"(sk_want)
+                     : "memory");
+      }
+    }
+    // The finished tile's other partials P_q (groups p0 .. grp-1) are summed
+    // in group order into S in the spare accumulator columns, and the tile's
+    // logits are fin + S: the same additions in the same order whichever
+    // way each partial arrives. While the main loop still runs, partials
+    // whose flags are already set stream in through registers; the rest land
+    // in the idle tile ring by bulk copies once the accumulator is complete.
+    const int nparts = has_fin ? grp - plan.p0 : 0;
+    const uint32_t tS = trow + (uint32_t)p.acc2;
+    int pre = 0;
+    for (int q = plan.p0; q < plan.p0 + nparts; ++q) {
+      const int slot = q * (PAIR ? 2 : 1) + crank;
+      if (threadIdx.x == 0) {
+        // whichever comes first: the partial (prefetch it) or the end of the
+        // main loop (the bulk copies below are then faster)
+        int go = 0;
+        const uint64_t t0 = globaltimer();
+        uint32_t ns = 64;
+        for (;;) {
+          if (ld_acquire_u32(p.sk_flag + slot) == sk_want) {
+            go = 1;
+            break;
+          }
+          if (mbar_try(smem_u32(accf), 0) || globaltimer() - t0 > kWaitNs) break;
+          __nanosleep(ns);
+          if (ns < 512) ns <<= 1;
+        }
+        s_go = go;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+      const bool go = *reinterpret_cast<volatile int*>(&s_go) != 0;
+      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+      if (!go) break;
+      wait_flag(p.sk_flag + slot, sk_want);  // set: this thread's own acquire
+      const float* part = p.sk_part + (size_t)slot * E * BM + row * 4;
+      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          // E % 16 == 0: a group of 4 columns is all in or all out
+          const int g4 = min(c0 / 4 + i, E / 4 - 1);
+          const float4 u = __ldcg(reinterpret_cast<const float4*>(part + (size_t)g4 * BM * 4));
+          v[4 * i] = u.x, v[4 * i + 1] = u.y, v[4 * i + 2] = u.z, v[4 * i + 3] = u.w;
+        }
+        if (pre > 0) {
+          float w[32];
+          tmem_ld32(tS + c0, w);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = w[j] + v[j];
+        }
+        tmem_st32(tS + c0, v);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      ++pre;
+    }
+    // a CTA whose range ends inside a tile has no rows to finish
+    const bool ok = has_fin && mbar_wait_warp(smem_u32(accf), 0);
+    tc_fence_after();
     const bool all_ok = __all_sync(kFull, ok);
+    if (all_ok && nparts > 0) {
+      const uint32_t pbytes = (uint32_t)E * BM * 4;
+      for (int q = plan.p0 + pre; q <= grp; ++q) {
+        // q < grp: P_q lands in the ring (S += P_q, and on the last one the
+        // logits fin + S); q == grp: every partial came early, fin + S only
+        const bool last = q >= grp - 1;
+        const bool have = q < grp;
+        bool okq = true;
+        if (have) {
+          const int slot = q * (PAIR ? 2 : 1) + crank;
+          wait_flag(p.sk_flag + slot, sk_want);
+          if (threadIdx.x == 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_expect_tx(smem_u32(&s_pbar), pbytes);
+            bulk_g2s(smem_u32(tiles), p.sk_part + (size_t)slot * E * BM, pbytes,
+                     smem_u32(&s_pbar));
+          }
+          okq = mbar_wait_warp(smem_u32(&s_pbar), (uint32_t)(q - plan.p0 - pre) & 1u);
+        }
+        if (okq) {
+          const bool hasS = q > plan.p0;  // S holds P_p0 .. P_(q-1)
+          const float4* sp4 = reinterpret_cast<const float4*>(tiles) + row;
+          for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+            float v[32];
+            if (have) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 u = sp4[(size_t)min(c0 / 4 + i, E / 4 - 1) * BM];
+                v[4 * i] = u.x, v[4 * i + 1] = u.y, v[4 * i + 2] = u.z, v[4 * i + 3] = u.w;
+              }
+            }
+            if (hasS) {
+              float w[32];
+              tmem_ld32(tS + c0, w);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = have ? w[j] + v[j] : w[j];
+            }
+            if (last) {
+              float f[32];
+              tmem_ld32(trow + c0, f);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = f[j] + v[j];
+              tmem_st32(trow + c0, v);
+            } else {
+              tmem_st32(tS + c0, v);
+            }
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+        // every warp is done with the staged partial before the next lands
+        // (or, after the last, before pass A writes over the ring)
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+        if (last) break;
+      }
+    }
     // the idle tile ring: exchange area, then per-(half, row) candidate lists
     uint32_t* xo = reinterpret_cast<uint32_t*>(tiles);       // [KC][BM]
     int32_t* xi = reinterpret_cast<int32_t*>(xo + KC * BM);  // [KC][BM]
@@ -1109,9 +1380,11 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       }
       xm[row] = amax;
       xm[BM + row] = kabs;
-
     }
+    // (stream-K: the first half reads columns the second half wrote back)
+    tc_fence_before();
     asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+    tc_fence_after();
     if (half == 0 && all_ok) {
 #pragma unroll
       for (int j = 0; j < KC; ++j) top.push(xo[j * BM + row], xi[j * BM + row], xz[j * BM + row]);
@@ -1299,16 +1572,102 @@ bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows)
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr int kSkMaxCtas = 160;    // stream-K flag and partial slots in the workspace
+constexpr int kSkMinRows = 4096;   // smaller M gets no partial slots
+constexpr int kSkMaxParts = 3;     // partials a finishing group may add
+
+// Largest number of other groups holding units of one tile when U = tiles *
+// nk units are split evenly over G groups (the group owning unit u is
+// ceil((u + 1) G / U) - 1).
+int sk_max_parts(int tiles, int nk, int G) {
+  const long long U = (long long)tiles * nk;
+  auto owner = [&](long long u) { return (int)(((u + 1) * G + U - 1) / U - 1); };
+  int mx = 0;
+  for (int t = 0; t < tiles; ++t) {
+    const int n = owner((long long)(t + 1) * nk - 1) - owner((long long)t * nk);
+    mx = n > mx ? n : mx;
+  }
+  return mx;
+}
+
+// Work groups that are resident at once, one CTA (or pair) per SM at most;
+// the stream-K finishers wait for other groups' partials, so the whole grid
+// has to fit. Cached per kernel, shared-memory size and device.
+int sk_resident_groups(const void* kern, size_t smem, int cl) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, size_t, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(kern, smem, dev);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int sms = 0, n = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 0;
+  if (cl > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cl);
+    cfg.blockDim = dim3((kEpiWarps + 2) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = cl;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  } else {
+    int per = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, (kEpiWarps + 2) * 32, smem) !=
+        cudaSuccess)
+      per = 0;
+    n = per * sms;
+  }
+  (void)cudaGetLastError();  // a failed query leaves no sticky error
+  if (n > sms / cl) n = sms / cl;
+  if (n > kSkMaxCtas / cl) n = kSkMaxCtas / cl;
+  // GBR_TC_SK_GROUPS=n caps the group count (tuning)
+  static const int cap = [] {
+    const char* v = getenv("GBR_TC_SK_GROUPS");
+    return v ? atoi(v) : 0;
+  }();
+  if (cap > 0 && n > cap) n = cap;
+  cache[key] = n;
+  return n;
+}
+
 template <int KC, bool FP4, bool PAIR>
-cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcParams& p,
-                      size_t smem, bool pdl, cudaStream_t stream) {
+cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcParams& p0,
+                      size_t smem, bool pdl, bool want_sk, cudaStream_t stream, int* query) {
   auto kern = k_tc_router<KC, FP4, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  const int tiles = (p.a.M + BM - 1) / BM;
+  TcParams p = p0;
   const int cl = PAIR ? 2 : p.mc;
-  cfg.gridDim = dim3((tiles + cl - 1) / cl * cl);
+  int grid = ((p.a.M + BM - 1) / BM + cl - 1) / cl * cl;
+  if (want_sk && p.mc == 1) {
+    // stream-K when there are fewer tiles than resident groups: the
+    // tiles x k-steps units split evenly over all of them
+    const int G = sk_resident_groups(reinterpret_cast<const void*>(kern), smem, cl);
+    const int tiles = (p.a.M + cl * BM - 1) / (cl * BM);
+    const int nk = p.a.H / BK;
+    if (G > 0 && tiles < G && (long long)tiles * nk >= G &&
+        sk_max_parts(tiles, nk, G) <= kSkMaxParts && 2 * p.tmem_cols <= 512) {
+      p.sk = 1;
+      p.groups = G;
+      p.tiles = tiles;
+      p.acc2 = p.tmem_cols;
+      p.tmem_cols *= 2;
+      grid = G * cl;
+    }
+  }
+  if (query) {  // report the choice without launching
+    *query = p.sk ? p.groups : 0;
+    return cudaSuccess;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3((kEpiWarps + 2) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -1333,15 +1692,15 @@ cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcPara
 
 template <bool FP4, bool PAIR>
 cudaError_t dispatch_k(const CUtensorMap& mx, const CUtensorMap& mw, const TcParams& p,
-                       size_t smem, bool pdl, cudaStream_t s) {
+                       size_t smem, bool pdl, bool sk, cudaStream_t s, int* q) {
   // KC >= k + 2: the list keeps one key past the (k+1)-th, so a near tie at
   // the k / k+1 boundary can be settled inside the list
   const int k = p.a.k;
-  if (k <= 2) return launch_kc<4, FP4, PAIR>(mx, mw, p, smem, pdl, s);
-  if (k <= 4) return launch_kc<6, FP4, PAIR>(mx, mw, p, smem, pdl, s);
-  if (k <= 6) return launch_kc<8, FP4, PAIR>(mx, mw, p, smem, pdl, s);
-  if (k <= 8) return launch_kc<10, FP4, PAIR>(mx, mw, p, smem, pdl, s);
-  return launch_kc<18, FP4, PAIR>(mx, mw, p, smem, pdl, s);
+  if (k <= 2) return launch_kc<4, FP4, PAIR>(mx, mw, p, smem, pdl, sk, s, q);
+  if (k <= 4) return launch_kc<6, FP4, PAIR>(mx, mw, p, smem, pdl, sk, s, q);
+  if (k <= 6) return launch_kc<8, FP4, PAIR>(mx, mw, p, smem, pdl, sk, s, q);
+  if (k <= 8) return launch_kc<10, FP4, PAIR>(mx, mw, p, smem, pdl, sk, s, q);
+  return launch_kc<18, FP4, PAIR>(mx, mw, p, smem, pdl, sk, s, q);
 }
 
 }  // namespace
@@ -1351,26 +1710,48 @@ bool tc_eligible(int M, int H, int E, int k, int x_dtype, int w_dtype) {
          E % 16 == 0 && E >= 16 && E <= 256 && H % BK == 0 && k <= kMaxK;
 }
 
-// NVFP4 workspace: the tile flags (after the claim counter and the epoch),
-// then the decoded W at a 256-byte boundary.
+// Workspace. The small-M kernels' ticket and logits may share it (one
+// library workspace per stream), so the prefill kernel's part starts past
+// their largest extent: words [0] claim / arrival counter, [1] epoch,
+// [2, 2 + H/64) NVFP4 column-block flags, then the stream-K flags; from the
+// next 256-byte boundary the stream-K partial accumulators (M >=
+// kSkMinRows), then the decoded NVFP4 W. Every flag holds the epoch + 1 of
+// the launch that set it, and the epoch only grows, so no stale flag
+// matches a later launch.
 static size_t tc_flag_bytes(int H) {
-  return ((size_t)(2 + H / BK) * 4 + 255) / 256 * 256;
+  return ((size_t)(2 + H / BK + kSkMaxCtas) * 4 + 255) / 256 * 256;
 }
 
-size_t tc_workspace(int H, int E, int w_dtype) {
-  if (w_dtype != DT_NVFP4) return 0;
-  return tc_flag_bytes(H) + (size_t)E * H * 2;
+static bool tc_sk_sized(int M) { return M >= kSkMinRows; }
+
+static size_t tc_part_bytes(int E) { return (size_t)kSkMaxCtas * E * BM * 4; }
+
+size_t tc_workspace(int M, int H, int E, int w_dtype) {
+  const bool fp4 = w_dtype == DT_NVFP4, sk = tc_sk_sized(M);
+  if (!fp4 && !sk) return 0;
+  return kSmallMScratchBytes + tc_flag_bytes(H) + (sk ? tc_part_bytes(E) : 0) +
+         (fp4 ? (size_t)E * H * 2 : 0);
 }
 
-cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
+cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream, int* query) {
   const bool fp4 = a.w_dtype == DT_NVFP4;
   TcParams p{};
   p.a = a;
-  if (fp4) {
-    if (!a.ticket) return cudaErrorInvalidValue;
-    p.wsync = a.ticket;
-    p.wdec = reinterpret_cast<uint8_t*>(a.ticket) + tc_flag_bytes(a.H);
+  if (fp4 && !a.ticket) return cudaErrorInvalidValue;
+  const bool sk_ws = a.ticket && tc_sk_sized(a.M);
+  if (a.ticket) {
+    uint8_t* ws = reinterpret_cast<uint8_t*>(a.ticket) + kSmallMScratchBytes;
+    p.wsync = reinterpret_cast<unsigned*>(ws);
+    p.sk_flag = p.wsync + 2 + a.H / BK;
+    p.sk_part = sk_ws ? reinterpret_cast<float*>(ws + tc_flag_bytes(a.H)) : nullptr;
+    if (fp4) p.wdec = ws + tc_flag_bytes(a.H) + (sk_ws ? tc_part_bytes(a.E) : 0);
   }
+  // stream-K (the default where it applies; GBR_TC_SK=0 turns it off)
+  static const bool sk_env = [] {
+    const char* v = getenv("GBR_TC_SK");
+    return !(v && v[0] == '0');
+  }();
+  const bool want_sk = sk_env && sk_ws;
   // CTA pairs (the default; GBR_TC_PAIR=0 turns them off): each CTA stages
   // its 128 rows of x and half of the W tile, and the even CTA issues
   // M = 256 MMAs for both, so each SM's shared memory carries a third less
@@ -1383,7 +1764,7 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
   p.a_bytes = BM * BK * 2;
   p.b_bytes = (uint32_t)(p.pair ? a.E / 2 : a.E) * BK * 2;
   p.stage_bytes = p.a_bytes + p.b_bytes;
-  const size_t extra = 1024 /*align*/ + 2 * 8 * 8 + 8 + 16 + BM * kMaxK * 4;
+  const size_t extra = 1024 /*align*/ + 2 * 8 * 8 + 16 + 16 + BM * kMaxK * 4;
   const size_t budget = 227 * 1024 - 4096;  // the rest holds the static shared arrays
   int S = (int)((budget - extra) / p.stage_bytes);
   if (S > 6) S = 6;
@@ -1406,17 +1787,19 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream) {
     return (v && v[0] == '1') ? 2 : 1;
   }();
   p.mc = (!fp4 && !p.pair && a.E % 16 == 0) ? mc_env : 1;
-  CUtensorMap mx, mw;
-  if (!make_map(&mx, a.x, a.M, a.H, BM)) return cudaErrorInvalidValue;
-  // NVFP4: the kernel decodes W into the workspace as a BF16 [E, H] copy
-  if (!make_map(&mw, fp4 ? static_cast<const void*>(p.wdec) : a.w, a.E, a.H,
-                p.pair ? a.E / 2 : a.E / p.mc))
-    return cudaErrorInvalidValue;
+  CUtensorMap mx{}, mw{};
+  if (!query) {
+    if (!make_map(&mx, a.x, a.M, a.H, BM)) return cudaErrorInvalidValue;
+    // NVFP4: the kernel decodes W into the workspace as a BF16 [E, H] copy
+    if (!make_map(&mw, fp4 ? static_cast<const void*>(p.wdec) : a.w, a.E, a.H,
+                  p.pair ? a.E / 2 : a.E / p.mc))
+      return cudaErrorInvalidValue;
+  }
   if (p.pair)
-    return fp4 ? dispatch_k<true, true>(mx, mw, p, smem, pdl, stream)
-               : dispatch_k<false, true>(mx, mw, p, smem, pdl, stream);
-  return fp4 ? dispatch_k<true, false>(mx, mw, p, smem, pdl, stream)
-             : dispatch_k<false, false>(mx, mw, p, smem, pdl, stream);
+    return fp4 ? dispatch_k<true, true>(mx, mw, p, smem, pdl, want_sk, stream, query)
+               : dispatch_k<false, true>(mx, mw, p, smem, pdl, want_sk, stream, query);
+  return fp4 ? dispatch_k<true, false>(mx, mw, p, smem, pdl, want_sk, stream, query)
+             : dispatch_k<false, false>(mx, mw, p, smem, pdl, want_sk, stream, query);
 }
 
 unsigned* status_word() {

@@ -22,7 +22,7 @@ GBR_REGIME_GENERIC, GBR_REGIME_GEMV, GBR_REGIME_TC, GBR_REGIME_UNFUSED, GBR_REGI
     0, 1, 2, 3, 4
 
 EXPORTS = ("router_forward", "router_forward_ex", "router_workspace_size", "router_regime",
-           "router_select", "route_table", "router_strerror", "router_device_status",
+           "router_tc_groups", "router_select", "route_table", "router_strerror", "router_device_status",
            "router_forward_noalloc", "router_near_tie_keys", "route_gather_add")
 
 
@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
             L.router_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(GbrOpts)]
             L.router_workspace_size.restype = S
             L.router_regime.argtypes = [I, I, I, I, ctypes.POINTER(GbrOpts)]
+            L.router_tc_groups.argtypes = [I, I, I, I, ctypes.POINTER(GbrOpts)]
             L.router_select.argtypes = [P, P, I, I, I, I, P, P, P]
             L.route_table.argtypes = [P, I, I, I, P, P, P, P, P]
             L.router_forward_noalloc.argtypes = [P, P, P, I, I, I, I, I, P, P, P]
@@ -67,7 +68,8 @@ def lib() -> ctypes.CDLL:
             L.router_strerror.argtypes = [I]
             L.router_strerror.restype = ctypes.c_char_p
             L.router_device_status.argtypes = [I]
-            for f in (L.router_forward, L.router_forward_ex, L.router_regime, L.router_select,
+            for f in (L.router_forward, L.router_forward_ex, L.router_regime, L.router_tc_groups,
+                      L.router_select,
                       L.route_table, L.router_device_status, L.router_forward_noalloc,
                       L.router_near_tie_keys, L.route_gather_add):
                 f.restype = I
@@ -141,6 +143,11 @@ def router_workspace_size(M, H, E, k, opts=None) -> int:
 
 def router_regime(M, H, E, k, opts=None) -> int:
     return lib().router_regime(M, H, E, k, ctypes.byref(opts) if opts is not None else None)
+
+
+def router_tc_groups(M, H, E, k, opts=None) -> int:
+    """Stream-K work groups of the prefill kernel for this shape (0: none)."""
+    return lib().router_tc_groups(M, H, E, k, ctypes.byref(opts) if opts is not None else None)
 
 
 def router_select(logits, bias, M, E, k, act, out_idx, out_w, stream=None):

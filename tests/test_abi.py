@@ -120,3 +120,20 @@ def test_regime_choice():
     assert R.router_regime(8, 2048, 256, 8, R.make_opts(flags=R.GBR_FLAG_FORCE_GENERIC)) == \
         R.GBR_REGIME_GENERIC
     assert R.router_regime(1, 64, 16, 17) == -1
+
+
+def test_prefill_workspace_layout():
+    # the prefill kernel's part of a workspace starts past the M <= 64
+    # kernels' ticket and logits (256 + 64 * 512 * 4 bytes); from 4096 rows
+    # it holds 160 stream-K partial accumulators of E x 128 FP32
+    small = 256 + 64 * 512 * 4
+    assert R.router_workspace_size(1000, 7168, 256, 8) == 0
+    big = R.router_workspace_size(16384, 7168, 256, 8)
+    assert big >= small + 160 * 256 * 128 * 4
+    assert big < small + 160 * 256 * 128 * 4 + 4096
+    fp4 = R.make_opts(w_dtype=R.GBR_NVFP4, w_scales=1)
+    assert R.router_workspace_size(1000, 7168, 256, 8, fp4) >= small + 256 * 7168 * 2
+    assert R.router_workspace_size(16384, 7168, 256, 8, fp4) >= big + 256 * 7168 * 2
+    # stream-K groups: none outside the prefill kernel, -1 for rejected shapes
+    assert R.router_tc_groups(8, 2048, 256, 8) == 0
+    assert R.router_tc_groups(1, 64, 16, 17) == -1
