@@ -35,7 +35,7 @@ LAYERS = 40          # router calls per decode token (one per MoE layer)
 # DRAM bytes per launch of the headline kernel from one ncu capture
 # (profiles/decode_router_m8_h2048_e256.md), valid only for the kernel
 # sources it was taken on.
-TRAFFIC = {"decode": {"bytes": 1160192, "src_sha": "90a7b685a3c06cf1"}}
+TRAFFIC = {"decode": {"bytes": 1160021, "src_sha": "b82eaca7f09986de"}}
 
 
 def kernel_src_sha():

@@ -148,13 +148,13 @@ int router_regime(int M, int H, int E, int k, const gbr_opts* opt);
 
 /* Stream-K work groups the prefill kernel (GBR_REGIME_TC) would split this
  * shape over on the current device: the tiles x k-steps units divided
- * evenly over one CTA pair (or CTA) per two SMs (per SM), each group
- * finishing at most one tile after adding the other groups' partial
- * accumulators from the workspace. 0 when every tile gets its own CTA
- * pair (fewer than 4096 rows, at least as many tiles as groups, a tile
- * split over more than four groups, GBR_TC_SK=0 in the environment) or the
- * shape takes another kernel family; -1 for arguments router_forward_ex
- * would reject or a failed device query. Launches nothing. */
+ * evenly over up to one CTA pair (or CTA) per two SMs (per SM), as many as
+ * keep every tile within four groups; each group finishes at most one tile
+ * after adding the other groups' partial accumulators from the workspace.
+ * 0 when every tile gets its own CTA pair (fewer than 256 rows, at least as
+ * many tiles as groups, GBR_TC_SK=0 in the environment) or the shape takes
+ * another kernel family; -1 for arguments router_forward_ex would reject or
+ * a failed device query. Launches nothing. */
 int router_tc_groups(int M, int H, int E, int k, const gbr_opts* opt);
 
 /*

@@ -43,7 +43,7 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream, int* q
 // and FP32 logits [M, E] for M <= 64, E <= 512.
 constexpr size_t kSmallMScratchBytes = 256 + 64 * 512 * 4;
 // Workspace the prefill router needs (flags, stream-K partial accumulators
-// for M >= 4096, NVFP4 W decoded); launch_tc takes it as RouterArgs::ticket.
+// for M >= 256, NVFP4 W decoded); launch_tc takes it as RouterArgs::ticket.
 size_t tc_workspace(int M, int H, int E, int w_dtype);
 int tc_read_status(int clear);  // 0 ok, 1 a bounded wait expired, -1 query failed
 unsigned* status_word();        // device address of that status word (current device)

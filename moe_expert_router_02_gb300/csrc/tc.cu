@@ -1573,7 +1573,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows)
 }
 
 constexpr int kSkMaxCtas = 160;    // stream-K flag and partial slots in the workspace
-constexpr int kSkMinRows = 4096;   // smaller M gets no partial slots
+constexpr int kSkMinRows = 256;    // smaller M gets no partial slots
 constexpr int kSkMaxParts = 3;     // partials a finishing group may add
 
 // Largest number of other groups holding units of one tile when U = tiles *
@@ -1588,6 +1588,24 @@ int sk_max_parts(int tiles, int nk, int G) {
     mx = n > mx ? n : mx;
   }
   return mx;
+}
+
+// The most groups, up to G, that split U = tiles * nk units with no tile
+// over more than kSkMaxParts + 1 groups and every range non-empty (0: none,
+// more groups than tiles being the point). Cached: a launch only looks it up.
+int sk_groups_for(int tiles, int nk, int G) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int>, int> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(tiles, nk, G);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int g = G;
+  if ((long long)tiles * nk < g) g = (int)((long long)tiles * nk);
+  while (g > tiles && sk_max_parts(tiles, nk, g) > kSkMaxParts) --g;
+  const int r = g > tiles ? g : 0;
+  cache[key] = r;
+  return r;
 }
 
 // Work groups that are resident at once, one CTA (or pair) per SM at most;
@@ -1648,12 +1666,13 @@ cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcPara
   int grid = ((p.a.M + BM - 1) / BM + cl - 1) / cl * cl;
   if (want_sk && p.mc == 1) {
     // stream-K when there are fewer tiles than resident groups: the
-    // tiles x k-steps units split evenly over all of them
-    const int G = sk_resident_groups(reinterpret_cast<const void*>(kern), smem, cl);
+    // tiles x k-steps units split evenly over as many of them as keep every
+    // tile within four groups
     const int tiles = (p.a.M + cl * BM - 1) / (cl * BM);
     const int nk = p.a.H / BK;
-    if (G > 0 && tiles < G && (long long)tiles * nk >= G &&
-        sk_max_parts(tiles, nk, G) <= kSkMaxParts && 2 * p.tmem_cols <= 512) {
+    const int Gr = sk_resident_groups(reinterpret_cast<const void*>(kern), smem, cl);
+    const int G = Gr > tiles ? sk_groups_for(tiles, nk, Gr) : 0;
+    if (G > 0 && 2 * p.tmem_cols <= 512) {
       p.sk = 1;
       p.groups = G;
       p.tiles = tiles;

@@ -1,7 +1,8 @@
 """Stream-K form of the tcgen05 prefill router. With fewer 256-row tiles
 than CTA pairs the device can hold, the tiles x k-steps units are split
-evenly over one CTA pair per two SMs: a group finishes at most one tile,
-adding the partial accumulators other groups published in the workspace.
+evenly over up to one CTA pair per two SMs (as many as keep each tile
+within four groups): a group finishes at most one tile, adding the partial
+accumulators other groups published in the workspace.
 Every case here is checked against the oracle as in the other prefill tests
 (ids, weights, logits, the selection on the kernel's own logits bit-exact,
 the unfused selection bit-identical)."""
@@ -35,9 +36,13 @@ def test_engaged_on_the_prefill_workload():
     g = R.router_tc_groups(16384, 7168, 256, 8)
     assert 64 < g <= 80
     assert R.router_tc_groups(8192, 7168, 256, 8) == g
-    # below 4096 rows, or with a tile split more than four ways: a pair per tile
-    assert R.router_tc_groups(2048, 7168, 256, 8) == 0
-    assert R.router_tc_groups(4096, 7168, 256, 8) == 0
+    # fewer tiles: fewer groups, so that no tile is split more than four ways
+    g16 = R.router_tc_groups(4096, 7168, 256, 8)
+    assert 16 < g16 <= 64 and g16 < g
+    g2 = R.router_tc_groups(300, 7168, 256, 8)
+    assert 2 < g2 <= 8
+    # below 256 rows: a pair per tile
+    assert R.router_tc_groups(200, 7168, 256, 8) == 0
     # not the prefill kernel
     assert R.router_tc_groups(8, 2048, 256, 8) == 0
     assert R.router_tc_groups(1, 64, 16, 17) == -1
@@ -50,6 +55,8 @@ def test_engaged_on_the_prefill_workload():
     (9000, 768, 64, 4, synth.SQRT_SOFTPLUS, False),
     (6000, 2048, 256, 16, synth.SQRT_SOFTPLUS, True),       # KC = 18 list
     (12000, 512, 256, 2, synth.SOFTMAX, False),
+    (300, 2048, 256, 8, synth.SQRT_SOFTPLUS, True),          # two tiles, few groups
+    (2000, 7168, 256, 8, synth.SOFTMAX, False),             # eight tiles, long K
 ])
 def test_parity(M, H, E, k, act, bias):
     case = small_prefill(M, H=H, E=E, k=k, act=act, bias=bias, seed=M + H + E + k)
