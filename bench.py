@@ -33,18 +33,19 @@ sys.path.insert(0, ROOT)
 LAYERS = 40          # router calls per decode token (one per MoE layer)
 
 # DRAM bytes per launch of the headline kernel from one ncu capture
-# (profiles/decode_router_m8_h2048_e256.md), valid only for the kernel
-# sources it was taken on.
-TRAFFIC = {"decode": {"bytes": 1160021, "src_sha": "b82eaca7f09986de"}}
+# (profiles/decode_router_m8_h2048_e256.md), valid only for the sources that
+# kernel is built from: its file (kernel and launcher) and the headers that
+# file includes.
+DECODE_SOURCES = ("gemv.cu", "kernels.h", "select.cuh", "dfkey.cuh", "common.cuh")
+TRAFFIC = {"decode": {"bytes": 1160021, "src_sha": "8d30b576444a97d5"}}
 
 
-def kernel_src_sha():
-    import glob
+def kernel_src_sha(files=DECODE_SOURCES):
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "moe_expert_router_02_gb300", "csrc", "*"))):
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for f in sorted(files):
+        h.update(f.encode())
+        with open(os.path.join(ROOT, "moe_expert_router_02_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -52,6 +53,8 @@ def kernel_src_sha():
 def traffic_for(name):
     t = TRAFFIC.get(name)
     return t["bytes"] if t and t["src_sha"] == kernel_src_sha() else None
+
+
 W_POOL_BYTES = 520 << 20
 
 

@@ -150,9 +150,10 @@ int router_tc_groups(int M, int H, int E, int k, const gbr_opts* opt) {
   gbr::RouterArgs a{};
   a.M = M, a.H = H, a.E = E, a.k = k, a.act = GBR_ACT_SOFTMAX;
   a.x_dtype = s.x_dtype, a.w_dtype = s.w_dtype;
-  // the launch gets a workspace whenever workspace_for asks for one
-  static uint32_t dummy[4];
-  a.ticket = workspace_for(s, GBR_REGIME_TC) ? dummy : nullptr;
+  // the launch gets a workspace whenever workspace_for asks for one (a
+  // query only tests the pointer for null)
+  static uint32_t present;
+  a.ticket = workspace_for(s, GBR_REGIME_TC) ? &present : nullptr;
   int groups = 0;
   if (gbr::launch_tc(a, false, nullptr, &groups) != cudaSuccess) {
     (void)cudaGetLastError();

@@ -1758,7 +1758,7 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream, int* q
   p.a = a;
   if (fp4 && !a.ticket) return cudaErrorInvalidValue;
   const bool sk_ws = a.ticket && tc_sk_sized(a.M);
-  if (a.ticket) {
+  if (a.ticket && !query) {  // a query only needs to know a workspace is there
     uint8_t* ws = reinterpret_cast<uint8_t*>(a.ticket) + kSmallMScratchBytes;
     p.wsync = reinterpret_cast<unsigned*>(ws);
     p.sk_flag = p.wsync + 2 + a.H / BK;
