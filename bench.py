@@ -471,6 +471,16 @@ def run_detail(args, peaks):
                           ("C3_prefill_bf16_sigmoid", synth.BF16, synth.SIGMOID)):
         rs = RouterSet(dict(cfg3, act=act), cfg3["M"], 1, w_dtype=wd, pool_bytes=0)
         record(name, rs, steps=10, flops=flops)
+    # smaller prefill batches of the same shape: stream-K spreads their few
+    # tiles over more SMs (router_tc_groups pairs)
+    for M in (4096, 8192):
+        name = f"C3_prefill_bf16_M{M}"
+        try:
+            record(name, RouterSet(cfg3, M, 1, pool_bytes=0), steps=10,
+                   flops=2 * M * cfg3["H"] * cfg3["E"])
+            out[name]["stream_k_groups"] = R.router_tc_groups(M, cfg3["H"], cfg3["E"], cfg3["k"])
+        except Exception as e:  # a detail row never costs the headline line
+            out[name] = {"error": str(e)[:200]}
     return out
 
 
