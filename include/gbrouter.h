@@ -57,7 +57,7 @@ typedef struct CUstream_st* cudaStream_t;
 enum {
   GBR_OK = 0,
   GBR_EINVAL = 1,       /* bad argument: null pointer, k < 1, k > E, bad enum, ... */
-  GBR_EUNSUPPORTED = 2, /* valid but outside this build: E > 512, k > 16 */
+  GBR_EUNSUPPORTED = 2, /* valid but beyond the library's limits: E > 512, k > 16 */
   GBR_ECUDA = 3,        /* a CUDA runtime call or launch failed */
   GBR_EWORKSPACE = 4,   /* caller workspace smaller than router_workspace_size() */
   GBR_ETIMEOUT = 5      /* a bounded device-side wait expired (see router_device_status) */

@@ -13,7 +13,7 @@ def pytest_configure(config):
 
 
 def pytest_collection_modifyitems(config, items):
-    # GPU tests need the device; off a GPU machine they are skipped, never faked.
+    # GPU tests need the device; without one they are skipped, never faked.
     try:
         import torch
         has_gpu = torch.cuda.is_available()
