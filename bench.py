@@ -32,10 +32,9 @@ sys.path.insert(0, ROOT)
 
 LAYERS = 40          # router calls per decode token (one per MoE layer)
 
-# DRAM bytes per launch of the headline kernel from one ncu capture
-# (profiles/decode_router_m8_h2048_e256.md), valid only for the sources that
-# kernel is built from: its file (kernel and launcher) and the headers that
-# file includes.
+# DRAM bytes per launch of the headline kernel from one ncu capture of the
+# decode workload, valid only for the sources that kernel is built from: its
+# file (kernel and launcher) and the headers that file includes.
 DECODE_SOURCES = ("gemv.cu", "kernels.h", "select.cuh", "dfkey.cuh", "common.cuh")
 TRAFFIC = {"decode": {"bytes": 1160021, "src_sha": "8d30b576444a97d5"}}
 

@@ -80,7 +80,9 @@ enum {
   GBR_FLAG_FORCE_GEMV = 4,    /* use the small-M tensor-core GEMV kernel when eligible */
   GBR_FLAG_FORCE_TC = 8,      /* use the tcgen05 prefill kernel when eligible */
   GBR_FLAG_UNFUSED = 16,      /* two launches: gate logits, then router_select (A/B only) */
-  GBR_FLAG_NO_SINGLE_CLUSTER = 32 /* small M: skip the single-cluster kernel (A/B only) */
+  GBR_FLAG_NO_SINGLE_CLUSTER = 32, /* small M: skip the single-cluster kernel (A/B only) */
+  GBR_FLAG_TC_NO_STREAMK = 64,    /* prefill: one CTA pair (or CTA) per tile, no stream-K */
+  GBR_FLAG_TC_SINGLE_CTA = 128    /* prefill: single CTAs (M = 128 MMAs) instead of CTA pairs */
 };
 
 /* kernel families reported by router_regime() */
@@ -152,9 +154,9 @@ int router_regime(int M, int H, int E, int k, const gbr_opts* opt);
  * keep every tile within four groups; each group finishes at most one tile
  * after adding the other groups' partial accumulators from the workspace.
  * 0 when every tile gets its own CTA pair (fewer than 256 rows, at least as
- * many tiles as groups, GBR_TC_SK=0 in the environment) or the shape takes
- * another kernel family; -1 for arguments router_forward_ex would reject or
- * a failed device query. Launches nothing. */
+ * many tiles as groups, GBR_FLAG_TC_NO_STREAMK in opt->flags) or the shape
+ * takes another kernel family; -1 for arguments router_forward_ex would
+ * reject or a failed device query. Launches nothing. */
 int router_tc_groups(int M, int H, int E, int k, const gbr_opts* opt);
 
 /*
@@ -208,9 +210,10 @@ int route_table(const int32_t* idx, int groups, int tokens_per_group, int k, int
  * per-stream workspace. This entry point allocates nothing: its scratch (an
  * arrival ticket and FP32 logits [M, E]) is one file-scope device array of
  * 131,328 bytes that every GPU loading the library holds until the process
- * exits. Limits: M <= 64 and E <= 512 (beyond them: GBR_EWORKSPACE), BF16 x
- * and W_gate with E % 16 == 0, H % 32 == 0 and 16-byte aligned x and W_gate
- * (otherwise GBR_EUNSUPPORTED). Other arguments and errors as router_forward.
+ * exits. Limits: M <= 64 (beyond it: GBR_EWORKSPACE); E <= 512 as for every
+ * entry point (beyond it: GBR_EUNSUPPORTED); BF16 x and W_gate with
+ * E % 16 == 0, H % 32 == 0 and 16-byte aligned x and W_gate (otherwise
+ * GBR_EUNSUPPORTED). Other arguments and errors as router_forward.
  * The first call on a device looks up the array's device address, so make
  * that first call before any stream capture. Every call on a device shares
  * the one array: calls that overlap on the GPU (other streams, other host

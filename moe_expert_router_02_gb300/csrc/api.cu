@@ -150,6 +150,7 @@ int router_tc_groups(int M, int H, int E, int k, const gbr_opts* opt) {
   gbr::RouterArgs a{};
   a.M = M, a.H = H, a.E = E, a.k = k, a.act = GBR_ACT_SOFTMAX;
   a.x_dtype = s.x_dtype, a.w_dtype = s.w_dtype;
+  a.flags = s.flags;
   // the launch gets a workspace whenever workspace_for asks for one (a
   // query only tests the pointer for null)
   static uint32_t present;
@@ -191,6 +192,7 @@ int router_forward_ex(const void* x, const void* W_gate, const float* bias, int 
   a.bias = bias;
   a.M = M, a.H = H, a.E = E, a.k = k, a.act = act;
   a.x_dtype = s.x_dtype, a.w_dtype = s.w_dtype;
+  a.flags = s.flags;
   a.out_idx = out_idx;
   a.out_w = out_w;
   a.logits = opt ? opt->out_logits : nullptr;

@@ -20,6 +20,9 @@ namespace {
 
 constexpr int kNoAllocMaxM = 64;
 constexpr int kNoAllocMaxE = 512;
+// every E the library accepts must fit the array (larger E is rejected
+// before this entry point looks at its scratch)
+static_assert(kNoAllocMaxE >= gbr::kMaxE, "static scratch smaller than the largest E");
 constexpr size_t kTicketRegion = 256;  // the arrival ticket, alone in the first 256 bytes
 constexpr size_t kNoAllocBytes = kTicketRegion + (size_t)kNoAllocMaxM * kNoAllocMaxE * 4;
 
@@ -59,7 +62,7 @@ extern "C" int router_forward_noalloc(const void* x, const void* W_gate, const f
     return GBR_EINVAL;
   if (act == GBR_ACT_SOFTMAX && bias) return GBR_EINVAL;
   if (E > gbr::kMaxE || k > gbr::kMaxK) return GBR_EUNSUPPORTED;
-  if (M > kNoAllocMaxM || E > kNoAllocMaxE) return GBR_EWORKSPACE;  // beyond the static scratch
+  if (M > kNoAllocMaxM) return GBR_EWORKSPACE;  // beyond the static scratch
   if (M == 0) return GBR_OK;
   if (!x || !W_gate || !out_idx || !out_w) return GBR_EINVAL;
   if (E % 16 != 0 || H % 32 != 0 || !aligned16(x) || !aligned16(W_gate)) return GBR_EUNSUPPORTED;

@@ -33,11 +33,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <tuple>
 
+#include "../../include/gbrouter.h"
 #include "kernels.h"
 #include "dfkey.cuh"
 #include "select.cuh"
@@ -153,27 +153,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
-}
-
-// TMA load delivered to the same shared-memory offset (and mbarrier offset)
-// in every CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c0,
-                                               int c1, uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
-// Arrive on the mbarrier at this offset in every CTA of cta_mask once the
-// MMAs issued so far by this thread have completed.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
@@ -639,7 +618,6 @@ struct TcParams {
   int stages;
   uint32_t stage_bytes, a_bytes, b_bytes;
   int tmem_cols;
-  int mc;  // CTAs per cluster sharing each W tile through TMA multicast (1 or 2)
   int pair;  // CTA pairs run M = 256 MMAs, each CTA holding half of every W tile
   // NVFP4 only, both in the workspace: W decoded to a BF16 [E, H] copy,
   // and [0] claim counter, [1] epoch, [2 + kb] flag of column block kb
@@ -759,7 +737,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int producer_warp = kEpiWarps, mma_warp = kEpiWarps + 1;
-  const int crank = (PAIR || p.mc > 1) ? (int)cluster_rank() : 0;
+  const int crank = PAIR ? (int)cluster_rank() : 0;
   const int nk = a.H / BK;
   const int E = a.E;
   const int grp = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
@@ -773,7 +751,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), (uint32_t)p.mc);  // one release per CTA using the stage
+      mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(accf), 1);
     mbar_init(smem_u32(accp), 1);
@@ -865,14 +843,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
             }
             asm volatile("fence.proxy.async.global;" ::: "memory");
           }
-          if (p.mc == 1) {
-            tma_load_2d(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, 0, fb, pol_w);
-          } else {
-            // this CTA's share of the W tile, written into every CTA of the pair
-            const int rows = E / p.mc;
-            tma_load_2d_mc(smem_u32(st + p.a_bytes + crank * rows * 128), &tmap_w, kb * BK,
-                           crank * rows, fb, (uint16_t)((1u << p.mc) - 1u));
-          }
+          tma_load_2d(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, 0, fb, pol_w);
         }
       }
       // let copies still in flight land before the CTA can exit (a pair's
@@ -910,8 +881,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
                        accum);
           }
           if (PAIR) mma_commit_pair(smem_u32(&empty[s]));
-          else if (p.mc == 1) mma_commit(smem_u32(&empty[s]));
-          else mma_commit_mc(smem_u32(&empty[s]), (uint16_t)((1u << p.mc) - 1u));
+          else mma_commit(smem_u32(&empty[s]));
         }
         const uint32_t done = smem_u32(plan.fin(sg) ? accf : accp);
         if (PAIR) mma_commit_pair(done);
@@ -1525,7 +1495,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
   __syncthreads();
   // the peer may still signal this CTA's barriers (or read its tensor
   // memory) until it is done as well
-  if (PAIR || p.mc > 1) cluster_sync_tc();
+  if (PAIR) cluster_sync_tc();
   if (warp == mma_warp) {
     tc_fence_after();
     if (PAIR)
@@ -1645,12 +1615,6 @@ int sk_resident_groups(const void* kern, size_t smem, int cl) {
   (void)cudaGetLastError();  // a failed query leaves no sticky error
   if (n > sms / cl) n = sms / cl;
   if (n > kSkMaxCtas / cl) n = kSkMaxCtas / cl;
-  // GBR_TC_SK_GROUPS=n caps the group count (tuning)
-  static const int cap = [] {
-    const char* v = getenv("GBR_TC_SK_GROUPS");
-    return v ? atoi(v) : 0;
-  }();
-  if (cap > 0 && n > cap) n = cap;
   cache[key] = n;
   return n;
 }
@@ -1662,9 +1626,9 @@ cudaError_t launch_kc(const CUtensorMap& mx, const CUtensorMap& mw, const TcPara
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   TcParams p = p0;
-  const int cl = PAIR ? 2 : p.mc;
+  const int cl = PAIR ? 2 : 1;
   int grid = ((p.a.M + BM - 1) / BM + cl - 1) / cl * cl;
-  if (want_sk && p.mc == 1) {
+  if (want_sk) {
     // stream-K when there are fewer tiles than resident groups: the
     // tiles x k-steps units split evenly over as many of them as keep every
     // tile within four groups
@@ -1765,21 +1729,13 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream, int* q
     p.sk_part = sk_ws ? reinterpret_cast<float*>(ws + tc_flag_bytes(a.H)) : nullptr;
     if (fp4) p.wdec = ws + tc_flag_bytes(a.H) + (sk_ws ? tc_part_bytes(a.E) : 0);
   }
-  // stream-K (the default where it applies; GBR_TC_SK=0 turns it off)
-  static const bool sk_env = [] {
-    const char* v = getenv("GBR_TC_SK");
-    return !(v && v[0] == '0');
-  }();
-  const bool want_sk = sk_env && sk_ws;
-  // CTA pairs (the default; GBR_TC_PAIR=0 turns them off): each CTA stages
-  // its 128 rows of x and half of the W tile, and the even CTA issues
-  // M = 256 MMAs for both, so each SM's shared memory carries a third less
-  // traffic per k-step
-  static const bool pair_env = [] {
-    const char* v = getenv("GBR_TC_PAIR");
-    return !(v && v[0] == '0');
-  }();
-  p.pair = pair_env && a.E % 32 == 0;
+  // stream-K where it applies, unless the caller turns it off
+  const bool want_sk = !(a.flags & GBR_FLAG_TC_NO_STREAMK) && sk_ws;
+  // CTA pairs unless the caller asks for single CTAs: each CTA stages its
+  // 128 rows of x and half of the W tile, and the even CTA issues M = 256
+  // MMAs for both, so each SM's shared memory carries a third less traffic
+  // per k-step
+  p.pair = !(a.flags & GBR_FLAG_TC_SINGLE_CTA) && a.E % 32 == 0;
   p.a_bytes = BM * BK * 2;
   p.b_bytes = (uint32_t)(p.pair ? a.E / 2 : a.E) * BK * 2;
   p.stage_bytes = p.a_bytes + p.b_bytes;
@@ -1798,20 +1754,12 @@ cudaError_t launch_tc(const RouterArgs& a, bool pdl, cudaStream_t stream, int* q
     return cudaErrorInvalidValue;
   const size_t smem = (size_t)S * p.stage_bytes + extra;
 
-  // BF16 W can be shared by pairs of CTAs through TMA multicast
-  // (GBR_TC_MULTICAST=1 turns it on). Measured on GB300 it does not speed the
-  // main loop up, which is bound by shared-memory traffic rather than by L2.
-  static const int mc_env = [] {
-    const char* v = getenv("GBR_TC_MULTICAST");
-    return (v && v[0] == '1') ? 2 : 1;
-  }();
-  p.mc = (!fp4 && !p.pair && a.E % 16 == 0) ? mc_env : 1;
   CUtensorMap mx{}, mw{};
   if (!query) {
     if (!make_map(&mx, a.x, a.M, a.H, BM)) return cudaErrorInvalidValue;
     // NVFP4: the kernel decodes W into the workspace as a BF16 [E, H] copy
     if (!make_map(&mw, fp4 ? static_cast<const void*>(p.wdec) : a.w, a.E, a.H,
-                  p.pair ? a.E / 2 : a.E / p.mc))
+                  p.pair ? a.E / 2 : a.E))
       return cudaErrorInvalidValue;
   }
   if (p.pair)

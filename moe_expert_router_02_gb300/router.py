@@ -17,7 +17,8 @@ GBR_OK, GBR_EINVAL, GBR_EUNSUPPORTED, GBR_ECUDA, GBR_EWORKSPACE, GBR_ETIMEOUT = 
 GBR_ACT_SOFTMAX, GBR_ACT_SQRT_SOFTPLUS, GBR_ACT_SIGMOID = 0, 1, 2
 GBR_F32, GBR_BF16, GBR_NVFP4 = 0, 1, 2
 GBR_FLAG_NO_PDL, GBR_FLAG_FORCE_GENERIC, GBR_FLAG_FORCE_GEMV, GBR_FLAG_FORCE_TC, \
-    GBR_FLAG_UNFUSED, GBR_FLAG_NO_SINGLE_CLUSTER = 1, 2, 4, 8, 16, 32
+    GBR_FLAG_UNFUSED, GBR_FLAG_NO_SINGLE_CLUSTER, GBR_FLAG_TC_NO_STREAMK, \
+    GBR_FLAG_TC_SINGLE_CTA = 1, 2, 4, 8, 16, 32, 64, 128
 GBR_REGIME_GENERIC, GBR_REGIME_GEMV, GBR_REGIME_TC, GBR_REGIME_UNFUSED, GBR_REGIME_GEMV1C = \
     0, 1, 2, 3, 4
 

@@ -70,7 +70,7 @@ def test_nvfp4_decode_claims_reset_across_launches():
                             idx, w, opts)
         torch.cuda.synchronize()
         ref = oracle.router(c)
-        check_routes(idx.cpu().numpy(), w.cpu().numpy(), ref["idx"], ref["w"], ref["keys"], c["k"])
+        check_routes(idx.cpu().numpy(), w.cpu().numpy(), ref, c)
 
 
 def test_fused_table():
@@ -93,7 +93,7 @@ def test_full_prefill_sampled_rows(w_dtype):
                                      synth.rng(1).choice(M, 256, replace=False)]))
     sub = dict(case, M=len(rows), x=case["x"][rows])
     ref = oracle.router(sub)
-    check_routes(got["idx"][rows], got["w"][rows], ref["idx"], ref["w"], ref["keys"], k)
+    check_routes(got["idx"][rows], got["w"][rows], ref, sub)
     np.testing.assert_allclose(got["logits"][rows], ref["logits"], rtol=0, atol=1e-4)
     # selection stage on every row, against the oracle fed the kernel's logits
     oi, ow, _ = oracle.select(got["logits"].astype(np.float64), k, case["act"], bias=case["bias"])
@@ -109,20 +109,11 @@ def test_no_timeout_recorded():
 
 
 def test_single_cta_variant():
-    """The prefill kernel runs CTA pairs by default; GBR_TC_PAIR=0 selects
-    the single-CTA form (one CTA stages the whole W tile and issues M = 128
-    MMAs). The setting is read once per process, so a child checks it."""
-    import os
-    import subprocess
-    import sys
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    code = ("from tests.test_prefill_gpu import small_prefill, check_case; "
-            "from moe_expert_router_02_gb300 import router as R, synth; "
-            "check_case(small_prefill(300, seed=31), expect_regime=R.GBR_REGIME_TC); "
-            "check_case(small_prefill(200, E=96, k=6, seed=32)); "
-            "check_case(small_prefill(320, H=1024, seed=33, w_dtype=synth.NVFP4)); "
-            "assert R.router_device_status(clear=True) == R.GBR_OK")
-    env = dict(os.environ, GBR_TC_PAIR="0")
-    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
-                       text=True, timeout=600)
-    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    """The prefill kernel runs CTA pairs by default; GBR_FLAG_TC_SINGLE_CTA
+    selects the single-CTA form (one CTA stages the whole W tile and issues
+    M = 128 MMAs)."""
+    f = R.GBR_FLAG_TC_SINGLE_CTA
+    check_case(small_prefill(300, seed=31), flags=f, expect_regime=R.GBR_REGIME_TC)
+    check_case(small_prefill(200, E=96, k=6, seed=32), flags=f)
+    check_case(small_prefill(320, H=1024, seed=33, w_dtype=synth.NVFP4), flags=f)
+    assert R.router_device_status(clear=True) == R.GBR_OK

@@ -7,8 +7,6 @@ Every case here is checked against the oracle as in the other prefill tests
 (ids, weights, logits, the selection on the kernel's own logits bit-exact,
 the unfused selection bit-identical)."""
 import os
-import subprocess
-import sys
 
 import numpy as np
 import pytest
@@ -114,8 +112,7 @@ def test_epochs_across_launches_and_regimes():
                             c["act"], idx, w, opts)
         torch.cuda.synchronize()
         ref = oracle.router(c)
-        check_routes(idx.cpu().numpy(), w.cpu().numpy(), ref["idx"], ref["w"], ref["keys"],
-                     c["k"])
+        check_routes(idx.cpu().numpy(), w.cpu().numpy(), ref, c)
     assert R.router_device_status(clear=True) == R.GBR_OK
 
 
@@ -140,41 +137,27 @@ def test_graph_replay():
         t["x"].copy_(dev(c2["x"]))
         g.replay()
         torch.cuda.synchronize()
-        ref = oracle.router(dict(c, x=c2["x"]))
-        check_routes(idx.cpu().numpy(), w.cpu().numpy(), ref["idx"], ref["w"], ref["keys"], k)
+        c3 = dict(c, x=c2["x"])
+        check_routes(idx.cpu().numpy(), w.cpu().numpy(), oracle.router(c3), c3)
     assert R.router_device_status(clear=True) == R.GBR_OK
 
 
-def _child(env, code):
-    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
-                       env=dict(os.environ, **env), timeout=900)
-    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    return r.stdout
-
-
 def test_single_cta_groups():
-    """GBR_TC_PAIR=0: one CTA per SM is a group (M = 128 MMAs). Read once per
-    process, so a child checks it."""
-    out = _child({"GBR_TC_PAIR": "0"}, (
-        "from tests.test_prefill_gpu import small_prefill; "
-        "from tests.test_forward_gpu import check_case; "
-        "from tests.test_streamk_gpu import groups; "
-        "from moe_expert_router_02_gb300 import synth; "
-        "c = small_prefill(8192 + 77, H=1024, seed=60); g = groups(c); assert g > 80, g; "
-        "check_case(c); "
-        "c = small_prefill(7000, H=1024, E=48, k=3, seed=61); assert groups(c) > 0; "
-        "check_case(c); print('ok', g)"))
-    assert out.startswith("ok")
+    """GBR_FLAG_TC_SINGLE_CTA: one CTA per SM is a group (M = 128 MMAs)."""
+    f = R.GBR_FLAG_TC_SINGLE_CTA
+    c = small_prefill(8192 + 77, H=1024, seed=60)
+    g = groups(c, flags=f)
+    assert g > 80, g
+    check_case(c, flags=f)
+    c = small_prefill(7000, H=1024, E=48, k=3, seed=61)
+    assert groups(c, flags=f) > 0
+    check_case(c, flags=f)
 
 
-def test_disabled_by_environment():
-    out = _child({"GBR_TC_SK": "0"}, (
-        "from tests.test_prefill_gpu import small_prefill; "
-        "from tests.test_forward_gpu import check_case; "
-        "from tests.test_streamk_gpu import groups; "
-        "c = small_prefill(8192, H=1024, seed=62); assert groups(c) == 0; "
-        "check_case(c); print('ok')"))
-    assert out.startswith("ok")
+def test_disabled_by_flag():
+    c = small_prefill(8192, H=1024, seed=62)
+    assert groups(c, flags=R.GBR_FLAG_TC_NO_STREAMK) == 0
+    check_case(c, flags=R.GBR_FLAG_TC_NO_STREAMK)
 
 
 def test_bitwise_repeatable():
