@@ -234,6 +234,50 @@ def tie_rows_sqrt_softplus(n: int, E: int, k: int, seed: int, std: float = 1.0):
     return rows, bias, kinds
 
 
+def tie_rows_softmax_bias(n: int, E: int, k: int, seed: int, std: float = 1.0):
+    """Logit rows plus a per-row bias for the softmax-probability + bias key,
+    with constructed exact and near ties at the k / k+1 boundary.
+
+    Returns (rows [n, E] float32, bias [n, E] float32, kinds). Placement (no
+    arithmetic of the key): the bulk is N(0, std) clipped to [-4 std, 4 std]
+    with bias U(-0.05, -0.02); the boundary pair (i, j) sits at logit
+    v = 4 std + 1 with a common bias b0 ~ U(0.005, 0.015); k-1 top experts
+    sit at logits v + 3 + t with bias U(0.04, 0.05). Every top expert's
+    probability is then at least e^3 times the pair's and every bulk
+    expert's at most 1/e of it, so the pair holds ranks k and k+1 whatever
+    the row's denominator. Kinds: equal logit and bias (exact key tie),
+    logit one ulp apart, bias one ulp apart.
+    """
+    gen = rng(seed)
+    rows = np.clip(normal(gen, (n, E), std), -4 * std, 4 * std).astype(np.float32)
+    bias = gen.uniform(-0.05, -0.02, size=(n, E)).astype(np.float32)
+    kinds_all = ("exact", "near_logit_up", "near_logit_down", "near_bias_up", "near_bias_down")
+    kinds = []
+    for r in range(n):
+        kind = kinds_all[r % len(kinds_all)]
+        kinds.append(kind)
+        if k + 1 > E:
+            continue
+        perm = gen.permutation(E)
+        top, (i, j) = perm[: k - 1], perm[k - 1: k + 1]
+        v = np.float32(4 * std + 1.0)
+        for t, e in enumerate(top):
+            rows[r, e] = np.float32(v + 3.0 + 1.0 * t + gen.uniform(0, 0.1))
+            bias[r, e] = np.float32(gen.uniform(0.04, 0.05))
+        b0 = np.float32(gen.uniform(0.005, 0.015))
+        rows[r, i] = rows[r, j] = v
+        bias[r, i] = bias[r, j] = b0
+        if kind == "near_logit_up":
+            rows[r, j] = np.nextafter(v, np.float32(np.inf))
+        elif kind == "near_logit_down":
+            rows[r, j] = np.nextafter(v, np.float32(-np.inf))
+        elif kind == "near_bias_up":
+            bias[r, j] = np.nextafter(b0, np.float32(np.inf))
+        elif kind == "near_bias_down":
+            bias[r, j] = np.nextafter(b0, np.float32(-np.inf))
+    return rows, bias, kinds
+
+
 def inject_tie_rows(rows: np.ndarray, frac: float, k: int, seed: int) -> np.ndarray:
     """Replace a fraction of logit rows with constructed boundary-tie rows
     (same E, same scale)."""

@@ -23,7 +23,7 @@ _lock = threading.Lock()
 _lib = None
 
 F32, BF16, NVFP4 = 0, 1, 2
-SOFTMAX, SQRT_SOFTPLUS = 0, 1
+SOFTMAX, SQRT_SOFTPLUS, SIGMOID = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -49,11 +49,12 @@ def lib():
             L.orc_sigmoid.argtypes, L.orc_sigmoid.restype = [D], D
             L.orc_logits.argtypes = [P, I, P, I, P, D, I, I, I, P]
             L.orc_select.argtypes = [P, P, I, I, I, I, I, P, P, P]
+            L.orc_keys.argtypes = [P, P, I, I, I, I, P, P]
             L.orc_select_by_prob.argtypes = [P, I, I, I, P]
             L.orc_route_table.argtypes = [P, I, I, I, P, P, P, P]
             L.orc_gather_add.argtypes = [P, P, P, P, I, I, I, I, P]
-            for f in (L.orc_logits, L.orc_select, L.orc_select_by_prob, L.orc_route_table,
-                      L.orc_gather_add):
+            for f in (L.orc_logits, L.orc_select, L.orc_keys, L.orc_select_by_prob,
+                      L.orc_route_table, L.orc_gather_add):
                 f.restype = I
             _lib = L
     return _lib
@@ -113,6 +114,22 @@ def select(lg, k, act, bias=None):
     return idx, w, keys
 
 
+def keys(lg, act, bias=None):
+    """Every expert's selection key and weight score, ``(key [M, E], score
+    [M, E])`` float64, as :func:`select` ranks and weights them."""
+    lg = np.ascontiguousarray(lg, dtype=np.float64)
+    M, E = lg.shape
+    per_row = 0
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+        per_row = 1 if bias.ndim == 2 else 0
+    key = np.empty((M, E), dtype=np.float64)
+    score = np.empty((M, E), dtype=np.float64)
+    if lib().orc_keys(_p(lg), _p(bias), per_row, M, E, act, _p(key), _p(score)) != 0:
+        raise ValueError("oracle: bad keys arguments")
+    return key, score
+
+
 def select_by_prob(lg, k):
     lg = np.ascontiguousarray(lg, dtype=np.float64)
     M, E = lg.shape
@@ -162,12 +179,13 @@ def router(case: dict):
     """Whole router on one synthetic case from ``synth.make_case``.
 
     Returns dict with logits (FP64), idx, w, keys (first k+1 sorted keys)
-    and, when the case asks for it, the M=2 route table.
+    and, when the case asks for it, the M=2 route table. ``keys(...)`` of the
+    returned logits gives every expert's key and score.
     """
     lg = logits(case["x"], case["x_dtype"], case["W"], case["w_dtype"], case["M"], case["H"],
                 case["E"], scales=case.get("scales"), g=case.get("g", 1.0))
-    idx, w, keys = select(lg, case["k"], case["act"], case.get("bias"))
-    out = dict(logits=lg, idx=idx, w=w, keys=keys)
+    idx, w, skeys = select(lg, case["k"], case["act"], case.get("bias"))
+    out = dict(logits=lg, idx=idx, w=w, keys=skeys)
     if case.get("table"):
         M, k = case["M"], case["k"]
         out["table"] = route_table(idx.reshape(M // 2, 2, k))

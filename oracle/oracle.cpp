@@ -18,7 +18,10 @@
 //       (commit page, "Numerically stable softplus"; the bias only selects,
 //       the heap keeps "(score, index, unbiased act)"); or a = sigmoid(l) =
 //       1 / (1 + exp(-l)) with key = a + bias in the same way (the same
-//       biased-score contract with the sigmoid as the score).
+//       biased-score contract with the sigmoid as the score). With a bias,
+//       softmax follows that contract too: key = p + bias with p the full-E
+//       softmax probability, weights the unbiased p renormalised (qwisp issue
+//       #145, "Gates": the bias variant of the softmax route kernel).
 //   * top-k            full stable sort of all E experts by (key desc, index
 //       asc): equal keys keep the lower expert index first
 //       (qwisp issue #145, "Bit-exactness": the tie-break order is part of
@@ -33,10 +36,11 @@
 //       (b70 lab note, "Unique-route router screen": encounter-ordered
 //       unique experts, per-expert token masks, slot-to-unique map, count).
 //
-// Readings where the pages are silent: the softmax selection key is the
-// logit (softmax is strictly increasing, so the order is the same and FP64
-// probabilities cannot collapse two distinct logits into a false tie); -0.0
-// and +0.0 compare equal; if every chosen score is zero the weights are 1/k.
+// Readings where the pages are silent: without a bias the softmax selection
+// key is the logit (softmax is strictly increasing, so the order is the same
+// and FP64 probabilities cannot collapse two distinct logits into a false
+// tie); with a bias it is the FP64 probability plus the bias; -0.0 and +0.0
+// compare equal; if every chosen score is zero the weights are 1/k.
 
 #include <algorithm>
 #include <cmath>
@@ -122,36 +126,46 @@ int orc_logits(const void* x, int x_dtype, const void* W, int w_dtype,
   return 0;
 }
 
+// The selection key and the weight score of every expert of one row of
+// FP64 logits l[E] (b: that row's FP32 bias, or null).
+//   softmax, no bias  score = exp(l - max) / sum_e exp(l_e - max), key = l
+//   softmax, bias     score as above,                             key = score + b
+//   sqrt-softplus     score = sqrt(max(l,0) + log1p(exp(-|l|))),   key = score + b
+//   sigmoid           score = 1 / (1 + exp(-l)),                   key = score + b
+static void row_keys(const double* l, const float* b, int E, int act, double* key,
+                     double* score) {
+  if (act == kSoftmax) {
+    double mx = l[0];
+    for (int e = 1; e < E; ++e) mx = std::max(mx, l[e]);
+    double z = 0.0;
+    for (int e = 0; e < E; ++e) z += std::exp(l[e] - mx);
+    for (int e = 0; e < E; ++e) {
+      score[e] = std::exp(l[e] - mx) / z;
+      key[e] = b ? score[e] + static_cast<double>(b[e]) : l[e];
+    }
+  } else {
+    for (int e = 0; e < E; ++e) {
+      score[e] = act == kSigmoid ? sigmoid(l[e]) : sqrt_softplus(l[e]);
+      key[e] = score[e] + (b ? static_cast<double>(b[e]) : 0.0);
+    }
+  }
+}
+
 // Selection + renormalisation on FP64 logits [M, E].
-//   bias: nullable FP32 [E] (sqrt-softplus only), or per-row [M, E] when
-//         bias_per_row != 0 (used by the adversarial tests).
+//   bias: nullable FP32 [E], or per-row [M, E] when bias_per_row != 0 (used
+//         by the adversarial tests).
 //   out_idx [M,k], out_w [M,k]; out_keys (nullable) [M, kk] receives the
 //   first kk = min(k+1, E) keys in sorted order (for the gap rule).
 int orc_select(const double* logits, const float* bias, int bias_per_row, int M, int E,
                int k, int act, int32_t* out_idx, double* out_w, double* out_keys) {
   if (k < 1 || k > E || (act != kSoftmax && act != kSqrtSoftplus && act != kSigmoid)) return -1;
-  if (act == kSoftmax && bias) return -1;
   const int kk = std::min(k + 1, E);
   std::vector<double> key(E), score(E);
   std::vector<int> order(E);
   for (int m = 0; m < M; ++m) {
     const double* l = logits + (size_t)m * E;
     const float* b = bias ? (bias_per_row ? bias + (size_t)m * E : bias) : nullptr;
-    if (act == kSoftmax) {
-      double mx = l[0];
-      for (int e = 1; e < E; ++e) mx = std::max(mx, l[e]);
-      double z = 0.0;
-      for (int e = 0; e < E; ++e) z += std::exp(l[e] - mx);
-      for (int e = 0; e < E; ++e) {
-        score[e] = std::exp(l[e] - mx) / z;
-        key[e] = l[e];
-      }
-    } else {
-      for (int e = 0; e < E; ++e) {
-        score[e] = act == kSigmoid ? sigmoid(l[e]) : sqrt_softplus(l[e]);
-        key[e] = score[e] + (b ? static_cast<double>(b[e]) : 0.0);
-      }
-    }
+    row_keys(l, b, E, act, key.data(), score.data());
     for (int e = 0; e < E; ++e) order[e] = e;
     std::stable_sort(order.begin(), order.end(),
                      [&](int a, int c) { return key[a] > key[c]; });
@@ -163,6 +177,19 @@ int orc_select(const double* logits, const float* bias, int bias_per_row, int M,
     }
     if (out_keys)
       for (int j = 0; j < kk; ++j) out_keys[(size_t)m * kk + j] = key[order[j]];
+  }
+  return 0;
+}
+
+// Every expert's key and score ([M, E] each), as orc_select ranks and
+// weights them; used to judge rows whose order is decided within rounding.
+int orc_keys(const double* logits, const float* bias, int bias_per_row, int M, int E, int act,
+             double* out_key, double* out_score) {
+  if (E < 1 || (act != kSoftmax && act != kSqrtSoftplus && act != kSigmoid)) return -1;
+  for (int m = 0; m < M; ++m) {
+    const float* b = bias ? (bias_per_row ? bias + (size_t)m * E : bias) : nullptr;
+    row_keys(logits + (size_t)m * E, b, E, act, out_key + (size_t)m * E,
+             out_score + (size_t)m * E);
   }
   return 0;
 }

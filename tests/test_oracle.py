@@ -214,6 +214,84 @@ def test_constructed_sqrt_softplus_bias_rows_against_decimal_brute_force():
             assert w[r, j] == pytest.approx(float(a[e] / tot), rel=1e-14)
 
 
+def _dec_softmax(row):
+    """Full-E softmax of one row in 60-digit decimal."""
+    with decimal.localcontext() as c:
+        c.prec = 60
+        ex = [decimal.Decimal(float(z)).exp() for z in row]
+        tot = sum(ex)
+        return [v / tot for v in ex]
+
+
+@pytest.mark.parametrize("E,k", [(12, 3), (9, 1), (16, 8)])
+def test_constructed_softmax_bias_rows_against_decimal_brute_force(E, k):
+    # key = the softmax probability + the bias, found by enumerating every
+    # ordered k-tuple in 60-digit decimal; weights the unbiased probabilities
+    # renormalised over the chosen k
+    rows, bias, kinds = synth.tie_rows_softmax_bias(25, E, k, seed=E + k)
+    idx, w, _ = oracle.select(rows.astype(np.float64), k, synth.SOFTMAX, bias=bias)
+    for r in range(len(rows)):
+        p = _dec_softmax(rows[r])
+        keys = [p[e] + decimal.Decimal(float(bias[r, e])) for e in range(E)]
+        if k <= 3:
+            assert list(idx[r]) == _brute_topk(keys, k), kinds[r]
+        else:  # the same order by sorting (key desc, index asc) in decimal
+            assert list(idx[r]) == sorted(range(E), key=lambda e: (-keys[e], e))[:k], kinds[r]
+        tot = sum(p[e] for e in idx[r])
+        for j, e in enumerate(idx[r]):
+            assert w[r, j] == pytest.approx(float(p[e] / tot), rel=1e-14)
+
+
+def test_softmax_bias_random_rows_against_decimal():
+    gen = synth.rng(17)
+    E, k = 10, 3
+    lg = gen.normal(size=(40, E)) * 1.5
+    bias = gen.uniform(-0.05, 0.05, size=(40, E)).astype(np.float32)
+    idx, w, keys = oracle.select(lg, k, synth.SOFTMAX, bias=bias)
+    kfull, score = oracle.keys(lg, synth.SOFTMAX, bias=bias)
+    for r in range(len(lg)):
+        p = _dec_softmax(lg[r])
+        dk = [p[e] + decimal.Decimal(float(bias[r, e])) for e in range(E)]
+        assert list(idx[r]) == _brute_topk(dk, k)
+        for e in range(E):  # every expert's key and score
+            assert kfull[r, e] == pytest.approx(float(dk[e]), rel=0, abs=5e-16)
+            assert score[r, e] == pytest.approx(float(p[e]), rel=1e-14)
+        np.testing.assert_array_equal(keys[r], kfull[r][np.concatenate([idx[r], [
+            sorted(range(E), key=lambda e: (-dk[e], e))[k]]])])
+
+
+def test_softmax_bias_flips_the_order_but_not_the_weights():
+    # expert 1 has the larger probability; expert 0 wins through its bias
+    lg = np.array([[1.0, 1.2, -5.0, -5.0]])
+    bias = np.array([0.1, 0.0, 0.0, 0.0], dtype=np.float32)
+    idx, w, _ = oracle.select(lg, 2, synth.SOFTMAX, bias=bias)
+    assert list(idx[0]) == [0, 1]
+    np.testing.assert_allclose(w[0], [math.exp(1.0) / (math.exp(1.0) + math.exp(1.2)),
+                                      math.exp(1.2) / (math.exp(1.0) + math.exp(1.2))],
+                               rtol=1e-14)
+    # a zero bias ranks by probability, the order of the logits
+    gen = synth.rng(23)
+    lg = gen.normal(size=(200, 32))
+    a, _, _ = oracle.select(lg, 4, synth.SOFTMAX)
+    b, _, _ = oracle.select(lg, 4, synth.SOFTMAX, bias=np.zeros(32, dtype=np.float32))
+    assert np.array_equal(a, b)
+
+
+def test_keys_agree_with_select_for_every_activation():
+    gen = synth.rng(29)
+    lg = gen.normal(size=(50, 64))
+    for act, bias in ((synth.SOFTMAX, None), (synth.SOFTMAX, synth.make_bias(64, 3)),
+                      (synth.SQRT_SOFTPLUS, synth.make_bias(64, 4)),
+                      (synth.SIGMOID, None)):
+        idx, w, skeys = oracle.select(lg, 6, act, bias=bias)
+        key, score = oracle.keys(lg, act, bias=bias)
+        # the sorted keys are the keys of the chosen experts, then the next
+        np.testing.assert_array_equal(np.take_along_axis(key, idx.astype(np.int64), 1),
+                                      skeys[:, :6])
+        sc = np.take_along_axis(score, idx.astype(np.int64), 1)
+        np.testing.assert_allclose(w, sc / sc.sum(axis=1, keepdims=True), rtol=1e-14)
+
+
 def test_bias_selects_but_does_not_weight():
     # Expert 1 has the larger activation but expert 0 wins through its bias;
     # the weights are the unbiased activations renormalised.
@@ -229,6 +307,7 @@ def test_renormalisation_invariants():
     gen = synth.rng(9)
     lg = gen.normal(size=(300, 256)) * 0.9
     for act, bias in ((synth.SOFTMAX, None),
+                      (synth.SOFTMAX, synth.make_bias(256, 3)),
                       (synth.SQRT_SOFTPLUS, synth.make_bias(256, 1)),
                       (synth.SIGMOID, synth.make_bias(256, 2))):
         idx, w, keys = oracle.select(lg, 8, act, bias=bias)
@@ -236,7 +315,7 @@ def test_renormalisation_invariants():
         assert all(len(set(r)) == 8 for r in idx)
         assert idx.min() >= 0 and idx.max() < 256
         assert np.all(np.diff(keys, axis=1) <= 0)
-        if act == synth.SOFTMAX:
+        if act == synth.SOFTMAX and bias is None:
             assert np.all(np.diff(w, axis=1) <= 0)
 
 
