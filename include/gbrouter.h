@@ -9,12 +9,14 @@
  *      postNorm", logits held on chip instead of round-tripping);
  *   2. the score: softmax over E, or a = sqrt(softplus(logit)) with the
  *      stable softplus max(z,0) + log1p(exp(-|z|)), or a = sigmoid(logit) =
- *      1 / (1 + exp(-logit)); with the last two a per-expert bias is added
- *      for selection only
+ *      1 / (1 + exp(-logit)); a per-expert bias, when given, is added to the
+ *      score for selection only (softmax: to the full-E probability; without
+ *      a bias the softmax key is the logit, which orders alike)
  *      (dense_router_decode commit page, "DenseRouterDecodeKernel: BF16 GEMM
  *      + sqrt(softplus) + bias + top-k", "Numerically stable softplus", heap
- *      of "(score, index, unbiased act)"; the sigmoid score is this
- *      library's widening of the same biased-score contract);
+ *      of "(score, index, unbiased act)"; qwisp issue #145, "Gates": the bias
+ *      variant of the softmax route; the sigmoid score and the softmax bias
+ *      are this library's widening of the same biased-score contract);
  *   3. top-k under the fixed comparison: higher key first, an equal key goes
  *      to the lower expert index; slots are returned in that order
  *      (qwisp issue #145, "Bit-exactness": the tie-break order is part of
@@ -116,14 +118,16 @@ typedef struct {
 
 /*
  * router_forward — steps 1-4 in one launch, BF16 x [M, H] and BF16
- * W_gate [E, H], FP32 bias [E] (nullable; sqrt-softplus only).
+ * W_gate [E, H], FP32 bias [E] (nullable; selection only, every
+ * activation). Softmax with a bias at M > 64 runs the generic kernel (the
+ * prefill kernel's epilogue does not take the probability key).
  * Outputs: out_idx int32 [M, k] (expert ids in slot order), out_w FP32
  * [M, k]. Uses a library-owned workspace for (current device, stream),
  * allocated and zero-filled on first use (call once before capturing the
  * stream into a CUDA graph). Thread-safe.
  * Errors: GBR_EINVAL for null required pointers, M < 0, H < 1, E < 1,
- * k < 1, k > E, act outside the enum, bias with softmax; GBR_EUNSUPPORTED
- * for E > 512 or k > 16; GBR_ECUDA if allocation or launch fails.
+ * k < 1, k > E, act outside the enum; GBR_EUNSUPPORTED for E > 512 or
+ * k > 16; GBR_ECUDA if allocation or launch fails.
  */
 int router_forward(const void* x, const void* W_gate, const float* bias, int M, int H, int E,
                    int k, int act, int32_t* out_idx, float* out_w, cudaStream_t stream);
@@ -144,8 +148,9 @@ int router_forward_ex(const void* x, const void* W_gate, const float* bias, int 
 /* Bytes of workspace router_forward_ex needs for this shape (0 if none). */
 size_t router_workspace_size(int M, int H, int E, int k, const gbr_opts* opt);
 
-/* Which kernel family router_forward_ex would launch (GBR_REGIME_*), or -1
- * for arguments it would reject. */
+/* Which kernel family router_forward_ex would launch (GBR_REGIME_*) for a
+ * call without a bias or with a non-softmax activation, or -1 for arguments
+ * it would reject. */
 int router_regime(int M, int H, int E, int k, const gbr_opts* opt);
 
 /* Stream-K work groups the prefill kernel (GBR_REGIME_TC) would split this
@@ -161,7 +166,7 @@ int router_tc_groups(int M, int H, int E, int k, const gbr_opts* opt);
 
 /*
  * router_select — steps 2-4 alone, on caller FP32 logits [M, E]; bias
- * nullable FP32 [E] (sqrt-softplus only). The same selection code the fused
+ * nullable FP32 [E] (every activation). The same selection code the fused
  * kernels run; it exists so the selection stage can be checked on identical
  * FP32 logits (qwisp issue #145, "Gates", G-A: synthetic logits with exact
  * and near ties at the top-k boundary). Errors as router_forward.

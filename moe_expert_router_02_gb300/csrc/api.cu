@@ -26,7 +26,6 @@ int check_shape(const Shape& s) {
   if (s.M < 0 || s.H < 1 || s.E < 1 || s.k < 1 || s.k > s.E) return GBR_EINVAL;
   if (s.act != GBR_ACT_SOFTMAX && s.act != GBR_ACT_SQRT_SOFTPLUS && s.act != GBR_ACT_SIGMOID)
     return GBR_EINVAL;
-  if (s.act == GBR_ACT_SOFTMAX && s.has_bias) return GBR_EINVAL;
   if (s.x_dtype != GBR_F32 && s.x_dtype != GBR_BF16) return GBR_EINVAL;
   if (s.w_dtype != GBR_F32 && s.w_dtype != GBR_BF16 && s.w_dtype != GBR_NVFP4) return GBR_EINVAL;
   if (s.w_dtype == GBR_NVFP4 && (s.H % 16 != 0 || !s.has_scales)) return GBR_EINVAL;
@@ -43,7 +42,10 @@ bool gemv_eligible(const Shape& s) {
 int regime_of(const Shape& s) {
   const int f = s.flags;
   if (f & GBR_FLAG_FORCE_GENERIC) return GBR_REGIME_GENERIC;
-  const bool tc = gbr::tc_eligible(s.M, s.H, s.E, s.k, s.x_dtype, s.w_dtype);
+  // softmax with a selection bias: not in the prefill kernel's epilogue (the
+  // generic kernel serves those shapes)
+  const bool tc = gbr::tc_eligible(s.M, s.H, s.E, s.k, s.x_dtype, s.w_dtype) &&
+                  !(s.act == GBR_ACT_SOFTMAX && s.has_bias);
   const bool gv = gemv_eligible(s);
   if (f & GBR_FLAG_UNFUSED) return gv ? GBR_REGIME_UNFUSED : GBR_REGIME_GENERIC;
   if ((f & GBR_FLAG_FORCE_TC) && tc) return GBR_REGIME_TC;
@@ -190,7 +192,7 @@ int router_forward_ex(const void* x, const void* W_gate, const float* bias, int 
   a.w_scales = opt ? opt->w_scales : nullptr;
   a.w_global = opt ? opt->w_global_scale : 1.0f;
   a.bias = bias;
-  a.M = M, a.H = H, a.E = E, a.k = k, a.act = act;
+  a.M = M, a.H = H, a.E = E, a.k = k, a.act = gbr::internal_act(act, bias);
   a.x_dtype = s.x_dtype, a.w_dtype = s.w_dtype;
   a.flags = s.flags;
   a.out_idx = out_idx;
@@ -231,7 +233,7 @@ int router_forward_ex(const void* x, const void* W_gate, const float* bias, int 
       if (!a.logits) a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + kTicketBytes);
       err = gbr::launch_gemv(a, false, pdl, stream);
       if (err == cudaSuccess)
-        err = gbr::launch_select(a.logits, bias, M, E, k, act, out_idx, out_w, stream);
+        err = gbr::launch_select(a.logits, bias, M, E, k, a.act, out_idx, out_w, stream);
       if (err == cudaSuccess && s.table)
         err = gbr::launch_route_table(out_idx, M / 2, 2, k, a.tbl_unique, a.tbl_mask, a.tbl_map,
                                       a.tbl_count, stream);
@@ -258,11 +260,11 @@ int router_select(const float* logits, const float* bias, int M, int E, int k, i
   if (M < 0 || E < 1 || k < 1 || k > E) return GBR_EINVAL;
   if (act != GBR_ACT_SOFTMAX && act != GBR_ACT_SQRT_SOFTPLUS && act != GBR_ACT_SIGMOID)
     return GBR_EINVAL;
-  if (act == GBR_ACT_SOFTMAX && bias) return GBR_EINVAL;
   if (E > gbr::kMaxE || k > gbr::kMaxK) return GBR_EUNSUPPORTED;
   if (M == 0) return GBR_OK;
   if (!logits || !out_idx || !out_w) return GBR_EINVAL;
-  return gbr::launch_select(logits, bias, M, E, k, act, out_idx, out_w, stream) == cudaSuccess
+  return gbr::launch_select(logits, bias, M, E, k, gbr::internal_act(act, bias), out_idx, out_w,
+                            stream) == cudaSuccess
              ? GBR_OK
              : GBR_ECUDA;
 }

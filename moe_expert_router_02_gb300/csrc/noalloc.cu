@@ -60,7 +60,6 @@ extern "C" int router_forward_noalloc(const void* x, const void* W_gate, const f
   if (M < 0 || H < 1 || E < 1 || k < 1 || k > E) return GBR_EINVAL;
   if (act != GBR_ACT_SOFTMAX && act != GBR_ACT_SQRT_SOFTPLUS && act != GBR_ACT_SIGMOID)
     return GBR_EINVAL;
-  if (act == GBR_ACT_SOFTMAX && bias) return GBR_EINVAL;
   if (E > gbr::kMaxE || k > gbr::kMaxK) return GBR_EUNSUPPORTED;
   if (M > kNoAllocMaxM) return GBR_EWORKSPACE;  // beyond the static scratch
   if (M == 0) return GBR_OK;
@@ -78,7 +77,7 @@ extern "C" int router_forward_noalloc(const void* x, const void* W_gate, const f
   a.w = W_gate;
   a.w_global = 1.0f;
   a.bias = bias;
-  a.M = M, a.H = H, a.E = E, a.k = k, a.act = act;
+  a.M = M, a.H = H, a.E = E, a.k = k, a.act = gbr::internal_act(act, bias);
   a.x_dtype = gbr::DT_BF16, a.w_dtype = gbr::DT_BF16;
   a.out_idx = out_idx;
   a.out_w = out_w;

@@ -11,6 +11,10 @@
 //                 the weights use the unbiased a: w_j = a_j / sum_i a_i.
 //   sigmoid       a = 1 / (1 + exp(-z)), key = a + bias, weights as above
 //                 (the biased sigmoid score of the same page's routing).
+//   softmax+bias  p = exp(z - max) / sum_e exp(z_e - max) over all E,
+//                 key = p + bias, weights the unbiased p renormalised (the
+//                 bias variant of the softmax route, qwisp issue #145,
+//                 "Gates"); near ties are re-ranked with FP64 keys.
 // Order (qwisp issue #145, "Bit-exactness"): higher key first, an equal key
 // goes to the lower expert index; -0.0 equals +0.0.
 //
@@ -58,21 +62,11 @@ __device__ __forceinline__ void sort_desc(uint64_t (&v)[VPL]) {
   }
 }
 
-// The FP64 re-ranking of the candidates in cmask (k rounds of
-// (key desc, index asc)); returns this lane's pick (lane < k). Out of line:
-// FP64 is slow on this part and must not be issued on the common path.
-template <int VPL, class Ld>
-__device__ __noinline__ int select_fp64(const Ld ld, const float* __restrict__ bias, int act, int k,
-                                        uint32_t cmask) {
+// k rounds of (key desc, index asc) over the FP64 keys of the candidates in
+// cmask (lane + 32 j holds k64[j]); returns this lane's pick (lane < k).
+template <int VPL>
+__device__ __forceinline__ int fp64_rounds(const double (&k64)[VPL], uint32_t cmask, int k) {
   const int lane = threadIdx.x & 31;
-  double k64[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int e = lane + 32 * j;
-    k64[j] = 0.0;
-    if ((cmask >> j) & 1u)
-      k64[j] = act_f64(act, (double)ld(e)) + (bias ? (double)__ldg(bias + e) : 0.0);
-  }
   int pick = -1;
   for (int r = 0; r < k; ++r) {
     double bv = -INFINITY;
@@ -97,6 +91,74 @@ __device__ __noinline__ int select_fp64(const Ld ld, const float* __restrict__ b
     if (lane == r) pick = bidx;
   }
   return pick;
+}
+
+// The FP64 re-ranking of the candidates in cmask (k rounds of
+// (key desc, index asc)); returns this lane's pick (lane < k). Out of line:
+// FP64 is slow on this part and must not be issued on the common path.
+template <int VPL, class Ld>
+__device__ __noinline__ int select_fp64(const Ld ld, const float* __restrict__ bias, int act, int k,
+                                        uint32_t cmask) {
+  const int lane = threadIdx.x & 31;
+  double k64[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    k64[j] = 0.0;
+    if ((cmask >> j) & 1u)
+      k64[j] = act_f64(act, (double)ld(e)) + (bias ? (double)__ldg(bias + e) : 0.0);
+  }
+  return fp64_rounds<VPL>(k64, cmask, k);
+}
+
+// Softmax probability + bias in FP64 for the candidates in cmask: the row's
+// FP64 denominator over all E experts (relative to the row maximum zmax),
+// then the rounds. Every lane ends the butterfly with the same sum.
+template <int VPL, class Ld>
+__device__ __noinline__ int select_softmax_bias_fp64(const Ld ld, const float* __restrict__ bias,
+                                                     int E, int k, float zmax, uint32_t cmask) {
+  const int lane = threadIdx.x & 31;
+  double ex[VPL];
+  double part = 0.0;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    ex[j] = 0.0;
+    if (e < E) {
+      ex[j] = exp((double)ld(e) - (double)zmax);
+      part += ex[j];
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+  double k64[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    k64[j] = ((cmask >> j) & 1u) ? ex[j] / part + (double)__ldg(bias + e) : 0.0;
+  }
+  return fp64_rounds<VPL>(k64, cmask, k);
+}
+
+// FP32 softmax-probability + bias key of one expert, given the row maximum
+// and the FP32 denominator (the main pass and the near-tie candidate mask
+// compute it the same way).
+__device__ __forceinline__ float softmax_bias_key32(float z, float zmax, float zsum, float b) {
+  return __fadd_rn(__fdiv_rn(expf(__fsub_rn(z, zmax)), zsum), b);
+}
+
+// Bound on |key32 - key| for the softmax-probability + bias key, u = 2^-24:
+// z - max rounds to d (1 + u), expf adds at most 2 ulp (4u), the FP32
+// denominator sums each term through at most VPL - 1 + 5 roundings, the
+// division and the bias add one rounding each. With pmax the row's largest
+// FP32 probability, s1z = sum_e e^d |d| / Z (the exp argument's error
+// carried into the denominator) and p |d| <= 1 / (e Z):
+//   |key32 - key| <= u ((VPL + 14 + 1.01 s1z) pmax + 0.37 / Z + |key|max).
+__device__ __forceinline__ float softmax_bias_err_bound(int vpl, float pmax, float s1z, float zsum,
+                                                        float kabs) {
+  const float c = __fadd_ru((float)(vpl + 14), __fmul_ru(1.01f, s1z));
+  const float t = __fadd_ru(__fmaf_ru(c, pmax, __fdiv_ru(0.37f, zsum)), kabs);
+  return __fadd_ru(__fmul_ru(t, 0x1p-24f), 0x1p-60f);
 }
 
 // The near-tie re-ranking of one row (all lanes call): every expert whose
@@ -212,20 +274,65 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
   const int lane = threadIdx.x & 31;
   uint64_t pk[VPL];  // (key << 32) | (0xffffffff - expert); 0 = empty
   float amax = 0.0f, kabs = 0.0f;
+  // softmax + bias: the row maximum, the FP32 denominator and the bound term
+  float zmax = 0.0f, zsum = 1.0f, s1z = 0.0f;
+  if (act == ACT_SOFTMAX_BIAS) {
+    float zv[VPL], ev[VPL];
+    uint32_t mo = 0u;
 #pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int e = lane + 32 * j;
-    pk[j] = 0ull;
-    if (e < E) {
-      const float z = ld(e);
-      float key = z;
-      if (act != ACT_SOFTMAX) {
-        const float a = act_f32(act, z);
-        key = bias ? a + __ldg(bias + e) : a;
-        amax = fmaxf(amax, a);
-        kabs = fmaxf(kabs, fabsf(key));
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane + 32 * j;
+      zv[j] = e < E ? ld(e) : 0.0f;
+      if (e < E) mo = max(mo, ord_of(zv[j]));
+    }
+    zmax = float_of_ord(__reduce_max_sync(kFull, mo));
+    float zs = 0.0f, s1 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane + 32 * j;
+      ev[j] = 0.0f;
+      if (e < E) {
+        const float d = __fsub_rn(zv[j], zmax);
+        ev[j] = expf(d);
+        zs = __fadd_rn(zs, ev[j]);
+        s1 = __fmaf_rn(ev[j], -d, s1);
       }
-      pk[j] = ((uint64_t)ord_of(key) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      zs = __fadd_rn(zs, __shfl_xor_sync(kFull, zs, off));
+      s1 = __fadd_rn(s1, __shfl_xor_sync(kFull, s1, off));
+    }
+    zsum = zs;  // >= 1: the maximum's term is exp(0)
+    s1z = __fdiv_ru(s1, zs);
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane + 32 * j;
+      pk[j] = 0ull;
+      if (e < E) {
+        const float p = __fdiv_rn(ev[j], zsum);
+        const float key = __fadd_rn(p, __ldg(bias + e));  // as softmax_bias_key32
+        amax = fmaxf(amax, p);
+        kabs = fmaxf(kabs, fabsf(key));
+        pk[j] = ((uint64_t)ord_of(key) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane + 32 * j;
+      pk[j] = 0ull;
+      if (e < E) {
+        const float z = ld(e);
+        float key = z;
+        if (act != ACT_SOFTMAX) {
+          const float a = act_f32(act, z);
+          key = bias ? a + __ldg(bias + e) : a;
+          amax = fmaxf(amax, a);
+          kabs = fmaxf(kabs, fabsf(key));
+        }
+        pk[j] = ((uint64_t)ord_of(key) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+      }
     }
   }
   sort_desc<VPL>(pk);
@@ -254,12 +361,29 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
     // FP32 key error bound; non-negative floats order like their bit patterns
     const float amax_w = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(amax)));
     const float kabs_w = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(kabs)));
-    const float band = 4.0f * key_err_bound(amax_w, kabs_w, act_err_coef(act));
+    const float band = 4.0f * (act == ACT_SOFTMAX_BIAS
+                                   ? softmax_bias_err_bound(VPL, amax_w, s1z, zsum, kabs_w)
+                                   : key_err_bound(amax_w, kabs_w, act_err_coef(act)));
     const float next_key = __shfl_down_sync(kFull, sel_key, 1);
     // the difference rounded down: a gap of at most band is never missed
     const bool close = (lane < kk - 1) && __fsub_rd(sel_key, next_key) <= band;
-    if (__any_sync(kFull, close))
-      sel_idx = refine_near_ties<VPL>(ld, bias, act, E, k, kk, sel_key, sel_idx, band);
+    if (__any_sync(kFull, close)) {
+      if (act == ACT_SOFTMAX_BIAS) {
+        // FP64 keys for every expert within the band of the k-th key
+        const float thr = __fsub_rd(__shfl_sync(kFull, sel_key, k - 1), band);
+        uint32_t cmask = 0u;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+          const int e = lane + 32 * j;
+          if (e < E && softmax_bias_key32(ld(e), zmax, zsum, __ldg(bias + e)) >= thr)
+            cmask |= 1u << j;
+        }
+        const int pick = select_softmax_bias_fp64<VPL>(ld, bias, E, k, zmax, cmask);
+        if (lane < k) sel_idx = pick;
+      } else {
+        sel_idx = refine_near_ties<VPL>(ld, bias, act, E, k, kk, sel_key, sel_idx, band);
+      }
+    }
   }
 
   // weights over the chosen k, summed in slot order
@@ -268,6 +392,12 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
     // the key is the logit (-0.0 read back as +0.0, which exp treats alike)
     const float z0 = __shfl_sync(kFull, sel_key, 0);
     if (lane < k) s = expf(sel_key - z0);
+  } else if (act == ACT_SOFTMAX_BIAS) {
+    // the unbiased probabilities renormalised: exp(z_j - zc) / sum, zc the
+    // largest chosen logit (the bias may rank a smaller logit first)
+    const float zj = lane < k ? ld(sel_idx) : -INFINITY;
+    const float zc = float_of_ord(__reduce_max_sync(kFull, lane < k ? ord_of(zj) : 0u));
+    if (lane < k) s = expf(zj - zc);
   } else {
     if (lane < k) s = act_f32(act, ld(sel_idx));
     const float smax = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(s)));
@@ -300,6 +430,8 @@ __device__ __forceinline__ void warp_select_row(const Ld ld, const float* __rest
                                                 float* __restrict__ out_w, int32_t* sel_out) {
   if (act == ACT_SOFTMAX)
     warp_select_row_act<VPL, ACT_SOFTMAX>(ld, bias, E, k, out_idx, out_w, sel_out);
+  else if (act == ACT_SOFTMAX_BIAS)
+    warp_select_row_act<VPL, ACT_SOFTMAX_BIAS>(ld, bias, E, k, out_idx, out_w, sel_out);
   else if (act == ACT_SIGMOID)
     warp_select_row_act<VPL, ACT_SIGMOID>(ld, bias, E, k, out_idx, out_w, sel_out);
   else

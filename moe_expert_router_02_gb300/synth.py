@@ -278,6 +278,37 @@ def tie_rows_softmax_bias(n: int, E: int, k: int, seed: int, std: float = 1.0):
     return rows, bias, kinds
 
 
+def tie_rows_softmax_bias_shared(n: int, E: int, k: int, seed: int, std: float = 1.0):
+    """As ``tie_rows_softmax_bias`` with one bias vector for all n rows (a
+    batch shares its bias). The boundary pair and the top experts are the
+    same in every row; the pair's bias is equal, or one ulp apart up or
+    down (by seed); each row's pair logits are equal, or one ulp apart up
+    or down (by row). Returns (rows [n, E] float32, bias [E] float32,
+    kinds)."""
+    gen = rng(seed)
+    rows = np.clip(normal(gen, (n, E), std), -4 * std, 4 * std).astype(np.float32)
+    bias = gen.uniform(-0.05, -0.02, size=E).astype(np.float32)
+    perm = gen.permutation(E)
+    top, (i, j) = perm[: k - 1], perm[k - 1: k + 1]
+    bias[top] = gen.uniform(0.04, 0.05, size=k - 1).astype(np.float32)
+    b0 = np.float32(gen.uniform(0.005, 0.015))
+    bias[i] = b0
+    bias_kind = ("bias_equal", "bias_up", "bias_down")[seed % 3]
+    bias[j] = {"bias_equal": b0, "bias_up": np.nextafter(b0, np.float32(np.inf)),
+               "bias_down": np.nextafter(b0, np.float32(-np.inf))}[bias_kind]
+    v = np.float32(4 * std + 1.0)
+    kinds = []
+    for r in range(n):
+        logit_kind = ("logit_equal", "logit_up", "logit_down")[r % 3]
+        kinds.append(bias_kind + "/" + logit_kind)
+        for t, e in enumerate(top):
+            rows[r, e] = np.float32(v + 3.0 + 1.0 * t + gen.uniform(0, 0.1))
+        rows[r, i] = v
+        rows[r, j] = {"logit_equal": v, "logit_up": np.nextafter(v, np.float32(np.inf)),
+                      "logit_down": np.nextafter(v, np.float32(-np.inf))}[logit_kind]
+    return rows, bias, kinds
+
+
 def inject_tie_rows(rows: np.ndarray, frac: float, k: int, seed: int) -> np.ndarray:
     """Replace a fraction of logit rows with constructed boundary-tie rows
     (same E, same scale)."""

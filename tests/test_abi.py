@@ -57,13 +57,22 @@ def test_router_forward_argument_errors(args, expect):
     assert R.lib().router_forward(None, None, None, M, H, E, k, act, None, None, None) == expect
 
 
-def test_bias_with_softmax_rejected():
+def test_bias_with_softmax_accepted_by_the_argument_checks():
+    # softmax with a bias is a valid call (key = probability + bias); these
+    # calls return before any CUDA call: M == 0 launches nothing, and the
+    # shape errors are still reported
     L = R.lib()
-    fake = ctypes.c_void_p(16)  # never dereferenced: the check comes first
-    assert L.router_forward(fake, fake, fake, 1, 64, 16, 2, R.GBR_ACT_SOFTMAX, fake, fake,
+    fake = ctypes.c_void_p(16)  # never dereferenced: the checks come first
+    assert L.router_forward(fake, fake, fake, 0, 64, 16, 2, R.GBR_ACT_SOFTMAX, fake, fake,
+                            None) == R.GBR_OK
+    assert L.router_forward(fake, fake, fake, 1, 64, 16, 17, R.GBR_ACT_SOFTMAX, fake, fake,
                             None) == R.GBR_EINVAL
-    assert L.router_select(fake, fake, 1, 16, 2, R.GBR_ACT_SOFTMAX, fake, fake,
-                           None) == R.GBR_EINVAL
+    assert L.router_select(fake, fake, 0, 16, 2, R.GBR_ACT_SOFTMAX, fake, fake,
+                           None) == R.GBR_OK
+    assert L.router_select(fake, fake, 1, 1024, 2, R.GBR_ACT_SOFTMAX, fake, fake,
+                           None) == R.GBR_EUNSUPPORTED
+    assert L.router_forward_noalloc(fake, fake, fake, 65, 64, 16, 2, R.GBR_ACT_SOFTMAX, fake,
+                                    fake, None) == R.GBR_EWORKSPACE
 
 
 def test_partial_table_and_odd_M_rejected():
