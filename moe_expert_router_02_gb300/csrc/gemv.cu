@@ -89,7 +89,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
   __shared__ float s_part[kGemvWarps][16][NTOK];
   __shared__ float s_cta[16][NTOK];
   __shared__ int32_t s_sel[kGemvWarps * kMaxK];
-  __shared__ int32_t s_rank[kGemvWarps][32];
   __shared__ uint32_t s_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -121,6 +120,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
 #pragma unroll
   for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
 
+  // x in sub-batches of XB chunks, every load of a sub-batch issued before
+  // its MMAs (one L2 round trip per sub-batch, not one per token tile)
+  constexpr int XB = NT >= 8 ? 2 : kChunkBatch;
   for (int jb = 0; jb < cpw; jb += kChunkBatch) {
     if (jb > 0) {
 #pragma unroll
@@ -133,16 +135,29 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
       }
     }
 #pragma unroll
-    for (int i = 0; i < kChunkBatch; ++i) {
-      if (jb + i < cpw) {
-        const int hoff = h_begin + (warp + kGemvWarps * (jb + i)) * 32 + 8 * t;
+    for (int ib = 0; ib < kChunkBatch; ib += XB) {
+      uint4 xv[XB][NT];
+#pragma unroll
+      for (int i = 0; i < XB; ++i) {
+        const int hoff = h_begin + (warp + kGemvWarps * (jb + ib + i)) * 32 + 8 * t;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           const int tok = n * 8 + g;
-          uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-          if (tok < M) xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + hoff));
-          mma_bf16_16816(acc[n], wa[i].x, wb[i].x, wa[i].y, wb[i].y, xv.x, xv.y);
-          mma_bf16_16816(acc[n], wa[i].z, wb[i].z, wa[i].w, wb[i].w, xv.z, xv.w);
+          xv[i][n] = make_uint4(0u, 0u, 0u, 0u);
+          if (jb + ib + i < cpw && tok < M)
+            xv[i][n] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + hoff));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < XB; ++i) {
+        if (jb + ib + i < cpw) {
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            mma_bf16_16816(acc[n], wa[ib + i].x, wb[ib + i].x, wa[ib + i].y, wb[ib + i].y,
+                           xv[i][n].x, xv[i][n].y);
+            mma_bf16_16816(acc[n], wa[ib + i].z, wb[ib + i].z, wa[ib + i].w, wb[ib + i].w,
+                           xv[i][n].z, xv[i][n].w);
+          }
         }
       }
     }
@@ -208,8 +223,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
       __syncthreads();
       if ((warp & 1) == 0 && row + 1 < M) {
         const size_t gi = (size_t)(row >> 1);
-        warp_route_table(s_sel + warp * k, s_rank[warp], 2, k, a.tbl_unique + gi * 2 * k,
-                         a.tbl_mask + gi * 2 * k, a.tbl_map + gi * 2 * k, a.tbl_count + gi);
+        warp_route_table_small(s_sel + warp * k, 2, k, a.tbl_unique + gi * 2 * k,
+                               a.tbl_mask + gi * 2 * k, a.tbl_map + gi * 2 * k, a.tbl_count + gi);
       }
       __syncthreads();
     }
@@ -221,23 +236,45 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
 // CTAs holds all of W_gate in shared memory: CTA r owns experts
 // [16r, 16r+16) over the whole H, so there are no partial sums to combine
 // and no logits leave the cluster. Each CTA starts bulk copies of its 16 W
-// rows before it waits on the preceding kernel (programmatic dependent
-// launch), then reads x, runs the mma.sync contraction from shared memory,
-// and publishes its 16 x M logits in shared memory. After one cluster
-// barrier, one warp per row gathers the row's E logits from the cluster's
-// CTAs through distributed shared memory and selects. No global scratch,
-// no atomics, no memory fences.
+// rows (L2 evict-first: the weight stream must not push x or the kernel's
+// code out of L2) before it waits on the preceding kernel (programmatic
+// dependent launch); NVFP4 rows are decoded to BF16 in shared memory there
+// too, when the copy fits. After the wait it reads x, runs the mma.sync
+// contraction from shared memory and sums its warps' partials. Row m is
+// selected by one CTA of the cluster (rows spread over the CTAs, a table's
+// row pairs kept together): every CTA sends its 16 logits of row m to that
+// CTA with st.async stores that complete on the receiver's mbarrier, whose
+// expected byte count the receiver set at start. No global scratch, no
+// atomics, no second cluster barrier.
 
 constexpr int k1cWarps = 16;
 constexpr int k1cBatch = 8;  // 32-element chunks of x held in registers per warp
 constexpr int kMaxE1c = 256;
+constexpr int kPartPitch = 20;  // floats per (warp, token) row of partials: 16 experts + pad
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
+                                         uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 16 bytes into shared memory of a CTA of the cluster (shared::cluster
+// address), completing 16 bytes of that CTA's mbarrier transaction count.
+__device__ __forceinline__ void st_async_v4(uint32_t dst, float a, float b, float c, float d,
+                                            uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
           "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
       : "memory");
 }
 
@@ -313,28 +350,49 @@ __device__ __forceinline__ uint4 fp4_frag(uint32_t packed, uint8_t scale_code, c
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__device__ __forceinline__ void dsmem_st_f32(float* p, uint32_t rank, float v) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(r), "f"(v) : "memory");
-}
+// Which CTA of the cluster selects row m, and in which of its row slots.
+// Without a table row m goes to CTA m % CL; with one, the pair (2g, 2g+1)
+// goes to CTA g % CL (the emitter needs both rows of a pair in one CTA).
+struct RowOwner {
+  int CL;
+  bool table;
+  __device__ __forceinline__ int cta(int m) const { return table ? (m >> 1) % CL : m % CL; }
+  __device__ __forceinline__ int slot(int m) const {
+    return table ? 2 * ((m >> 1) / CL) + (m & 1) : m / CL;
+  }
+  __device__ __forceinline__ int row(int c, int s) const {
+    return table ? 2 * (c + CL * (s >> 1)) + (s & 1) : c + CL * s;
+  }
+  __device__ __forceinline__ int count(int c, int M) const {
+    if (table) {
+      const int pairs = M >> 1;
+      return c < pairs ? 2 * ((pairs - c + CL - 1) / CL) : 0;
+    }
+    return c < M ? (M - c + CL - 1) / CL : 0;
+  }
+};
 
-// NVFP4 weights: the CTA stages its 16 packed rows (pitch bytes apart) and
-// their E4M3 block scales; each 16-byte A fragment (8 BF16 values) is
-// decoded from 4 packed bytes through a byte -> two-BF16 table and one exact
-// BF16 multiply by the block scale, so the MMA sees W / g exactly and g
-// multiplies the FP32 sum.
-template <int NT, int VPL, bool FP4>
-__global__ void __launch_bounds__(k1cWarps * 32) k_gemv1c_router(const RouterArgs a, int pitch) {
+// NVFP4 weights: the CTA stages its 16 packed rows (fpitch bytes apart) and
+// their E4M3 block scales. With PREDEC the rows are decoded to BF16 in
+// shared memory before the wait on the preceding kernel, so the contraction
+// after it is the BF16 one; otherwise each 16-byte A fragment (8 BF16
+// values) is decoded from 4 packed bytes as it is used. Either way the MMA
+// sees W / g exactly (a byte -> two-BF16 table, one exact BF16 multiply by
+// the block scale) and g multiplies the FP32 sums.
+template <int NT, int VPL, bool FP4, bool PREDEC>
+__global__ void __launch_bounds__(k1cWarps * 32)
+    k_gemv1c_router(const RouterArgs a, int pitch, int fpitch) {
   constexpr int NTOK = 8 * NT;
-  extern __shared__ __align__(128) uint8_t s_w[];  // [16][pitch bytes]: this CTA's W rows
+  constexpr bool kFrag4 = FP4 && !PREDEC;  // NVFP4 fragments decoded in the MMA loop
+  // BF16 rows [16][pitch] (BF16 weights, or NVFP4 decoded there); NVFP4:
+  // packed rows [16][fpitch] at fbase, then the block scales [16][H/16]
+  extern __shared__ __align__(128) uint8_t s_w[];
   __shared__ uint32_t s_lut[FP4 ? 256 : 1];
-  __shared__ float s_part[k1cWarps][16][NTOK];
-  __shared__ float s_all[NTOK][kMaxE1c];  // CTA 0: every expert's logit, row by row
+  __shared__ __align__(16) float s_part[k1cWarps][NTOK][kPartPitch];
+  __shared__ __align__(16) float s_all[16][kMaxE1c];  // logits of the rows this CTA selects
   __shared__ int32_t s_sel[k1cWarps * kMaxK];
-  __shared__ int32_t s_rank[k1cWarps][32];
-  __shared__ __align__(8) uint64_t s_bar;
-  __shared__ __align__(8) uint64_t s_join;  // CTA 0: one arrival per CTA once its logits are in
+  __shared__ __align__(8) uint64_t s_bar;   // this CTA's W rows have landed
+  __shared__ __align__(8) uint64_t s_join;  // every logit of this CTA's rows has landed
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -342,19 +400,27 @@ __global__ void __launch_bounds__(k1cWarps * 32) k_gemv1c_router(const RouterArg
   const int CL = gridDim.x;
   const int e0 = rank * 16;
   const int H = a.H, M = a.M, E = a.E;
-  const uint32_t bar = smem_u32(&s_bar);
+  const bool table = a.tbl_unique != nullptr;
+  const RowOwner own{CL, table};
+  const int nown = own.count(rank, M);
+  const uint32_t bar = smem_u32(&s_bar), join = smem_u32(&s_join);
   const uint32_t wsm = smem_u32(s_w);
 
   const int row_bytes = FP4 ? H / 2 : H * 2;
   const int scale_bytes = FP4 ? 16 * (H / 16) : 0;
+  const int fbase = PREDEC ? 16 * pitch : 0;  // packed NVFP4 rows
+  const int spitch = FP4 ? fpitch : pitch;    // pitch of the staged rows
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&s_join)), "r"(CL)
-                 : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(join) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                  "r"((uint32_t)(16 * row_bytes + scale_bytes))
                  : "memory");
+    if (nown > 0)  // the other CTAs' stores complete this many bytes on it
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(join),
+                   "r"((uint32_t)(nown * E * 4))
+                   : "memory");
   }
   if (FP4) {
     for (int b = tid; b < 256; b += k1cWarps * 32) {
@@ -364,16 +430,36 @@ __global__ void __launch_bounds__(k1cWarps * 32) k_gemv1c_router(const RouterArg
     }
   }
   __syncthreads();
-  // publish the join barrier's initialisation; the matching wait comes just
-  // before the first remote arrival, long after every CTA has arrived here
+  // publish the barriers' initialisation; the matching wait comes just
+  // before the first remote store, long after every CTA has arrived here
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  if (tid < 16) {  // this CTA's 16 W rows, one bulk copy per row into the padded pitch
-    const uint8_t* w = static_cast<const uint8_t*>(a.w) + (size_t)(e0 + tid) * row_bytes;
-    bulk_g2s(wsm + tid * pitch, w, row_bytes, bar);
-  } else if (FP4 && tid == 16) {  // the 16 rows of block scales are contiguous
-    bulk_g2s(wsm + 16 * pitch, a.w_scales + (size_t)e0 * (H / 16), scale_bytes, bar);
+  if (tid < 17) {
+    const uint64_t pol = policy_evict_first();
+    if (tid < 16) {  // this CTA's 16 W rows, one bulk copy per row into the padded pitch
+      const uint8_t* w = static_cast<const uint8_t*>(a.w) + (size_t)(e0 + tid) * row_bytes;
+      bulk_g2s(wsm + fbase + tid * spitch, w, row_bytes, bar, pol);
+    } else if (FP4) {  // the 16 rows of block scales are contiguous
+      bulk_g2s(wsm + fbase + 16 * spitch, a.w_scales + (size_t)e0 * (H / 16), scale_bytes, bar,
+               pol);
+    }
   }
   pdl_launch_dependents();
+  bool w_ok = true;
+  if (PREDEC) {
+    // W does not depend on the preceding kernel: decode it before the wait
+    w_ok = mbar_wait_bounded(bar, 0, a.status);
+    const int n8 = H / 8;  // 8-element chunks per row
+    const uint8_t* sc = s_w + fbase + 16 * fpitch;
+    for (int i = tid; i < 16 * n8; i += k1cWarps * 32) {
+      const int r = i / n8, c8 = i - r * n8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (w_ok)
+        v = fp4_frag(*reinterpret_cast<const uint32_t*>(s_w + fbase + r * fpitch + c8 * 4),
+                     sc[r * (H / 16) + (c8 >> 1)], s_lut);
+      *reinterpret_cast<uint4*>(s_w + r * pitch + c8 * 16) = v;
+    }
+    __syncthreads();
+  }
   pdl_wait();  // x and the outputs belong to the preceding kernel until here
 
   const uint16_t* __restrict__ x = static_cast<const uint16_t*>(a.x);
@@ -382,11 +468,10 @@ __global__ void __launch_bounds__(k1cWarps * 32) k_gemv1c_router(const RouterArg
   float acc[NT][4];
 #pragma unroll
   for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-  const uint8_t* w0 = s_w + g * pitch + (FP4 ? 4 : 16) * t;
-  const uint8_t* w1 = w0 + 8 * pitch;
-  const uint8_t* sc0 = s_w + 16 * pitch + g * (H / 16) + (t >> 1);  // NVFP4 block scales
+  const uint8_t* w0 = s_w + g * (kFrag4 ? fpitch : pitch) + (kFrag4 ? 4 : 16) * t;
+  const uint8_t* w1 = w0 + 8 * (kFrag4 ? fpitch : pitch);
+  const uint8_t* sc0 = s_w + 16 * fpitch + g * (H / 16) + (t >> 1);  // kFrag4 block scales
   const uint8_t* sc1 = sc0 + 8 * (H / 16);
-  bool w_ok = true;
   for (int jb = 0; jb < cpw; jb += k1cBatch) {
     uint4 xv[k1cBatch][NT];
 #pragma unroll
@@ -400,13 +485,13 @@ __global__ void __launch_bounds__(k1cWarps * 32) k_gemv1c_router(const RouterArg
           xv[i][n] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + hoff));
       }
     }
-    if (jb == 0) w_ok = mbar_wait_bounded(bar, 0, a.status);  // x loads are in flight meanwhile
+    if (!PREDEC && jb == 0) w_ok = mbar_wait_bounded(bar, 0, a.status);  // x loads in flight
 #pragma unroll
     for (int i = 0; i < k1cBatch; ++i) {
       if (jb + i < cpw && w_ok) {
         const int c = warp + k1cWarps * (jb + i);
         uint4 wa, wb;
-        if (FP4) {
+        if (kFrag4) {
           wa = fp4_frag(*reinterpret_cast<const uint32_t*>(w0 + c * 16), sc0[2 * c], s_lut);
           wb = fp4_frag(*reinterpret_cast<const uint32_t*>(w1 + c * 16), sc1[2 * c], s_lut);
         } else {
@@ -421,52 +506,59 @@ __global__ void __launch_bounds__(k1cWarps * 32) k_gemv1c_router(const RouterArg
       }
     }
   }
-  if (cpw == 0) mbar_wait_bounded(bar, 0, a.status);  // never leave with copies in flight
+  if (!PREDEC && cpw == 0) mbar_wait_bounded(bar, 0, a.status);  // never leave with copies in flight
+  // accumulator layout: c0,c1 -> expert g, tokens 2t, 2t+1; c2,c3 -> expert g+8
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
-    s_part[warp][g][n * 8 + 2 * t] = acc[n][0];
-    s_part[warp][g][n * 8 + 2 * t + 1] = acc[n][1];
-    s_part[warp][g + 8][n * 8 + 2 * t] = acc[n][2];
-    s_part[warp][g + 8][n * 8 + 2 * t + 1] = acc[n][3];
+    s_part[warp][n * 8 + 2 * t][g] = acc[n][0];
+    s_part[warp][n * 8 + 2 * t + 1][g] = acc[n][1];
+    s_part[warp][n * 8 + 2 * t][g + 8] = acc[n][2];
+    s_part[warp][n * 8 + 2 * t + 1][g + 8] = acc[n][3];
   }
   __syncthreads();
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-  // sum the warps' partials in a fixed order and push them into CTA 0
-  for (int i = tid; i < 16 * M; i += k1cWarps * 32) {
-    const int m = i >> 4, el = i & 15;
-    float v = s_part[0][el][m];
+  // sum the warps' partials in a fixed order; four experts of a row per
+  // thread go to the CTA that selects the row
+  for (int i = tid; i < 4 * M; i += k1cWarps * 32) {
+    const int m = i >> 2, q = i & 3;
+    float4 v = *reinterpret_cast<const float4*>(&s_part[0][m][4 * q]);
 #pragma unroll
-    for (int w = 1; w < k1cWarps; ++w) v += s_part[w][el][m];
-    if (FP4) v *= a.w_global;
-    dsmem_st_f32(&s_all[m][e0 + el], 0u, v);
-    if (a.logits) a.logits[(size_t)m * E + e0 + el] = v;
+    for (int w = 1; w < k1cWarps; ++w) {
+      const float4 u = *reinterpret_cast<const float4*>(&s_part[w][m][4 * q]);
+      v.x += u.x, v.y += u.y, v.z += u.z, v.w += u.w;
+    }
+    if (FP4) {
+      v.x *= a.w_global, v.y *= a.w_global, v.z *= a.w_global, v.w *= a.w_global;
+    }
+    if (a.logits) {
+      float* lg = a.logits + (size_t)m * E + e0 + 4 * q;
+      lg[0] = v.x, lg[1] = v.y, lg[2] = v.z, lg[3] = v.w;
+    }
+    const uint32_t dst_cta = (uint32_t)own.cta(m);
+    uint32_t dst, dbar;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(dst)
+                 : "r"(smem_u32(&s_all[own.slot(m)][e0 + 4 * q])), "r"(dst_cta));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dbar) : "r"(join), "r"(dst_cta));
+    st_async_v4(dst, v.x, v.y, v.z, v.w, dbar);
   }
-  __syncthreads();  // this CTA's pushes happen before its arrival (the release is cumulative)
-  if (tid == 0) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(smem_u32(&s_join)));
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(r)
-                 : "memory");
-  }
-  if (rank != 0) return;  // nothing reads this CTA's shared memory
-  if (!mbar_wait_cluster(smem_u32(&s_join), 0, a.status)) return;
+  if (nown == 0) return;  // no row to select; no CTA reads this one's shared memory
+  if (!mbar_wait_cluster(join, 0, a.status)) return;
 
-  const bool table = a.tbl_unique != nullptr;
+  // warp s selects the CTA's row slot s; rows 2g and 2g+1 of a table's pair
+  // sit in slots 2p and 2p + 1
   const int k = a.k;
-  for (int base = 0; base < M; base += k1cWarps) {
-    const int row = base + warp;
-    if (row < M)
-      warp_select_row<VPL>(LdPlain{&s_all[row][0]}, a.bias, E, k, a.act,
-                           a.out_idx + (size_t)row * k, a.out_w + (size_t)row * k,
-                           s_sel + warp * k);
-    if (table) {
-      __syncthreads();
-      if ((warp & 1) == 0 && row + 1 < M) {
-        const size_t gi = (size_t)(row >> 1);
-        warp_route_table(s_sel + warp * k, s_rank[warp], 2, k, a.tbl_unique + gi * 2 * k,
-                         a.tbl_mask + gi * 2 * k, a.tbl_map + gi * 2 * k, a.tbl_count + gi);
-      }
-      __syncthreads();
+  const int row = own.row(rank, warp);
+  if (warp < nown)
+    warp_select_row<VPL>(LdPlain{&s_all[warp][0]}, a.bias, E, k, a.act,
+                         a.out_idx + (size_t)row * k, a.out_w + (size_t)row * k,
+                         s_sel + warp * k);
+  if (table) {
+    __syncthreads();
+    if ((warp & 1) == 0 && warp + 1 < nown) {
+      const size_t gi = (size_t)(row >> 1);
+      warp_route_table_small(s_sel + warp * k, 2, k, a.tbl_unique + gi * 2 * k,
+                             a.tbl_mask + gi * 2 * k, a.tbl_map + gi * 2 * k, a.tbl_count + gi);
     }
   }
 }
@@ -495,7 +587,6 @@ template <int VPL>
 __global__ void __launch_bounds__(kGenWarps * 32) k_generic_router(const RouterArgs a, int rows) {
   __shared__ float s_log[2][kMaxE];
   __shared__ int32_t s_sel[2 * kMaxK];
-  __shared__ int32_t s_rank[32];
   pdl_launch_dependents();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -525,8 +616,8 @@ __global__ void __launch_bounds__(kGenWarps * 32) k_generic_router(const RouterA
   __syncthreads();
   if (a.tbl_unique && rows == 2 && warp == 0 && row0 + 1 < M) {
     const size_t gi = (size_t)(row0 >> 1);
-    warp_route_table(s_sel, s_rank, 2, k, a.tbl_unique + gi * 2 * k, a.tbl_mask + gi * 2 * k,
-                     a.tbl_map + gi * 2 * k, a.tbl_count + gi);
+    warp_route_table_small(s_sel, 2, k, a.tbl_unique + gi * 2 * k, a.tbl_mask + gi * 2 * k,
+                           a.tbl_map + gi * 2 * k, a.tbl_count + gi);
   }
 }
 
@@ -576,23 +667,29 @@ cudaError_t gemv_dispatch(const RouterArgs& a, int CL, bool pdl, cudaStream_t s)
 // Row pitch of the staged W rows: BF16 rows padded to 64 (mod 128) bytes and
 // NVFP4 rows to 16 (mod 32) bytes, which keeps the fragment loads free of
 // bank conflicts.
-int gemv1c_pitch(int H, bool fp4) {
-  if (fp4) return H / 2 + ((H / 2) % 32 == 16 ? 0 : 16);
-  return 2 * H + ((2 * H) % 128 == 0 ? 64 : 0);
+int gemv1c_pitch(int H) { return 2 * H + ((2 * H) % 128 == 0 ? 64 : 0); }
+int gemv1c_fpitch(int H) { return H / 2 + ((H / 2) % 32 == 16 ? 0 : 16); }
+
+// Dynamic shared memory of the single-cluster kernel: BF16 rows, NVFP4 packed
+// rows and scales, or both when NVFP4 rows are decoded before the wait.
+size_t gemv1c_smem(int H, bool fp4, bool predec) {
+  const size_t bf = (size_t)16 * gemv1c_pitch(H);
+  const size_t f4 = (size_t)16 * gemv1c_fpitch(H) + (size_t)16 * (H / 16);
+  return fp4 ? (predec ? bf + f4 : f4) : bf;
 }
 
-size_t gemv1c_smem(int H, bool fp4) {
-  return (size_t)16 * gemv1c_pitch(H, fp4) + (fp4 ? (size_t)16 * (H / 16) : 0);
-}
+constexpr size_t k1cMaxDynSmem = 180 * 1024;  // leaves room for the static arrays (about 40 KB)
+
+// NVFP4 rows are decoded before the wait whenever both copies fit.
+bool gemv1c_predec(int H) { return gemv1c_smem(H, true, true) <= k1cMaxDynSmem; }
 
 // Launches (or, with probe, only sizes) the single-cluster kernel.
-template <int NT, int VPL, bool FP4>
+template <int NT, int VPL, bool FP4, bool PREDEC>
 cudaError_t launch_1c_inst(const RouterArgs& a, bool pdl, cudaStream_t stream, bool probe,
                            bool* fits) {
-  auto kern = k_gemv1c_router<NT, VPL, FP4>;
+  auto kern = k_gemv1c_router<NT, VPL, FP4, PREDEC>;
   const int CL = a.E / 16;
-  const int pitch = gemv1c_pitch(a.H, FP4);
-  const size_t dsmem = gemv1c_smem(a.H, FP4);
+  const size_t dsmem = gemv1c_smem(a.H, FP4, PREDEC);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dsmem);
   if (e != cudaSuccess) return e;
@@ -620,22 +717,24 @@ cudaError_t launch_1c_inst(const RouterArgs& a, bool pdl, cudaStream_t stream, b
     *fits = (e == cudaSuccess && n > 0);
     return cudaSuccess;
   }
-  return cudaLaunchKernelEx(&cfg, kern, a, pitch);
+  return cudaLaunchKernelEx(&cfg, kern, a, gemv1c_pitch(a.H), gemv1c_fpitch(a.H));
 }
 
-template <int NT, bool FP4>
+template <int NT, bool FP4, bool PREDEC>
 cudaError_t launch_1c_vpl(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe, bool* fits) {
-  if (a.E <= 128) return launch_1c_inst<NT, 4, FP4>(a, pdl, s, probe, fits);
-  return launch_1c_inst<NT, 8, FP4>(a, pdl, s, probe, fits);
+  if (a.E <= 128) return launch_1c_inst<NT, 4, FP4, PREDEC>(a, pdl, s, probe, fits);
+  return launch_1c_inst<NT, 8, FP4, PREDEC>(a, pdl, s, probe, fits);
+}
+
+template <int NT>
+cudaError_t launch_1c_nt(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe, bool* fits) {
+  if (a.w_dtype != DT_NVFP4) return launch_1c_vpl<NT, false, false>(a, pdl, s, probe, fits);
+  if (gemv1c_predec(a.H)) return launch_1c_vpl<NT, true, true>(a, pdl, s, probe, fits);
+  return launch_1c_vpl<NT, true, false>(a, pdl, s, probe, fits);
 }
 
 cudaError_t launch_1c(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe, bool* fits) {
-  const bool fp4 = a.w_dtype == DT_NVFP4;
-  if (a.M <= 8)
-    return fp4 ? launch_1c_vpl<1, true>(a, pdl, s, probe, fits)
-               : launch_1c_vpl<1, false>(a, pdl, s, probe, fits);
-  return fp4 ? launch_1c_vpl<2, true>(a, pdl, s, probe, fits)
-             : launch_1c_vpl<2, false>(a, pdl, s, probe, fits);
+  return a.M <= 8 ? launch_1c_nt<1>(a, pdl, s, probe, fits) : launch_1c_nt<2>(a, pdl, s, probe, fits);
 }
 
 }  // namespace
@@ -643,13 +742,13 @@ cudaError_t launch_1c(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe,
 bool gemv1c_eligible(int M, int H, int E, bool fp4) {
   if (M < 1 || M > 16 || E % 16 != 0 || E < 16 || E > 256 || H % (fp4 ? 256 : 32) != 0)
     return false;
-  if (gemv1c_smem(H, fp4) > (size_t)200 * 1024) return false;
+  if (gemv1c_smem(H, fp4, fp4 && gemv1c_predec(H)) > k1cMaxDynSmem) return false;
   // the cluster must be schedulable with this much shared memory per CTA
   static std::mutex mu;
   static std::map<std::tuple<int, int, int, int>, bool> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  const auto key = std::make_tuple(dev, (M <= 8 ? 1 : 2) + (fp4 ? 2 : 0), E, gemv1c_pitch(H, fp4));
+  const auto key = std::make_tuple(dev, (M <= 8 ? 1 : 2) + (fp4 ? 2 : 0), E, H);
   std::lock_guard<std::mutex> lk(mu);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
@@ -658,6 +757,7 @@ bool gemv1c_eligible(int M, int H, int E, bool fp4) {
   probe_args.w_dtype = fp4 ? DT_NVFP4 : DT_BF16;
   bool fits = false;
   if (launch_1c(probe_args, true, 0, true, &fits) != cudaSuccess) fits = false;
+  (void)cudaGetLastError();
   cache[key] = fits;
   return fits;
 }

@@ -36,6 +36,45 @@ __global__ void __launch_bounds__(kTblWarps * 32)
                    map + (size_t)g * n, count + g);
 }
 
+// Groups of n = T*k <= 32 entries: floor(32 / n) groups per warp, one entry
+// per lane, so a warp's loads and stores cover consecutive groups'
+// contiguous rows; each warp takes kTblChunks such sets of groups and
+// issues all of their loads first (enough bytes in flight to stream HBM).
+constexpr int kTblChunks = 8;
+
+__global__ void __launch_bounds__(kTblWarps * 32)
+    k_route_table32(const int32_t* __restrict__ idx, int G, int T, int k,
+                    int32_t* __restrict__ unique, uint8_t* __restrict__ mask,
+                    uint8_t* __restrict__ map, int32_t* __restrict__ count) {
+  const int lane = threadIdx.x & 31;
+  const int n = T * k;
+  const int gpw = 32 / n;  // groups per warp and chunk
+  const int gl = lane / n, p = lane - gl * n;
+  const int gbase = gl * n;
+  const uint32_t gmask = gl < gpw ? (n == 32 ? kFull : ((1u << n) - 1u) << gbase) : 0u;
+  const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long g0 = warp_id * kTblChunks * gpw;  // first group of this warp
+  int32_t v[kTblChunks];
+#pragma unroll
+  for (int c = 0; c < kTblChunks; ++c) {
+    const long long g = g0 + (long long)c * gpw + gl;
+    v[c] = (gl < gpw && g < G) ? __ldg(idx + g * n + p) : 0;
+  }
+#pragma unroll
+  for (int c = 0; c < kTblChunks; ++c) {
+    const long long g = g0 + (long long)c * gpw + gl;
+    const bool valid = gl < gpw && g < G;
+    const TableLane r = table_lanes(v[c], valid, gmask, gbase, T, k);
+    if (valid) {
+      const long long o = g * n + p;
+      unique[o] = r.uniq;
+      mask[o] = (uint8_t)r.mask;
+      map[o] = (uint8_t)r.map;
+      if (p == 0) count[g] = r.count;
+    }
+  }
+}
+
 __global__ void k_near_tie_keys(const float* __restrict__ z, const float* __restrict__ bias, int n,
                                 int act, float* __restrict__ hi, float* __restrict__ lo) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
@@ -67,8 +106,16 @@ cudaError_t launch_select(const float* logits, const float* bias, int M, int E, 
 
 cudaError_t launch_route_table(const int32_t* idx, int groups, int T, int k, int32_t* unique,
                                uint8_t* mask, uint8_t* map, int32_t* count, cudaStream_t stream) {
-  const dim3 grid((groups + kTblWarps - 1) / kTblWarps), block(kTblWarps * 32);
-  k_route_table<<<grid, block, 0, stream>>>(idx, groups, T, k, unique, mask, map, count);
+  const dim3 block(kTblWarps * 32);
+  if (T * k <= 32) {
+    const long long per_warp = (long long)(32 / (T * k)) * kTblChunks;
+    const long long warps = (groups + per_warp - 1) / per_warp;
+    const dim3 grid((unsigned)((warps + kTblWarps - 1) / kTblWarps));
+    k_route_table32<<<grid, block, 0, stream>>>(idx, groups, T, k, unique, mask, map, count);
+  } else {
+    const dim3 grid((groups + kTblWarps - 1) / kTblWarps);
+    k_route_table<<<grid, block, 0, stream>>>(idx, groups, T, k, unique, mask, map, count);
+  }
   return cudaGetLastError();
 }
 

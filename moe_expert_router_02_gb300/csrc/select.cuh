@@ -257,6 +257,22 @@ __device__ __noinline__ int refine_near_ties(const Ld ld, const float* __restric
   return sel_idx;
 }
 
+// The sum of the first k of v[0..KC) in the tree order of the warp
+// selection's butterfly (j + j^8, then ^4, ^2, ^1 over 16 slots), for
+// kernels that hold a row's chosen scores in one thread.
+template <int KC>
+__device__ __forceinline__ float slot_tree_sum(const float (&v)[KC], int k) {
+  float t[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t[j] = (j < KC && j < k) ? v[j < KC ? j : 0] : 0.0f;
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1) {
+#pragma unroll
+    for (int j = 0; j < w; ++j) t[j] = t[j] + t[j + w];
+  }
+  return t[0];
+}
+
 // One warp selects the top-k of one row of E <= 32*VPL logits.
 // Lane r < k writes slot r of out_idx / out_w and, if sel_out is not null,
 // sel_out[r] (for a route table). All 32 lanes must call.
@@ -411,12 +427,14 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
       s = (lane < k && lm > -INFINITY) ? expf(la - lm) : 0.0f;
     }
   }
-  float sum = 0.0f;
-#pragma unroll
-  for (int r = 0; r < kMaxK; ++r) {
-    const float v = __shfl_sync(kFull, s, r);
-    if (r < k) sum += v;
-  }
+  // summed over the slots by a fixed tree (slot j + slot j^8, then ^4, ^2,
+  // ^1; slots >= k add 0): every lane gets the same sum, in the order
+  // slot_tree_sum follows
+  float sum = lane < k ? s : 0.0f;
+  sum += __shfl_xor_sync(kFull, sum, 8);
+  sum += __shfl_xor_sync(kFull, sum, 4);
+  sum += __shfl_xor_sync(kFull, sum, 2);
+  sum += __shfl_xor_sync(kFull, sum, 1);
   if (lane < k) {
     out_idx[lane] = sel_idx;
     out_w[lane] = (sum > 0.0f) ? s / sum : 1.0f / (float)k;
@@ -436,6 +454,67 @@ __device__ __forceinline__ void warp_select_row(const Ld ld, const float* __rest
     warp_select_row_act<VPL, ACT_SIGMOID>(ld, bias, E, k, out_idx, out_w, sel_out);
   else
     warp_select_row_act<VPL, ACT_SQRT_SOFTPLUS>(ld, bias, E, k, out_idx, out_w, sel_out);
+}
+
+// The unique-route table of groups of n = T*k <= 32 (token, slot) entries
+// laid over a warp's lanes in row-major order: the lanes gbase .. gbase+n-1
+// (gmask) hold one group, lane gbase + p its entry p with id v (b70 lab
+// note, "Unique-route router screen": stable dedup, prefix ranking, token
+// masks, slot mapping, done with warp match and ballot). The lowest lane
+// holding an id is its first occurrence; its unique position is the number
+// of first occurrences below it. Returns, for this lane: map (the entry's
+// unique position), the unique id and token mask of unique position
+// p = lane - gbase (-1 and 0 past the count), and the count. All lanes call.
+struct TableLane {
+  int32_t uniq;
+  uint32_t mask;
+  uint32_t map;
+  int count;
+};
+
+__device__ __forceinline__ TableLane table_lanes(int32_t v, bool valid, uint32_t gmask, int gbase,
+                                                 int T, int k) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t eq = __match_any_sync(kFull, v) & gmask;  // lanes of this group holding v
+  const int first = eq ? __ffs(eq) - 1 : lane;  // eq == 0: a lane outside every group
+  const uint32_t fb = __ballot_sync(kFull, valid && first == lane) & gmask;
+  TableLane r;
+  r.map = (uint32_t)__popc(fb & ((1u << first) - 1u));
+  r.count = __popc(fb);
+  // bit t when token t (lanes gbase + t k .. gbase + t k + k - 1) holds v
+  const uint32_t slots = (k == 32 ? kFull : (1u << k) - 1u);
+  uint32_t tm = 0u;
+  for (int t = 0; t < T; ++t) tm |= ((eq >> (gbase + t * k)) & slots) ? (1u << t) : 0u;
+  // lane gbase + u takes the id and mask of the u-th first occurrence
+  const int u = lane - gbase;
+  const bool has = valid && u < r.count;
+  uint32_t src = (uint32_t)lane;
+  if (has) asm("fns.b32 %0, %1, 0, %2;" : "=r"(src) : "r"(fb), "r"(u + 1));
+  const int32_t uv = __shfl_sync(kFull, v, (int)src);
+  const uint32_t um = __shfl_sync(kFull, tm, (int)src);
+  r.uniq = has ? uv : -1;
+  r.mask = has ? um : 0u;
+  return r;
+}
+
+// One group of T x k <= 32 entries from ids in shared memory s_idx[T*k]
+// (one warp; lanes >= T*k idle).
+__device__ __forceinline__ void warp_route_table_small(const int32_t* s_idx, int T, int k,
+                                                       int32_t* __restrict__ unique,
+                                                       uint8_t* __restrict__ mask,
+                                                       uint8_t* __restrict__ map,
+                                                       int32_t* __restrict__ count) {
+  const int lane = threadIdx.x & 31;
+  const int n = T * k;
+  const bool valid = lane < n;
+  const int32_t v = valid ? s_idx[lane] : 0;
+  const TableLane r = table_lanes(v, valid, n == 32 ? kFull : (1u << n) - 1u, 0, T, k);
+  if (valid) {
+    unique[lane] = r.uniq;
+    mask[lane] = (uint8_t)r.mask;
+    map[lane] = (uint8_t)r.map;
+    if (lane == 0) *count = r.count;
+  }
 }
 
 // One warp emits the unique-route table of one group of T tokens x k slots

@@ -1413,12 +1413,10 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       }
       if (m < a.M) {
         float sv[KC];
-        float sum = 0.0f;
 #pragma unroll
-        for (int j = 0; j < KC; ++j) {
+        for (int j = 0; j < KC; ++j)
           sv[j] = sp ? top.z[j] : expf(top.z[j] - top.z[0]);  // the list keeps scores
-          if (j < k) sum += sv[j];
-        }
+        float sum = slot_tree_sum<KC>(sv, k);  // the warp selection's summation order
         if (sp) {
           float smax = 0.0f;
 #pragma unroll
@@ -1433,12 +1431,9 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
               la[j] = j < k ? log_act(act, zbuf[top.i[j] * BM + row]) : -INFINITY;
               lm = fmaxf(lm, la[j]);
             }
-            sum = 0.0f;
 #pragma unroll
-            for (int j = 0; j < KC; ++j) {
-              sv[j] = lm > -INFINITY ? expf(la[j] - lm) : 0.0f;
-              if (j < k) sum += sv[j];
-            }
+            for (int j = 0; j < KC; ++j) sv[j] = lm > -INFINITY ? expf(la[j] - lm) : 0.0f;
+            sum = slot_tree_sum<KC>(sv, k);
           }
         }
         const float inv = 1.0f / (float)k;

@@ -57,6 +57,14 @@ def test_duplicates_and_group_sizes(T, k):
     assert_table_equal(gen.integers(0, 1000, size=(333, T, k)).astype(np.int32))
 
 
+@pytest.mark.parametrize("T,k", [(2, 6), (1, 7), (4, 8), (2, 16), (8, 16)])
+@pytest.mark.parametrize("G", [1, 2, 3, 17, 31, 1000])
+def test_ragged_group_counts(T, k, G):
+    # counts that leave the last warp's groups partly empty
+    gen = synth.rng(G * 7 + T + k)
+    assert_table_equal(gen.integers(0, 9, size=(G, T, k)).astype(np.int32))
+
+
 def test_graph_replay_with_changing_inputs():
     import torch
     G, T, k = 4096, 2, 6
