@@ -1,26 +1,18 @@
-// Small-M (decode / verify widths) fused router and the generic router.
+// Small-M (decode / verify widths) fused routers and the generic router.
 //
-// Small-M design. At M <= 64 the router reads W_gate (E x H BF16, 1-4 MiB)
-// once and little else, so it is bound by HBM and by latency. The grid
-// spreads W over the whole GPU: CTA (r, eg) owns expert group eg (16
-// experts) and the r-th of CL slices of H; the CL CTAs of one expert group
-// form a thread-block cluster. Every thread issues its 16-byte W loads
-// before it waits on the preceding kernel (programmatic dependent launch),
-// so back-to-back calls overlap their W streams with the previous call's
-// tail. The contraction runs on the tensor cores with mma.sync m16n8k16
-// (experts as the 16-row operand, up to 8 tokens per n-tile), which keeps
-// the FP32-accumulate arithmetic far below the memory time even at M=64.
-//
-// Reductions. Per-warp partials are summed in shared memory, the CL slices
-// of a cluster through distributed shared memory, both in a fixed order, so
-// the logits are deterministic. Each cluster writes its 16 x M logits to a
-// small FP32 buffer [M, E] (L2-resident scratch, or the caller's logits
-// tap) and bumps an arrival ticket; the last cluster to arrive runs the
-// selection, one warp per row, and resets the ticket for the next call.
-// Nothing ever waits on another CTA except through the hardware cluster
-// barrier. This is the "threadgroup-level reduction" option that qwisp
+// At M <= 64 the router reads W_gate (E x H BF16, 1-4 MiB) once and little
+// else, so it is bound by HBM and by latency. W rows are bulk-copied into
+// shared memory before each kernel waits on the preceding one (programmatic
+// dependent launch), so back-to-back calls overlap their W streams with the
+// previous call's tail. The contraction runs on the tensor cores with
+// mma.sync m16n8k16 (experts as the 16-row operand, 8 tokens per n-tile).
+// The logits are combined on chip in a fixed order (deterministic): inside
+// one cluster of E/16 CTAs that holds all of W (single-cluster kernel), or
+// over clusters that each hold a slice of H, through distributed shared
+// memory and an L2-resident buffer with an arrival ticket (split-cluster
+// kernel). Both are the "threadgroup-level reduction" option that qwisp
 // issue #145 ("Change") leaves to measurement, with the E logits kept on
-// chip and in L2 instead of a separate launch.
+// chip or in L2 instead of a separate launch.
 #include <cuda_bf16.h>
 
 #include <map>
@@ -33,8 +25,6 @@
 namespace gbr {
 namespace {
 
-constexpr int kGemvWarps = 4;
-constexpr int kChunkBatch = 4;  // 32-element H chunks held in registers per warp at once
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -77,160 +67,6 @@ __device__ __forceinline__ void atom_exch_relaxed_gpu(uint32_t* p, uint32_t v) {
                : "memory");
 }
 
-// K permutation inside a 32-element chunk: thread t of a quad owns the 8
-// consecutive elements [8t, 8t+8). For MMA j (0, 1) its logical k slots
-// {2t, 2t+1, 2t+8, 2t+9} are the physical elements 8t + 4j + {0,1,2,3}.
-// A (W rows g, g+8) and B (x token g) use the same map, so every product
-// pairs the same h and each h is used once.
-template <int NT, int VPL, bool SELECT>
-__global__ void __launch_bounds__(kGemvWarps * 32)
-    k_gemv_router(const RouterArgs a, int CL) {
-  constexpr int NTOK = 8 * NT;
-  __shared__ float s_part[kGemvWarps][16][NTOK];
-  __shared__ float s_cta[16][NTOK];
-  __shared__ int32_t s_sel[kGemvWarps * kMaxK];
-  __shared__ uint32_t s_flag;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int rank = blockIdx.x;  // the grid's x extent equals the cluster size
-  const int e0 = blockIdx.y * 16;
-  const int H = a.H, M = a.M, E = a.E;
-  const int Hc = H / CL, nchunk = Hc / 32, h_begin = rank * Hc;
-  const uint16_t* __restrict__ x = static_cast<const uint16_t*>(a.x);
-  const uint16_t* w0 =
-      static_cast<const uint16_t*>(a.w) + (size_t)(e0 + g) * H + h_begin + 8 * t;
-  const uint16_t* w1 = w0 + (size_t)8 * H;
-  const int cpw = warp < nchunk ? (nchunk - warp + kGemvWarps - 1) / kGemvWarps : 0;
-
-  pdl_launch_dependents();
-
-  uint4 wa[kChunkBatch], wb[kChunkBatch];
-#pragma unroll
-  for (int i = 0; i < kChunkBatch; ++i) {
-    if (i < cpw) {
-      const int off = (warp + kGemvWarps * i) * 32;
-      wa[i] = ld_nc_v4(w0 + off);
-      wb[i] = ld_nc_v4(w1 + off);
-    }
-  }
-  pdl_wait();  // x, the scratch and the ticket belong to the preceding call until here
-
-  float acc[NT][4];
-#pragma unroll
-  for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
-
-  // x in sub-batches of XB chunks, every load of a sub-batch issued before
-  // its MMAs (one L2 round trip per sub-batch, not one per token tile)
-  constexpr int XB = NT >= 8 ? 2 : kChunkBatch;
-  for (int jb = 0; jb < cpw; jb += kChunkBatch) {
-    if (jb > 0) {
-#pragma unroll
-      for (int i = 0; i < kChunkBatch; ++i) {
-        if (jb + i < cpw) {
-          const int off = (warp + kGemvWarps * (jb + i)) * 32;
-          wa[i] = ld_nc_v4(w0 + off);
-          wb[i] = ld_nc_v4(w1 + off);
-        }
-      }
-    }
-#pragma unroll
-    for (int ib = 0; ib < kChunkBatch; ib += XB) {
-      uint4 xv[XB][NT];
-#pragma unroll
-      for (int i = 0; i < XB; ++i) {
-        const int hoff = h_begin + (warp + kGemvWarps * (jb + ib + i)) * 32 + 8 * t;
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          const int tok = n * 8 + g;
-          xv[i][n] = make_uint4(0u, 0u, 0u, 0u);
-          if (jb + ib + i < cpw && tok < M)
-            xv[i][n] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + hoff));
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < XB; ++i) {
-        if (jb + ib + i < cpw) {
-#pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            mma_bf16_16816(acc[n], wa[ib + i].x, wb[ib + i].x, wa[ib + i].y, wb[ib + i].y,
-                           xv[i][n].x, xv[i][n].y);
-            mma_bf16_16816(acc[n], wa[ib + i].z, wb[ib + i].z, wa[ib + i].w, wb[ib + i].w,
-                           xv[i][n].z, xv[i][n].w);
-          }
-        }
-      }
-    }
-  }
-
-  // accumulator layout: c0,c1 -> expert g, tokens 2t, 2t+1; c2,c3 -> expert g+8
-#pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    s_part[warp][g][n * 8 + 2 * t] = acc[n][0];
-    s_part[warp][g][n * 8 + 2 * t + 1] = acc[n][1];
-    s_part[warp][g + 8][n * 8 + 2 * t] = acc[n][2];
-    s_part[warp][g + 8][n * 8 + 2 * t + 1] = acc[n][3];
-  }
-  __syncthreads();
-  for (int i = tid; i < 16 * NTOK; i += kGemvWarps * 32) {
-    const int el = i / NTOK, m = i % NTOK;
-    float v = s_part[0][el][m];
-#pragma unroll
-    for (int w = 1; w < kGemvWarps; ++w) v += s_part[w][el][m];
-    s_cta[el][m] = v;
-  }
-  cluster_sync_all();
-
-  // cluster reduction over the CL slices of H; item i = m * 16 + el
-  for (int i = rank + CL * tid; i < 16 * M; i += CL * kGemvWarps * 32) {
-    const int m = i >> 4, el = i & 15;
-    float part[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) part[q] = q < CL ? dsmem_ld_f32(&s_cta[el][m], (uint32_t)q) : 0.0f;
-    float v = part[0];
-#pragma unroll
-    for (int q = 1; q < 8; ++q) v += part[q];  // fixed order; absent slices add +0
-    a.logits[(size_t)m * E + e0 + el] = v;
-  }
-  if (!SELECT) {
-    cluster_sync_all();  // keep shared memory alive until every peer has read it
-    return;
-  }
-  // The cluster barrier (release/acquire) orders every peer's logits stores
-  // before rank 0's acq_rel arrival on the ticket; the arrivals form one
-  // release sequence, so the cluster that arrives last observes all logits
-  // and hands them to its peers through the next cluster barrier.
-  cluster_sync_all();
-  if (rank == 0 && tid == 0) {
-    const uint32_t old = atom_add_acq_rel_gpu(a.ticket, 1u);
-    const uint32_t last = (old == gridDim.y - 1) ? 1u : 0u;
-    if (last) atom_exch_relaxed_gpu(a.ticket, 0u);
-    for (int q = 0; q < CL; ++q) dsmem_st_u32(&s_flag, (uint32_t)q, last);
-  }
-  cluster_sync_all();
-  if (!s_flag) return;
-
-  // the last cluster selects: row = base + warp, rows 2p and 2p+1 share a CTA
-  const bool table = a.tbl_unique != nullptr;
-  const int k = a.k;
-  for (int base = rank * kGemvWarps; base < M; base += CL * kGemvWarps) {
-    const int row = base + warp;
-    if (row < M)
-      warp_select_row<VPL>(LdCG{a.logits + (size_t)row * E}, a.bias, E, k, a.act,
-                           a.out_idx + (size_t)row * k, a.out_w + (size_t)row * k,
-                           s_sel + warp * k);
-    if (table) {
-      __syncthreads();
-      if ((warp & 1) == 0 && row + 1 < M) {
-        const size_t gi = (size_t)(row >> 1);
-        warp_route_table_small(s_sel + warp * k, 2, k, a.tbl_unique + gi * 2 * k,
-                               a.tbl_mask + gi * 2 * k, a.tbl_map + gi * 2 * k, a.tbl_count + gi);
-      }
-      __syncthreads();
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Single-cluster small-M router (M <= 16, E <= 256). One cluster of E/16
 // CTAs holds all of W_gate in shared memory: CTA r owns experts
@@ -246,6 +82,31 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
 // CTA with st.async stores that complete on the receiver's mbarrier, whose
 // expected byte count the receiver set at start. No global scratch, no
 // atomics, no second cluster barrier.
+
+#ifdef GBR_PHASE_STAMPS
+// Measurement build only: %globaltimer stamps (ns) that thread 0 of each
+// CTA of the single-cluster kernel takes at phase boundaries, kept for the
+// last kStampCalls launches (slot = launch count of that CTA rank):
+//   0 entry, 1 W copies issued and dependents released, 2 wait on the
+//   preceding kernel returned, 3 W in shared memory, 4 warps' partials
+//   stored, 5 logits sent, 6 (selecting CTAs) this CTA's rows landed,
+//   7 row selected and stored.
+constexpr int kStampCalls = 256, kStampPhases = 8;
+__device__ unsigned long long g_stamps[kStampCalls][16][kStampPhases];
+__device__ unsigned g_stamp_seq[16];
+#define GBR_STAMP(slot, i)                                                  \
+  do {                                                                      \
+    if (threadIdx.x == 0) {                                                 \
+      unsigned long long t_;                                                \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_)::"memory");      \
+      g_stamps[slot][blockIdx.x][i] = t_;                                   \
+    }                                                                       \
+  } while (0)
+#else
+#define GBR_STAMP(slot, i) \
+  do {                     \
+  } while (0)
+#endif
 
 constexpr int k1cWarps = 16;
 constexpr int k1cBatch = 8;  // 32-element chunks of x held in registers per warp
@@ -356,9 +217,14 @@ __device__ __forceinline__ uint4 fp4_frag(uint32_t packed, uint8_t scale_code, c
 struct RowOwner {
   int CL;
   bool table;
-  __device__ __forceinline__ int cta(int m) const { return table ? (m >> 1) % CL : m % CL; }
+  uint32_t inv;  // (65536 + CL - 1) / CL: i / CL = (i * inv) >> 16 exactly for i < 512
+  __device__ __forceinline__ int div(int i) const { return (int)(((uint32_t)i * inv) >> 16); }
+  __device__ __forceinline__ int cta(int m) const {
+    const int i = table ? m >> 1 : m;
+    return i - CL * div(i);
+  }
   __device__ __forceinline__ int slot(int m) const {
-    return table ? 2 * ((m >> 1) / CL) + (m & 1) : m / CL;
+    return table ? 2 * div(m >> 1) + (m & 1) : div(m);
   }
   __device__ __forceinline__ int row(int c, int s) const {
     return table ? 2 * (c + CL * (s >> 1)) + (s & 1) : c + CL * s;
@@ -401,10 +267,15 @@ __global__ void __launch_bounds__(k1cWarps * 32)
   const int e0 = rank * 16;
   const int H = a.H, M = a.M, E = a.E;
   const bool table = a.tbl_unique != nullptr;
-  const RowOwner own{CL, table};
+  const RowOwner own{CL, table, (65536u + (uint32_t)CL - 1u) / (uint32_t)CL};
   const int nown = own.count(rank, M);
   const uint32_t bar = smem_u32(&s_bar), join = smem_u32(&s_join);
   const uint32_t wsm = smem_u32(s_w);
+#ifdef GBR_PHASE_STAMPS
+  const int stamp =
+      threadIdx.x == 0 ? (int)(atomicAdd(&g_stamp_seq[blockIdx.x], 1u) % kStampCalls) : 0;
+#endif
+  GBR_STAMP(stamp, 0);
 
   const int row_bytes = FP4 ? H / 2 : H * 2;
   const int scale_bytes = FP4 ? 16 * (H / 16) : 0;
@@ -430,8 +301,8 @@ __global__ void __launch_bounds__(k1cWarps * 32)
     }
   }
   __syncthreads();
-  // publish the barriers' initialisation; the matching wait comes just
-  // before the first remote store, long after every CTA has arrived here
+  // publish the barriers' initialisation (the matching wait follows the W
+  // copies' issue, before the wait on the preceding kernel)
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   if (tid < 17) {
     const uint64_t pol = policy_evict_first();
@@ -444,6 +315,11 @@ __global__ void __launch_bounds__(k1cWarps * 32)
     }
   }
   pdl_launch_dependents();
+  // every CTA of the cluster has initialised its barriers (they all arrived
+  // above): the remote stores below may target them. Waiting here keeps the
+  // cluster barrier off the chain that starts at the preceding kernel's end.
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  GBR_STAMP(stamp, 1);
   bool w_ok = true;
   if (PREDEC) {
     // W does not depend on the preceding kernel: decode it before the wait
@@ -461,6 +337,7 @@ __global__ void __launch_bounds__(k1cWarps * 32)
     __syncthreads();
   }
   pdl_wait();  // x and the outputs belong to the preceding kernel until here
+  GBR_STAMP(stamp, 2);
 
   const uint16_t* __restrict__ x = static_cast<const uint16_t*>(a.x);
   const int nchunk = H / 32;
@@ -485,7 +362,10 @@ __global__ void __launch_bounds__(k1cWarps * 32)
           xv[i][n] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + hoff));
       }
     }
-    if (!PREDEC && jb == 0) w_ok = mbar_wait_bounded(bar, 0, a.status);  // x loads in flight
+    if (!PREDEC && jb == 0) {
+      w_ok = mbar_wait_bounded(bar, 0, a.status);  // x loads in flight
+      GBR_STAMP(stamp, 3);
+    }
 #pragma unroll
     for (int i = 0; i < k1cBatch; ++i) {
       if (jb + i < cpw && w_ok) {
@@ -516,17 +396,23 @@ __global__ void __launch_bounds__(k1cWarps * 32)
     s_part[warp][n * 8 + 2 * t + 1][g + 8] = acc[n][3];
   }
   __syncthreads();
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  GBR_STAMP(stamp, 4);
   // sum the warps' partials in a fixed order; four experts of a row per
   // thread go to the CTA that selects the row
   for (int i = tid; i < 4 * M; i += k1cWarps * 32) {
     const int m = i >> 2, q = i & 3;
-    float4 v = *reinterpret_cast<const float4*>(&s_part[0][m][4 * q]);
+    float4 u[k1cWarps];
 #pragma unroll
-    for (int w = 1; w < k1cWarps; ++w) {
-      const float4 u = *reinterpret_cast<const float4*>(&s_part[w][m][4 * q]);
-      v.x += u.x, v.y += u.y, v.z += u.z, v.w += u.w;
+    for (int w = 0; w < k1cWarps; ++w) u[w] = *reinterpret_cast<const float4*>(&s_part[w][m][4 * q]);
+#pragma unroll
+    for (int h = k1cWarps / 2; h > 0; h >>= 1) {  // a fixed tree: warp w + warp w + h
+#pragma unroll
+      for (int w = 0; w < h; ++w) {
+        u[w].x += u[w + h].x, u[w].y += u[w + h].y;
+        u[w].z += u[w + h].z, u[w].w += u[w + h].w;
+      }
     }
+    float4 v = u[0];
     if (FP4) {
       v.x *= a.w_global, v.y *= a.w_global, v.z *= a.w_global, v.w *= a.w_global;
     }
@@ -542,8 +428,10 @@ __global__ void __launch_bounds__(k1cWarps * 32)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dbar) : "r"(join), "r"(dst_cta));
     st_async_v4(dst, v.x, v.y, v.z, v.w, dbar);
   }
+  GBR_STAMP(stamp, 5);
   if (nown == 0) return;  // no row to select; no CTA reads this one's shared memory
   if (!mbar_wait_cluster(join, 0, a.status)) return;
+  GBR_STAMP(stamp, 6);
 
   // warp s selects the CTA's row slot s; rows 2g and 2g+1 of a table's pair
   // sit in slots 2p and 2p + 1
@@ -553,12 +441,167 @@ __global__ void __launch_bounds__(k1cWarps * 32)
     warp_select_row<VPL>(LdPlain{&s_all[warp][0]}, a.bias, E, k, a.act,
                          a.out_idx + (size_t)row * k, a.out_w + (size_t)row * k,
                          s_sel + warp * k);
+  GBR_STAMP(stamp, 7);
   if (table) {
     __syncthreads();
     if ((warp & 1) == 0 && warp + 1 < nown) {
       const size_t gi = (size_t)(row >> 1);
       warp_route_table_small(s_sel + warp * k, 2, k, a.tbl_unique + gi * 2 * k,
                              a.tbl_mask + gi * 2 * k, a.tbl_map + gi * 2 * k, a.tbl_count + gi);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Split-cluster small-M router (M <= 64; used where the single-cluster
+// kernel is not, and for the logits-only half of the unfused A/B pair).
+// CTA (r, eg) owns expert group eg (16 experts) and the r-th of CL slices
+// of H; the CL CTAs of an expert group form a cluster. Each CTA bulk-copies
+// its 16 x H/CL slice of W into shared memory (L2 evict-first) before it
+// waits on the preceding kernel. Its 8 warps split the work by token tile
+// and chunk group: warp w takes the 8-token tile w % NT over every
+// (8/NT)-th 32-element chunk of the slice, so each warp issues all of its
+// x loads at once. The cluster sums its H slices over distributed shared
+// memory in a fixed order and writes the 16 x M logits to an L2-resident
+// buffer [M, E] (or the caller's logits tap); the cluster that arrives last
+// on a ticket selects, one warp per row across its CTAs, and resets the
+// ticket. The K permutation inside a 32-element chunk is the one of the
+// single-cluster kernel: thread t of a quad owns elements [8t, 8t+8), and
+// for MMA j its logical k slots {2t, 2t+1, 2t+8, 2t+9} are the physical
+// elements 8t + 4j + {0,1,2,3}, the same for W (A) and x (B).
+constexpr int kSplitWarps = 8;  // two CTAs fit an SM: the next call's CTAs can start early
+
+template <int NT, int VPL, bool SELECT>
+__global__ void __launch_bounds__(kSplitWarps * 32)
+    k_gemv_router(const RouterArgs a, int CL, int pitch) {
+  constexpr int NTOK = 8 * NT;
+  constexpr int NG = kSplitWarps / NT;  // chunk groups: warps per token tile
+  constexpr int kSplitXB = NG == 1 ? 16 : 8;  // x chunks per warp held in registers at once
+  extern __shared__ __align__(128) uint8_t s_w[];  // [16][pitch]: this CTA's W slice
+  __shared__ float s_part[NG][16][NTOK];
+  __shared__ float s_cta[16][NTOK];
+  __shared__ int32_t s_sel[kSplitWarps * kMaxK];
+  __shared__ uint32_t s_flag;
+  __shared__ __align__(8) uint64_t s_bar;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int rank = blockIdx.x;  // the grid's x extent equals the cluster size
+  const int e0 = blockIdx.y * 16;
+  const int H = a.H, M = a.M, E = a.E;
+  const int Hc = H / CL, nchunk = Hc / 32, h_begin = rank * Hc;
+  const int tile = warp % NT, cg = warp / NT;
+  const uint32_t bar = smem_u32(&s_bar);
+
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"((uint32_t)(16 * Hc * 2))
+                 : "memory");
+  }
+  __syncthreads();
+  if (tid < 16) {  // row tid of the slice: H/CL contiguous BF16 values
+    const uint16_t* src = static_cast<const uint16_t*>(a.w) + (size_t)(e0 + tid) * H + h_begin;
+    bulk_g2s(smem_u32(s_w) + tid * pitch, src, (uint32_t)(Hc * 2), bar, policy_evict_first());
+  }
+  pdl_launch_dependents();
+  pdl_wait();  // x, the scratch and the ticket belong to the preceding call until here
+
+  const uint16_t* __restrict__ x = static_cast<const uint16_t*>(a.x);
+  const int tok = tile * 8 + g;
+  const uint8_t* w0 = s_w + g * pitch + 16 * t;
+  const uint8_t* w1 = w0 + 8 * pitch;
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  bool w_ok = true, waited = false;
+  for (int cb = cg; cb < nchunk; cb += NG * kSplitXB) {
+    uint4 xv[kSplitXB];
+#pragma unroll
+    for (int i = 0; i < kSplitXB; ++i) {
+      const int c = cb + NG * i;
+      xv[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < nchunk && tok < M)
+        xv[i] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + h_begin + c * 32 + 8 * t));
+    }
+    if (!waited) {  // the x loads are in flight meanwhile
+      w_ok = mbar_wait_bounded(bar, 0, a.status);
+      waited = true;
+    }
+#pragma unroll
+    for (int i = 0; i < kSplitXB; ++i) {
+      const int c = cb + NG * i;
+      if (c < nchunk && w_ok) {
+        const uint4 wa = *reinterpret_cast<const uint4*>(w0 + c * 64);
+        const uint4 wb = *reinterpret_cast<const uint4*>(w1 + c * 64);
+        mma_bf16_16816(acc, wa.x, wb.x, wa.y, wb.y, xv[i].x, xv[i].y);
+        mma_bf16_16816(acc, wa.z, wb.z, wa.w, wb.w, xv[i].z, xv[i].w);
+      }
+    }
+  }
+  if (!waited) mbar_wait_bounded(bar, 0, a.status);  // never leave with the copy in flight
+
+  // accumulator layout: c0,c1 -> expert g, tokens 2t, 2t+1; c2,c3 -> expert g+8
+  s_part[cg][g][tile * 8 + 2 * t] = acc[0];
+  s_part[cg][g][tile * 8 + 2 * t + 1] = acc[1];
+  s_part[cg][g + 8][tile * 8 + 2 * t] = acc[2];
+  s_part[cg][g + 8][tile * 8 + 2 * t + 1] = acc[3];
+  __syncthreads();
+  for (int i = tid; i < 16 * NTOK; i += kSplitWarps * 32) {
+    const int el = i / NTOK, m = i % NTOK;
+    float v = s_part[0][el][m];
+#pragma unroll
+    for (int q = 1; q < NG; ++q) v += s_part[q][el][m];
+    s_cta[el][m] = v;
+  }
+  cluster_sync_all();
+
+  // cluster reduction over the CL slices of H; item i = m * 16 + el
+  for (int i = rank + CL * tid; i < 16 * M; i += CL * kSplitWarps * 32) {
+    const int m = i >> 4, el = i & 15;
+    float part[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) part[q] = q < CL ? dsmem_ld_f32(&s_cta[el][m], (uint32_t)q) : 0.0f;
+    float v = part[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) v += part[q];  // fixed order; absent slices add +0
+    a.logits[(size_t)m * E + e0 + el] = v;
+  }
+  if (!SELECT) {
+    cluster_sync_all();  // keep shared memory alive until every peer has read it
+    return;
+  }
+  // The cluster barrier (release/acquire) orders every peer's logits stores
+  // before rank 0's acq_rel arrival on the ticket; the arrivals form one
+  // release sequence, so the cluster that arrives last observes all logits
+  // and hands them to its peers through the next cluster barrier.
+  cluster_sync_all();
+  if (rank == 0 && tid == 0) {
+    const uint32_t old = atom_add_acq_rel_gpu(a.ticket, 1u);
+    const uint32_t last = (old == gridDim.y - 1) ? 1u : 0u;
+    if (last) atom_exch_relaxed_gpu(a.ticket, 0u);
+    for (int q = 0; q < CL; ++q) dsmem_st_u32(&s_flag, (uint32_t)q, last);
+  }
+  cluster_sync_all();
+  if (!s_flag) return;
+
+  // the last cluster selects: warp w of CTA r takes rows r*8 + w, then
+  // every CL*8 rows further; rows 2p and 2p+1 share a CTA
+  const bool table = a.tbl_unique != nullptr;
+  const int k = a.k;
+  for (int base = rank * kSplitWarps; base < M; base += CL * kSplitWarps) {
+    const int row = base + warp;
+    if (row < M)
+      warp_select_row<VPL>(LdCG{a.logits + (size_t)row * E}, a.bias, E, k, a.act,
+                           a.out_idx + (size_t)row * k, a.out_w + (size_t)row * k,
+                           s_sel + warp * k);
+    if (table) {
+      __syncthreads();
+      if ((warp & 1) == 0 && row + 1 < M) {
+        const size_t gi = (size_t)(row >> 1);
+        warp_route_table_small(s_sel + warp * k, 2, k, a.tbl_unique + gi * 2 * k,
+                               a.tbl_mask + gi * 2 * k, a.tbl_map + gi * 2 * k, a.tbl_count + gi);
+      }
+      __syncthreads();
     }
   }
 }
@@ -648,12 +691,46 @@ cudaError_t launch_ex(Kern kern, dim3 grid, dim3 block, int cluster, bool pdl, c
   return cudaLaunchKernelEx(&cfg, kern, a, extra);
 }
 
+// Row pitch of a CTA's W slice (H/CL BF16 values per row), padded to 64
+// (mod 128) bytes like the single-cluster kernel's rows.
+int split_pitch(int Hc) { return 2 * Hc + ((2 * Hc) % 128 == 0 ? 64 : 0); }
+
+template <class Kern>
+cudaError_t launch_split(Kern kern, const RouterArgs& a, int CL, bool pdl, cudaStream_t stream) {
+  const int pitch = split_pitch(a.H / CL);
+  const size_t dsmem = (size_t)16 * pitch;
+  if (dsmem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)dsmem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL, a.E / 16);
+  cfg.blockDim = dim3(kSplitWarps * 32);
+  cfg.dynamicSmemBytes = dsmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int n = 0;
+  attrs[n].id = cudaLaunchAttributeClusterDimension;
+  attrs[n].val.clusterDim.x = CL;
+  attrs[n].val.clusterDim.y = 1;
+  attrs[n].val.clusterDim.z = 1;
+  ++n;
+  if (pdl) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, a, CL, pitch);
+}
+
 template <int NT, bool SELECT>
 cudaError_t gemv_dispatch_vpl(const RouterArgs& a, int CL, bool pdl, cudaStream_t s) {
-  const dim3 grid(CL, a.E / 16), block(kGemvWarps * 32);
-  if (a.E <= 128) return launch_ex(k_gemv_router<NT, 4, SELECT>, grid, block, CL, pdl, s, a, CL);
-  if (a.E <= 256) return launch_ex(k_gemv_router<NT, 8, SELECT>, grid, block, CL, pdl, s, a, CL);
-  return launch_ex(k_gemv_router<NT, 16, SELECT>, grid, block, CL, pdl, s, a, CL);
+  if (a.E <= 128) return launch_split(k_gemv_router<NT, 4, SELECT>, a, CL, pdl, s);
+  if (a.E <= 256) return launch_split(k_gemv_router<NT, 8, SELECT>, a, CL, pdl, s);
+  return launch_split(k_gemv_router<NT, 16, SELECT>, a, CL, pdl, s);
 }
 
 template <bool SELECT>
@@ -761,6 +838,23 @@ bool gemv1c_eligible(int M, int H, int E, bool fp4) {
   cache[key] = fits;
   return fits;
 }
+
+#ifdef GBR_PHASE_STAMPS
+// Copies the stamps [kStampCalls][16][kStampPhases] to host memory and
+// clears the launch counters (measurement build only).
+extern "C" int router_phase_stamps(unsigned long long* host, int* calls, int* ctas, int* phases) {
+  *calls = kStampCalls, *ctas = 16, *phases = kStampPhases;
+  if (!host) return 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return 3;
+  if (cudaMemcpyFromSymbol(host, g_stamps, sizeof(g_stamps)) != cudaSuccess) return 3;
+  // the last selection's sub-phase stamps of each CTA rank follow
+  if (cudaMemcpyFromSymbol(host + kStampCalls * 16 * kStampPhases, g_sel_stamps,
+                           sizeof(g_sel_stamps)) != cudaSuccess)
+    return 3;
+  static const unsigned zero[16] = {};
+  return cudaMemcpyToSymbol(g_stamp_seq, zero, sizeof(zero)) == cudaSuccess ? 0 : 3;
+}
+#endif
 
 cudaError_t launch_gemv1c(const RouterArgs& a, bool pdl, cudaStream_t stream) {
   bool unused = false;

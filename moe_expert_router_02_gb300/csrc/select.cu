@@ -75,6 +75,85 @@ __global__ void __launch_bounds__(kTblWarps * 32)
   }
 }
 
+// Groups of n = T*k <= 16 entries, one group per lane: a warp stages its 32
+// groups' ids in shared memory (coalesced), each lane deduplicates its
+// group with compares on register copies (static indices), writes the
+// table rows into its own shared-memory row, and the warp stores all rows
+// coalesced. Rows are padded to an odd stride (no bank conflicts).
+constexpr int kLaneWarps = 8;
+constexpr int kLaneMax = 16;
+constexpr int kLaneStride = kLaneMax + 1;
+
+__global__ void __launch_bounds__(kLaneWarps * 32)
+    k_route_table_lane(const int32_t* __restrict__ idx, int G, int T, int k,
+                       int32_t* __restrict__ unique, uint8_t* __restrict__ mask,
+                       uint8_t* __restrict__ map, int32_t* __restrict__ count) {
+  __shared__ int32_t s_in[kLaneWarps][32 * kLaneStride];
+  __shared__ int32_t s_un[kLaneWarps][32 * kLaneStride];
+  __shared__ uint8_t s_mk[kLaneWarps][32 * kLaneStride];
+  __shared__ uint8_t s_mp[kLaneWarps][32 * kLaneStride];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = T * k;
+  const long long g0 = ((long long)blockIdx.x * kLaneWarps + warp) * 32;
+  if (g0 >= G) return;  // whole warps leave together
+  const int ng = G - g0 < 32 ? (int)(G - g0) : 32;
+  const int total = ng * n;
+  const uint32_t inv_n = (65536u + (uint32_t)n - 1u) / (uint32_t)n;  // i / n = (i * inv_n) >> 16, i < 512
+  int32_t* in = s_in[warp];
+  const int32_t* src = idx + g0 * n;
+  for (int i = lane; i < total; i += 32) {
+    const int gl = (int)(((uint32_t)i * inv_n) >> 16);
+    in[gl * kLaneStride + (i - gl * n)] = __ldg(src + i);
+  }
+  __syncwarp();
+  const int row = lane * kLaneStride;
+  int32_t v[kLaneMax];
+#pragma unroll
+  for (int p = 0; p < kLaneMax; ++p) v[p] = p < n ? in[row + p] : 0;
+  // first occurrence of each entry's id, and the set of first occurrences
+  int fp[kLaneMax];
+  uint32_t F = 0u;
+#pragma unroll
+  for (int p = 0; p < kLaneMax; ++p) {
+    int f = p;
+#pragma unroll
+    for (int q = p - 1; q >= 0; --q) f = (v[q] == v[p]) ? q : f;
+    fp[p] = f;
+    if (p < n && f == p) F |= 1u << p;
+  }
+  int32_t* un = s_un[warp] + row;
+  uint8_t* mk = s_mk[warp] + row;
+  uint8_t* mp = s_mp[warp] + row;
+#pragma unroll
+  for (int u = 0; u < kLaneMax; ++u) {
+    if (u < n) {
+      un[u] = -1;
+      mk[u] = 0;
+    }
+  }
+  int tok = 0, rem = 0;  // token of entry p = p / k
+#pragma unroll
+  for (int p = 0; p < kLaneMax; ++p) {
+    if (p < n) {
+      const int u = __popc(F & ((1u << fp[p]) - 1u));  // unique position of the id
+      mp[p] = (uint8_t)u;
+      if (fp[p] == p) un[u] = v[p];
+      mk[u] = (uint8_t)(mk[u] | (1u << tok));
+      if (++rem == k) rem = 0, ++tok;
+    }
+  }
+  __syncwarp();
+  const long long o = g0 * n;
+  for (int i = lane; i < total; i += 32) {
+    const int gl = (int)(((uint32_t)i * inv_n) >> 16);
+    const int e = gl * kLaneStride + (i - gl * n);
+    unique[o + i] = s_un[warp][e];
+    mask[o + i] = s_mk[warp][e];
+    map[o + i] = s_mp[warp][e];
+  }
+  if (lane < ng) count[g0 + lane] = __popc(F);
+}
+
 __global__ void k_near_tie_keys(const float* __restrict__ z, const float* __restrict__ bias, int n,
                                 int act, float* __restrict__ hi, float* __restrict__ lo) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
@@ -107,7 +186,12 @@ cudaError_t launch_select(const float* logits, const float* bias, int M, int E, 
 cudaError_t launch_route_table(const int32_t* idx, int groups, int T, int k, int32_t* unique,
                                uint8_t* mask, uint8_t* map, int32_t* count, cudaStream_t stream) {
   const dim3 block(kTblWarps * 32);
-  if (T * k <= 32) {
+  if (T * k <= kLaneMax) {
+    const long long warps = (groups + 31) / 32;
+    const dim3 grid((unsigned)((warps + kLaneWarps - 1) / kLaneWarps));
+    k_route_table_lane<<<grid, dim3(kLaneWarps * 32), 0, stream>>>(idx, groups, T, k, unique, mask,
+                                                                   map, count);
+  } else if (T * k <= 32) {
     const long long per_warp = (long long)(32 / (T * k)) * kTblChunks;
     const long long warps = (groups + per_warp - 1) / per_warp;
     const dim3 grid((unsigned)((warps + kTblWarps - 1) / kTblWarps));

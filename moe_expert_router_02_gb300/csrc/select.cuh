@@ -34,6 +34,28 @@
 
 namespace gbr {
 
+#ifdef GBR_PHASE_STAMPS
+// Measurement build only: lane 0 of a selecting warp of CTA b < 16 stamps
+// %globaltimer at the selection's sub-phases (0 keys loaded and packed,
+// 1 sorted, 2 k+1 rounds done, 3 weights computed, 4 stored); the last
+// selection of each CTA rank wins.
+namespace {
+__device__ unsigned long long g_sel_stamps[16][5];
+}
+#define SEL_STAMP(i)                                                           \
+  do {                                                                         \
+    if ((threadIdx.x & 31) == 0 && blockIdx.x < 16) {                          \
+      unsigned long long t_;                                                   \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_)::"memory");         \
+      g_sel_stamps[blockIdx.x][i] = t_;                                        \
+    }                                                                          \
+  } while (0)
+#else
+#define SEL_STAMP(i) \
+  do {               \
+  } while (0)
+#endif
+
 struct LdPlain {  // generic-address loads (shared memory or read-only global)
   const float* p;
   __device__ __forceinline__ float operator()(int e) const { return p[e]; }
@@ -351,10 +373,13 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
       }
     }
   }
+  SEL_STAMP(0);
   sort_desc<VPL>(pk);
+  SEL_STAMP(1);
 
-  // k+1 rounds: the (k+1)-th key is kept for the gap test.
-  const int kk = min(k + 1, E);
+  // k+1 rounds for the biased scores: the (k+1)-th key is kept for the gap
+  // test; softmax has none and stops at k.
+  const int kk = act == ACT_SOFTMAX ? k : min(k + 1, E);
   int sel_idx = -1;
   float sel_key = 0.0f;
   for (int r = 0; r < kk; ++r) {
@@ -373,6 +398,7 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
     }
   }
 
+  SEL_STAMP(2);
   if (act != ACT_SOFTMAX) {
     // FP32 key error bound; non-negative floats order like their bit patterns
     const float amax_w = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(amax)));
@@ -435,11 +461,13 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
   sum += __shfl_xor_sync(kFull, sum, 4);
   sum += __shfl_xor_sync(kFull, sum, 2);
   sum += __shfl_xor_sync(kFull, sum, 1);
+  SEL_STAMP(3);
   if (lane < k) {
     out_idx[lane] = sel_idx;
     out_w[lane] = (sum > 0.0f) ? s / sum : 1.0f / (float)k;
     if (sel_out) sel_out[lane] = sel_idx;
   }
+  SEL_STAMP(4);
 }
 
 template <int VPL, class Ld>
