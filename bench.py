@@ -36,7 +36,7 @@ LAYERS = 40          # router calls per decode token (one per MoE layer)
 # decode workload, valid only for the sources that kernel is built from: its
 # file (kernel and launcher) and the headers that file includes.
 DECODE_SOURCES = ("gemv.cu", "kernels.h", "select.cuh", "dfkey.cuh", "common.cuh")
-TRAFFIC = {"decode": {"bytes": 1160021, "src_sha": "8d30b576444a97d5"}}
+TRAFFIC = {"decode": {"bytes": 1159680, "src_sha": "7283978b2d5ec852"}}
 
 
 def kernel_src_sha(files=DECODE_SOURCES):
@@ -293,6 +293,48 @@ def oracle_tokens_per_s(cfg, M, budget_s=10.0, min_calls=1, w_dtype=None, rows=N
     return case["M"] * calls / dt, calls, dt
 
 
+def host_cores():
+    """Cores this process may run on (its affinity set)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_prefill(cfg, budget_s=10.0):
+    """The oracle on the prefill workload (M=16384, H=7168, E=256, k=8,
+    sqrt-softplus + bias, BF16): 256 rows on one core, and row slices on
+    every core of the affinity set at once (threads: the oracle's C code
+    runs without the interpreter lock), each extrapolated to all 16384 rows.
+    The oracle's arithmetic is untouched; only its rows are split."""
+    import concurrent.futures as cf
+
+    import oracle
+    from moe_expert_router_02_gb300 import synth
+    case = synth.make_case(cfg, seed=0)
+    M = case["M"]
+
+    def rows(a, b):
+        return dict(case, M=b - a, x=case["x"][a:b])
+
+    t0 = time.perf_counter()
+    oracle.router(rows(0, 256))
+    one = time.perf_counter() - t0
+    cores = host_cores()
+    # as many rows per core as one core did in about budget_s / 2 seconds
+    per = max(16, min(M // cores, int(256 * (budget_s / 2) / max(one, 1e-3))))
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        list(ex.map(lambda c: oracle.router(rows(c * per, (c + 1) * per)), range(cores)))
+    par = time.perf_counter() - t0
+    return {"unit": "router tokens/s", "single_core": 256 / one,
+            "single_core_call_s_extrapolated": one * M / 256,
+            "all_cores": cores * per / par, "all_cores_call_s_extrapolated": par * M / (cores * per),
+            "cores": cores,
+            "sample": f"256 rows on one core ({one:.1f} s); {per} rows on each of {cores} cores "
+                      f"at once ({par:.1f} s)"}
+
+
 # ---------------------------------------------------------------- main arms
 def run_ours(args, rank, world, local):
     import torch
@@ -326,18 +368,33 @@ def run_ours(args, rank, world, local):
     algo = head.algo_bytes()
     achieved = algo / (us_call * 1e-6) / 1e9
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: the 40 layer calls
+    # are router_forward calls captured once as a CUDA graph (how a decode
+    # loop issues them); every step copies its x from pinned host memory,
+    # replays the calls and copies the ids and weights back
     x_host = torch.empty((LAYERS, M, head.H), dtype=torch.int16).pin_memory()
     x_host.copy_(head.x.cpu())
     idx_host = torch.empty((LAYERS, M, head.k), dtype=torch.int32).pin_memory()
     w_host = torch.empty((LAYERS, M, head.k), dtype=torch.float32).pin_memory()
     s = head.stream
+    n_w = head.W.shape[0]
+    with torch.cuda.stream(s):
+        for c in range(LAYERS):  # the library workspace exists before capture
+            R.router_forward(head.x[c], head.W[c], None, M, head.H, head.E, head.k, head.act,
+                             head.idx[c], head.w[c], stream=s)
+    s.synchronize()
+    e2e_graphs = []
+    for gi in range(head.n_graphs):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for c in range(LAYERS):
+                R.router_forward(head.x[c], head.W[(gi * LAYERS + c) % n_w], None, M, head.H,
+                                 head.E, head.k, head.act, head.idx[c], head.w[c], stream=s)
+        e2e_graphs.append(g)
 
     def e2e_step(i):
         head.x.copy_(x_host, non_blocking=True)
-        for c in range(LAYERS):
-            R.router_forward(head.x[c], head.W[(i * LAYERS + c) % head.W.shape[0]], None, M,
-                             head.H, head.E, head.k, head.act, head.idx[c], head.w[c], stream=s)
+        e2e_graphs[i % len(e2e_graphs)].replay()
         idx_host.copy_(head.idx, non_blocking=True)
         w_host.copy_(head.w, non_blocking=True)
 
@@ -352,6 +409,7 @@ def run_ours(args, rank, world, local):
         e2e_s = time.perf_counter() - t0
     e2e_value = max_over_ranks(e2e_s, world)
     e2e_value = tokens / e2e_value
+    del e2e_graphs
 
     detail = {}
     if not args.quick and rank == 0:
@@ -362,7 +420,10 @@ def run_ours(args, rank, world, local):
         tps, calls, dt = oracle_tokens_per_s(C["C1"], M, budget_s=args.cpu_budget)
         cpu = {"value": tps, "unit": "router tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{calls} oracle router calls at M=8, H=2048, E=256, k=8 "
-                         f"({dt:.1f} s, single thread)"}
+                         f"({dt:.1f} s, single thread)",
+               "host_cores": host_cores()}
+        if not args.quick:
+            cpu["prefill"] = oracle_prefill(C["C3"], args.cpu_budget)
 
     line = {
         "metric": "router tokens/s (decode M=8, H=2048, E=256, top-8 softmax, 40 layers)",
@@ -418,6 +479,26 @@ def run_detail(args, peaks):
 
     for M in (1, 2, 8):
         record(f"C1_softmax_M{M}", RouterSet(C["C1"], M, LAYERS))
+    # floors of a dependent call with the single-cluster kernel's launch shape
+    # (include/gbrouter_diag.h): a chain of launches that only release and
+    # wait, and one that also reads the call's x (8 x 2048 BF16)
+    try:
+        xs = torch.zeros((8, C["C1"]["H"]), dtype=torch.int16, device="cuda")
+        sink = torch.zeros(16, dtype=torch.int32, device="cuda")
+        fs = torch.cuda.Stream()
+        for kind, name in ((0, "C1_floor_pdl_chain"), (1, "C1_floor_pdl_chain_read_x")):
+            with torch.cuda.stream(fs):
+                R.diag_chain(kind, LAYERS, xs, sink, fs)
+            fs.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=fs):
+                R.diag_chain(kind, LAYERS, xs, sink, fs)
+            out[name] = {"us_per_launch": time_graph(g.replay, 20) * 1e3 / LAYERS}
+        if "C1_softmax_M8" in out:
+            out["C1_M8_us_above_read_x_floor"] = (out["C1_softmax_M8"]["us_per_call_pipelined"] -
+                                                 out["C1_floor_pdl_chain_read_x"]["us_per_launch"])
+    except Exception as e:  # a detail row never costs the headline line
+        out["C1_floor"] = {"error": str(e)[:200]}
     record("C1_softmax_M8_unfused", RouterSet(C["C1"], 8, LAYERS, flags=R.GBR_FLAG_UNFUSED))
     for M in (1, 16, 64):
         record(f"C2_sqrtsoftplus_bias_M{M}", RouterSet(C["C2"], M, LAYERS))
@@ -499,12 +580,136 @@ def run_only(args):
         "prefill_nvfp4": lambda: RouterSet(C["C3"], C["C3"]["M"], 1, w_dtype=synth.NVFP4,
                                            pool_bytes=0),
     }
+    if args.only in ("table_1e5", "gather_1e3"):
+        from moe_expert_router_02_gb300 import router as R
+        k = C["C4"]["k"]
+        G = C["C4"]["table_groups"] if args.only == "table_1e5" else 1000
+        idx = dev(synth.table_pairs(G, k, 256, seed=0))
+        tb = (torch.empty((G, 2 * k), dtype=torch.int32, device="cuda"),
+              torch.empty((G, 2 * k), dtype=torch.uint8, device="cuda"),
+              torch.empty((G, 2, k), dtype=torch.uint8, device="cuda"),
+              torch.empty((G,), dtype=torch.int32, device="cuda"))
+        if args.only == "table_1e5":
+            fn = lambda: R.route_table(idx, G, 2, k, *tb)  # noqa: E731
+        else:
+            D = C["C4"]["H"]
+            R.route_table(idx, G, 2, k, *tb)
+            y, w, sh = synth.gather_inputs(G, k, D, seed=0)
+            yd, wd, sd = dev(y.view(np.int16)), dev(w), dev(sh.view(np.int16))
+            od = torch.empty((G, 2, D), dtype=torch.int16, device="cuda")
+            fn = lambda: R.route_gather_add(yd, tb[2], wd, sd, G, 2, k, D, od)  # noqa: E731
+        ms = time_graph(fn, args.steps, warm=args.warmup)
+        print(json.dumps({"workload": args.only, "us_per_call": ms * 1e3, "steps": args.steps}))
+        torch.cuda.synchronize()
+        return
     rs = table[args.only]()
     rs.capture()
     ms = time_graph(rs.step, args.steps, warm=args.warmup)
     print(json.dumps({"workload": args.only, "us_per_call": ms * 1e3 / rs.calls,
                       "calls_per_step": rs.calls, "steps": args.steps}))
     torch.cuda.synchronize()
+
+
+def run_phase_stamps(args):
+    """Per-phase latency of the decode kernel from the measurement build's
+    %globaltimer stamps (moe_expert_router_02_gb300/build.py, variant
+    "stamps"): the 40-call decode graph replayed, then the median over calls
+    of each phase (ns). Prints one JSON line."""
+    import torch
+
+    from moe_expert_router_02_gb300 import router as R
+    from moe_expert_router_02_gb300 import synth
+    R.use_variant("stamps")
+    M = args.stamps_m
+    rs = RouterSet(synth.CONFIGS["C1"], M, LAYERS)
+    rs.capture()
+    for _ in range(args.warmup):
+        rs.step()
+    torch.cuda.synchronize()
+    R.phase_stamps()  # clears the launch counters
+    reps = 6  # 240 calls, inside the 256 stamp slots
+    for _ in range(reps):
+        rs.step()
+    torch.cuda.synchronize()
+    st, sel = R.phase_stamps()
+    st, sel = st.astype(np.int64), sel.astype(np.int64)
+    n = reps * LAYERS
+    own = [c for c in range(16) if c < M]  # CTAs that select a row (no table)
+    ph = {k: [] for k in ("prev_end_to_wait_return", "wait_return_to_w_ready",
+                          "w_ready_to_partials", "partials_to_sent", "sent_to_rows_landed",
+                          "rows_landed_to_selected", "wait_return_to_last_selected",
+                          "call_period", "start_before_prev_end")}
+    for c in range(1, n):
+        cur, prev = st[c], st[c - 1]
+        prev_end = prev[own, 7].max()
+        w2 = cur[:, 2].min()
+        ph["prev_end_to_wait_return"].append(w2 - prev_end)
+        ph["wait_return_to_w_ready"].append(np.median(cur[:, 3] - cur[:, 2]))
+        ph["w_ready_to_partials"].append(np.median(cur[:, 4] - cur[:, 3]))
+        ph["partials_to_sent"].append(np.median(cur[:, 5] - cur[:, 4]))
+        ph["sent_to_rows_landed"].append(np.median(cur[own, 6] - cur[:, 5].max()))
+        ph["rows_landed_to_selected"].append(np.median(cur[own, 7] - cur[own, 6]))
+        ph["wait_return_to_last_selected"].append(cur[own, 7].max() - w2)
+        ph["call_period"].append(cur[own, 7].max() - prev_end)
+        ph["start_before_prev_end"].append(prev_end - cur[:, 0].min())
+    res = {k: float(np.median(v)) for k, v in ph.items()}
+    # the last call's selection, sub-phase by sub-phase (selecting CTAs)
+    sub = np.diff(sel[own], axis=1)
+    res_sel = {n_: float(np.median(sub[:, i])) for i, n_ in
+               enumerate(("sort", "rounds", "weights", "stores"))}
+    res_sel["entry_to_packed"] = float(np.median(sel[own, 0] - st[n - 1][own, 6]))
+    print(json.dumps({"workload": f"decode M={M}, H=2048, E=256, k=8, 40-call graph",
+                      "calls": n - 1, "median_ns": res, "selection_ns": res_sel}))
+
+
+def run_phase_stamps_prefill(args):
+    """Per-CTA phase timeline of the prefill kernel (measurement build) on
+    the M=16384, H=7168, E=256, k=8 sqrt-softplus + bias workload: each
+    phase's median and largest time from the launch's first CTA start (us),
+    and the CTAs that re-ranked near ties. Prints one JSON line."""
+    import torch
+
+    from moe_expert_router_02_gb300 import router as R
+    from moe_expert_router_02_gb300 import synth
+    R.use_variant("stamps")
+    cfg = synth.CONFIGS["C3"]
+    w_dtype = synth.NVFP4 if args.stamps_nvfp4 else None
+    rs = RouterSet(cfg, args.stamps_prefill_m, 1, w_dtype=w_dtype, pool_bytes=0)
+    rs.capture()
+    out = []
+    for rep in range(args.steps):
+        rs.step()
+        torch.cuda.synchronize()
+        st = R.tc_phase_stamps().astype(np.int64)
+        live = st[:, 0] > 0
+        st = st[live]
+        t0 = st[:, 0].min()
+        names = ["entry", "setup", "epi_setup", "acc_complete", "partials_added", "pass_a",
+                 "pass_bc", "merged", "stored", "cta_end"]
+        rel = (st[:, :10] - t0) / 1e3
+        ent = {n: {"median": float(np.median(rel[:, i])), "max": float(rel[:, i].max())}
+               for i, n in enumerate(names)}
+        fm = st[:, 11][st[:, 11] > 0]
+        ent["first_mma"] = {"median": float(np.median((fm - t0) / 1e3)),
+                            "max": float(((fm - t0) / 1e3).max())}
+        fin = st[:, 15] > 0  # CTAs that finished a tile (ran passes A-C)
+        for i, n_ in ((12, "threshold"), (13, "pass_b"), (14, "pooled_act"), (15, "inserted")):
+            ent[n_] = {"median": float(np.median((st[fin, i] - t0) / 1e3)),
+                       "max": float(((st[fin, i] - t0) / 1e3).max())}
+        ent["cand_thread0"] = {"median": float(np.median(st[fin, 16])),
+                               "max": int(st[fin, 16].max())}
+        ent["cand_warp0_total"] = {"median": float(np.median(st[fin, 17])),
+                                   "max": int(st[fin, 17].max())}
+        ref = np.nonzero(st[:, 10] == 1)[0]
+        ent["refined_ctas"] = [{"cta": int(c), "end": float(rel[c, 9])} for c in ref]
+        ent["ctas"] = int(live.sum())
+        ent["slowest"] = [{"cta": int(c), "end": float(rel[c, 9]),
+                           "acc": float(rel[c, 3]), "refined": int(st[c, 10])}
+                          for c in np.argsort(-rel[:, 9])[:6]]
+        out.append(ent)
+    print(json.dumps({"workload": f"prefill M={args.stamps_prefill_m}, H=7168, E=256, k=8, "
+                                  f"sqrt-softplus + bias, {'NVFP4' if w_dtype else 'BF16'} W",
+                      "launches": out}))
 
 
 def run_reference(args, rank, world):
@@ -551,13 +756,26 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only, no per-config detail")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-calls", type=int, default=8)
+    ap.add_argument("--phase-stamps", action="store_true",
+                    help="per-phase latency of the decode kernel (measurement build)")
+    ap.add_argument("--stamps-m", type=int, default=8)
+    ap.add_argument("--phase-stamps-prefill", action="store_true",
+                    help="per-CTA phase timeline of the prefill kernel (measurement build)")
+    ap.add_argument("--stamps-prefill-m", type=int, default=16384)
+    ap.add_argument("--stamps-nvfp4", action="store_true")
     ap.add_argument("--only", default=None,
                     choices=["decode", "decode_m1", "sqrtsoftplus_m64", "m2_table",
-                             "prefill_bf16", "prefill_nvfp4"],
+                             "prefill_bf16", "prefill_nvfp4", "table_1e5", "gather_1e3"],
                     help="run one workload's calls only (profiling)")
     args = ap.parse_args()
     if args.only:
         run_only(args)
+        return
+    if args.phase_stamps:
+        run_phase_stamps(args)
+        return
+    if args.phase_stamps_prefill:
+        run_phase_stamps_prefill(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -3,6 +3,11 @@
 Each ``csrc/*.cu`` compiles to an object in parallel, then nvcc links the
 shared library next to this file. Rebuilds only when a source or header is
 newer than the library.
+
+``build(variant="stamps")`` builds the measurement variant
+``libgbrouter_stamps.so`` from the same sources with ``-DGBR_PHASE_STAMPS``
+(per-phase timestamps in the single-cluster kernel); nothing loads it
+unless asked to.
 """
 from __future__ import annotations
 
@@ -39,23 +44,35 @@ def _deps():
         glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB):
+VARIANTS = {None: ("libgbrouter.so", "_build", []),
+            "stamps": ("libgbrouter_stamps.so", "_build_stamps", ["-DGBR_PHASE_STAMPS"])}
+
+
+def lib_path(variant=None) -> str:
+    return os.path.join(HERE, VARIANTS[variant][0])
+
+
+def is_stale(variant=None) -> bool:
+    lib = lib_path(variant)
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not is_stale():
+def build(force: bool = False, verbose: bool = False, variant=None) -> str:
+    LIB = lib_path(variant)
+    if not force and not is_stale(variant):
         return LIB
     nvcc = _nvcc()
-    os.makedirs(OBJ_DIR, exist_ok=True)
+    obj_dir = os.path.join(HERE, VARIANTS[variant][1])
+    defines = VARIANTS[variant][2]
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *defines, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")
@@ -76,4 +93,5 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                variant="stamps" if "--stamps" in sys.argv else None))

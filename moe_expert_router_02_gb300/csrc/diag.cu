@@ -1,0 +1,77 @@
+// Floors for the dependent launch chain of the small-M router: chains of
+// kernels with the router's launch shape (one cluster of 16 CTAs x 512
+// threads, programmatic dependent launch) that do nothing but the parts of
+// a router call that cannot overlap the preceding kernel. A router call
+// minus such a floor is the time its own work adds.
+#include <cuda_runtime.h>
+
+#include "../../include/gbrouter_diag.h"
+#include "common.cuh"
+
+namespace gbr {
+namespace {
+
+constexpr int kDiagCtas = 16, kDiagThreads = 512;
+
+// Releases the next kernel, then waits for the preceding one.
+__global__ void __launch_bounds__(kDiagThreads) k_diag_wait_only() {
+  pdl_launch_dependents();
+  pdl_wait();
+}
+
+// As above, then reads x [M, H] BF16 the way the single-cluster router does
+// (every CTA reads all of it, 16-byte loads spread over its warps), folds it
+// to one word per CTA and stores that.
+__global__ void __launch_bounds__(kDiagThreads)
+    k_diag_read_x(const uint4* __restrict__ x, int n16, unsigned* sink) {
+  pdl_launch_dependents();
+  pdl_wait();
+  unsigned f = 0;
+  for (int i = threadIdx.x; i < n16; i += kDiagThreads) {
+    const uint4 v = __ldg(x + i);
+    f ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+  f = __reduce_xor_sync(kFull, f);
+  if ((threadIdx.x & 31) == 0) atomicXor(sink + blockIdx.x, f);
+}
+
+cudaError_t launch_one(int kind, const void* x, int n16, unsigned* sink, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kDiagCtas);
+  cfg.blockDim = dim3(kDiagThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kDiagCtas;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  if (kind == 0) return cudaLaunchKernelEx(&cfg, k_diag_wait_only);
+  return cudaLaunchKernelEx(&cfg, k_diag_read_x, static_cast<const uint4*>(x), n16, sink);
+}
+
+}  // namespace
+}  // namespace gbr
+
+extern "C" int gbr_diag_chain(int kind, int n, const void* x, size_t x_bytes, unsigned* sink,
+                              cudaStream_t stream) {
+  if (n < 0 || (kind != 0 && kind != 1) || !sink) return 1;
+  if (kind == 1 && (!x || x_bytes % 16 != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0))
+    return 1;
+  static bool attr_set = false;
+  if (!attr_set) {
+    // a 16-CTA cluster is a non-portable size
+    if (cudaFuncSetAttribute(gbr::k_diag_wait_only, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) != cudaSuccess ||
+        cudaFuncSetAttribute(gbr::k_diag_read_x, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) != cudaSuccess)
+      return 3;
+    attr_set = true;
+  }
+  for (int i = 0; i < n; ++i)
+    if (gbr::launch_one(kind, x, (int)(x_bytes / 16), sink, stream) != cudaSuccess) return 3;
+  return 0;
+}

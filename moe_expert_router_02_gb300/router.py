@@ -24,7 +24,7 @@ GBR_REGIME_GENERIC, GBR_REGIME_GEMV, GBR_REGIME_TC, GBR_REGIME_UNFUSED, GBR_REGI
 
 EXPORTS = ("router_forward", "router_forward_ex", "router_workspace_size", "router_regime",
            "router_tc_groups", "router_select", "route_table", "router_strerror", "router_device_status",
-           "router_forward_noalloc", "router_near_tie_keys", "route_gather_add")
+           "router_forward_noalloc", "router_near_tie_keys", "route_gather_add", "gbr_diag_chain")
 
 
 class RouterError(RuntimeError):
@@ -46,12 +46,26 @@ _lock = threading.Lock()
 _lib = None
 
 
+_variant = None
+
+
+def use_variant(variant) -> None:
+    """Load the named build variant (``"stamps"``: the measurement build with
+    per-phase timestamps) instead of the library; call before the first
+    router call of the process."""
+    global _variant
+    with _lock:
+        if _lib is not None:
+            raise RuntimeError("the router library is already loaded")
+        _variant = variant
+
+
 def lib() -> ctypes.CDLL:
     """Load (building first if stale) the in-tree ``libgbrouter.so``."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build()
+            path = _build.build(variant=_variant)
             L = ctypes.CDLL(path)
             P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             L.router_forward.argtypes = [P, P, P, I, I, I, I, I, P, P, P]
@@ -69,6 +83,13 @@ def lib() -> ctypes.CDLL:
             L.router_strerror.argtypes = [I]
             L.router_strerror.restype = ctypes.c_char_p
             L.router_device_status.argtypes = [I]
+            L.gbr_diag_chain.argtypes = [I, I, P, S, P, P]
+            L.gbr_diag_chain.restype = I
+            if _variant == "stamps":
+                L.router_phase_stamps.argtypes = [P, P, P, P]
+                L.router_phase_stamps.restype = I
+                L.router_tc_phase_stamps.argtypes = [P, P, P]
+                L.router_tc_phase_stamps.restype = I
             for f in (L.router_forward, L.router_forward_ex, L.router_regime, L.router_tc_groups,
                       L.router_select,
                       L.route_table, L.router_device_status, L.router_forward_noalloc,
@@ -176,3 +197,42 @@ def route_gather_add(y, mp, w, shared, groups, tokens_per_group, k, D, out, stre
 
 def router_device_status(clear: bool = False) -> int:
     return lib().router_device_status(1 if clear else 0)
+
+
+def diag_chain(kind, n, x, sink, stream=None):
+    """Launch-chain floor (``include/gbrouter_diag.h``): n PDL launches of the
+    single-cluster router's shape; kind 0 waits only, kind 1 also reads x."""
+    xb = 0 if x is None else x.numel() * x.element_size()
+    rc = lib().gbr_diag_chain(int(kind), int(n), _ptr(x), xb, _ptr(sink), _stream(stream))
+    if rc != 0:
+        raise RuntimeError(f"gbr_diag_chain failed ({rc})")
+
+
+def phase_stamps():
+    """Measurement build only: the single-cluster kernel's phase stamps as a
+    numpy array [calls, ctas, phases] of %globaltimer ns (0 = not stamped),
+    and the last selection's sub-phase stamps per CTA rank [16, 5]."""
+    import numpy as np
+    L = lib()
+    c, t, p = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    L.router_phase_stamps(None, ctypes.byref(c), ctypes.byref(t), ctypes.byref(p))
+    n = c.value * t.value * p.value
+    buf = np.zeros(n + 16 * 5, dtype=np.uint64)
+    if L.router_phase_stamps(buf.ctypes.data_as(ctypes.c_void_p), ctypes.byref(c), ctypes.byref(t),
+                             ctypes.byref(p)) != 0:
+        raise RuntimeError("router_phase_stamps failed")
+    return buf[:n].reshape(c.value, t.value, p.value), buf[n:].reshape(16, 5)
+
+
+def tc_phase_stamps():
+    """Measurement build only: the last prefill launch's phase stamps as a
+    numpy array [ctas, phases] (%globaltimer ns; see the prefill kernel)."""
+    import numpy as np
+    L = lib()
+    c, p = ctypes.c_int(), ctypes.c_int()
+    L.router_tc_phase_stamps(None, ctypes.byref(c), ctypes.byref(p))
+    out = np.zeros((c.value, p.value), dtype=np.uint64)
+    if L.router_tc_phase_stamps(out.ctypes.data_as(ctypes.c_void_p), ctypes.byref(c),
+                                ctypes.byref(p)) != 0:
+        raise RuntimeError("router_tc_phase_stamps failed")
+    return out
