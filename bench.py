@@ -621,7 +621,8 @@ def run_phase_stamps(args):
     from moe_expert_router_02_gb300 import synth
     R.use_variant("stamps")
     M = args.stamps_m
-    rs = RouterSet(synth.CONFIGS["C1"], M, LAYERS)
+    cfg = synth.CONFIGS[args.stamps_config]
+    rs = RouterSet(cfg, M, LAYERS)
     rs.capture()
     for _ in range(args.warmup):
         rs.step()
@@ -658,8 +659,74 @@ def run_phase_stamps(args):
     res_sel = {n_: float(np.median(sub[:, i])) for i, n_ in
                enumerate(("sort", "rounds", "weights", "stores"))}
     res_sel["entry_to_packed"] = float(np.median(sel[own, 0] - st[n - 1][own, 6]))
-    print(json.dumps({"workload": f"decode M={M}, H=2048, E=256, k=8, 40-call graph",
+    act = {synth.SOFTMAX: "softmax", synth.SQRT_SOFTPLUS: "sqrt-softplus + bias"}[cfg["act"]]
+    print(json.dumps({"workload": f"single-cluster router M={M}, H={cfg['H']}, E={cfg['E']}, "
+                                  f"k={cfg['k']}, {act}, 40-call graph",
                       "calls": n - 1, "median_ns": res, "selection_ns": res_sel}))
+
+
+def run_phase_stamps_split(args):
+    """Per-phase latency of the split-cluster kernel (measurement build) on
+    the sqrt-softplus + bias router at M=64, H=4096, E=256, k=6 (40-call
+    graph): medians over calls of each phase (ns). Prints one JSON line."""
+    import torch
+
+    from moe_expert_router_02_gb300 import router as R
+    from moe_expert_router_02_gb300 import synth
+    R.use_variant("stamps")
+    rs = RouterSet(synth.CONFIGS["C2"], 64, LAYERS)
+    rs.capture()
+    for _ in range(args.warmup):
+        rs.step()
+    torch.cuda.synchronize()
+    R.split_phase_stamps()  # clears the launch counters
+    rs.step()  # 40 calls, inside the 64 stamp slots
+    torch.cuda.synchronize()
+    st = R.split_phase_stamps().astype(np.int64)
+    names = ("wait_return_to_w_ready", "w_ready_to_partials", "partials_to_slices_ready",
+             "slices_to_logits_stored", "logits_to_barrier", "barrier_to_ticket_known")
+    ph = {n: [] for n in names + ("prev_end_to_wait_return", "ticket_to_selected",
+                                   "wait_return_to_selected", "call_period")}
+    prev_end = None
+    ph["last_cluster_ticket_after_median"] = []
+    for c in range(LAYERS):
+        cur = st[c]
+        live = cur[:, 0] > 0
+        # the last cluster's CTAs: a selection stamp of this call (after its
+        # ticket stamp); other slots keep stamps of earlier calls
+        sel = live & (cur[:, 9] > cur[:, 8]) & (cur[:, 8] > 0)
+        if sel.any():
+            ph["last_cluster_ticket_after_median"].append(
+                np.median(cur[sel, 7]) - np.median(cur[live, 7]))
+        end = cur[sel, 9].max() if sel.any() else None
+        w2 = cur[live, 2].min()
+        if prev_end is not None and end is not None:
+            ph["prev_end_to_wait_return"].append(w2 - prev_end)
+            ph["call_period"].append(end - prev_end)
+        for i, n_ in enumerate(names):
+            ph[n_].append(np.median(cur[live, i + 3] - cur[live, i + 2]))
+        if sel.any():
+            ph["ticket_to_selected"].append(np.median(cur[sel, 9] - cur[sel, 8]))
+            ph["wait_return_to_selected"].append(end - w2)
+        prev_end = end
+    # the last call's selection, sub-phase by sub-phase: lane 0 of the last
+    # warp of each of the selecting cluster's CTAs to select a row
+    _, ss = R.phase_stamps()
+    ss = ss.astype(np.int64)
+    cl = int(sel.sum())
+    last = st[LAYERS - 1]
+    sel_rows = np.nonzero((last[:, 9] > last[:, 8]) & (last[:, 8] > 0))[0]
+    ranks = [int(c) % cl for c in sel_rows] if cl else []
+    res_sel = {}
+    if ranks:
+        sub = np.diff(ss[ranks], axis=1)
+        res_sel = {n_: float(np.median(sub[:, i])) for i, n_ in
+                   enumerate(("sort", "rounds", "weights", "stores"))}
+        res_sel["entry_to_packed"] = float(np.median(ss[ranks, 0] - last[sel_rows, 8]))
+    print(json.dumps({"workload": "split-cluster router M=64, H=4096, E=256, k=6, "
+                                  "sqrt-softplus + bias, 40-call graph",
+                      "median_ns": {k: float(np.median(v)) for k, v in ph.items() if v},
+                      "selection_ns": res_sel}))
 
 
 def run_phase_stamps_prefill(args):
@@ -759,6 +826,10 @@ def main():
     ap.add_argument("--phase-stamps", action="store_true",
                     help="per-phase latency of the decode kernel (measurement build)")
     ap.add_argument("--stamps-m", type=int, default=8)
+    ap.add_argument("--stamps-config", default="C1", choices=["C1", "C2"],
+                    help="--phase-stamps: decode softmax (C1) or sqrt-softplus + bias (C2)")
+    ap.add_argument("--phase-stamps-split", action="store_true",
+                    help="per-phase latency of the split-cluster kernel (measurement build)")
     ap.add_argument("--phase-stamps-prefill", action="store_true",
                     help="per-CTA phase timeline of the prefill kernel (measurement build)")
     ap.add_argument("--stamps-prefill-m", type=int, default=16384)
@@ -776,6 +847,9 @@ def main():
         return
     if args.phase_stamps_prefill:
         run_phase_stamps_prefill(args)
+        return
+    if args.phase_stamps_split:
+        run_phase_stamps_split(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

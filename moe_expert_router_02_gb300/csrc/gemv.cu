@@ -94,6 +94,22 @@ __device__ __forceinline__ void atom_exch_relaxed_gpu(uint32_t* p, uint32_t v) {
 constexpr int kStampCalls = 256, kStampPhases = 8;
 __device__ unsigned long long g_stamps[kStampCalls][16][kStampPhases];
 __device__ unsigned g_stamp_seq[16];
+// The split-cluster kernel's stamps: [call slot][CTA = group * CL + rank]
+// [phase], phases 0 entry, 1 W copy issued, 2 wait returned, 3 W in shared
+// memory, 4 warps' partials stored, 5 slices ready (cluster barrier), 6 the
+// cluster's logits stored, 7 cluster barrier, 8 ticket known to the
+// cluster, 9 (last cluster) rows selected.
+constexpr int kSplitStampCalls = 64, kSplitStampCtas = 128, kSplitStampPhases = 10;
+__device__ unsigned long long g_split_stamps[kSplitStampCalls][kSplitStampCtas][kSplitStampPhases];
+__device__ unsigned g_split_seq[kSplitStampCtas];
+#define GBR_SPLIT_STAMP(slot, cta, i)                                       \
+  do {                                                                      \
+    if (threadIdx.x == 0 && (cta) < kSplitStampCtas) {                      \
+      unsigned long long t_;                                                \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_)::"memory");      \
+      g_split_stamps[slot][cta][i] = t_;                                    \
+    }                                                                       \
+  } while (0)
 #define GBR_STAMP(slot, i)                                                  \
   do {                                                                      \
     if (threadIdx.x == 0) {                                                 \
@@ -106,10 +122,14 @@ __device__ unsigned g_stamp_seq[16];
 #define GBR_STAMP(slot, i) \
   do {                     \
   } while (0)
+#define GBR_SPLIT_STAMP(slot, cta, i) \
+  do {                                \
+  } while (0)
 #endif
 
 constexpr int k1cWarps = 16;
 constexpr int k1cBatch = 8;  // 32-element chunks of x held in registers per warp
+
 constexpr int kMaxE1c = 256;
 constexpr int kPartPitch = 20;  // floats per (warp, token) row of partials: 16 experts + pad
 
@@ -492,6 +512,13 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
   const int Hc = H / CL, nchunk = Hc / 32, h_begin = rank * Hc;
   const int tile = warp % NT, cg = warp / NT;
   const uint32_t bar = smem_u32(&s_bar);
+#ifdef GBR_PHASE_STAMPS
+  const int scta = blockIdx.y * CL + rank;
+  const int sslot = (threadIdx.x == 0 && scta < kSplitStampCtas)
+                        ? (int)(atomicAdd(&g_split_seq[scta], 1u) % kSplitStampCalls)
+                        : 0;
+#endif
+  GBR_SPLIT_STAMP(sslot, scta, 0);
 
   if (tid == 0) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
@@ -506,13 +533,17 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
     bulk_g2s(smem_u32(s_w) + tid * pitch, src, (uint32_t)(Hc * 2), bar, policy_evict_first());
   }
   pdl_launch_dependents();
+  GBR_SPLIT_STAMP(sslot, scta, 1);
   pdl_wait();  // x, the scratch and the ticket belong to the preceding call until here
+  GBR_SPLIT_STAMP(sslot, scta, 2);
 
   const uint16_t* __restrict__ x = static_cast<const uint16_t*>(a.x);
   const int tok = tile * 8 + g;
   const uint8_t* w0 = s_w + g * pitch + 16 * t;
   const uint8_t* w1 = w0 + 8 * pitch;
-  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  // two accumulators (even and odd chunks of a batch) halve the chain of
+  // dependent MMAs; they are added once at the end
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   bool w_ok = true, waited = false;
   for (int cb = cg; cb < nchunk; cb += NG * kSplitXB) {
     uint4 xv[kSplitXB];
@@ -526,6 +557,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
     if (!waited) {  // the x loads are in flight meanwhile
       w_ok = mbar_wait_bounded(bar, 0, a.status);
       waited = true;
+      GBR_SPLIT_STAMP(sslot, scta, 3);
     }
 #pragma unroll
     for (int i = 0; i < kSplitXB; ++i) {
@@ -533,12 +565,15 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
       if (c < nchunk && w_ok) {
         const uint4 wa = *reinterpret_cast<const uint4*>(w0 + c * 64);
         const uint4 wb = *reinterpret_cast<const uint4*>(w1 + c * 64);
-        mma_bf16_16816(acc, wa.x, wb.x, wa.y, wb.y, xv[i].x, xv[i].y);
-        mma_bf16_16816(acc, wa.z, wb.z, wa.w, wb.w, xv[i].z, xv[i].w);
+        float (&ac)[4] = (i & 1) ? acc2 : acc;
+        mma_bf16_16816(ac, wa.x, wb.x, wa.y, wb.y, xv[i].x, xv[i].y);
+        mma_bf16_16816(ac, wa.z, wb.z, wa.w, wb.w, xv[i].z, xv[i].w);
       }
     }
   }
   if (!waited) mbar_wait_bounded(bar, 0, a.status);  // never leave with the copy in flight
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] += acc2[j];
 
   // accumulator layout: c0,c1 -> expert g, tokens 2t, 2t+1; c2,c3 -> expert g+8
   s_part[cg][g][tile * 8 + 2 * t] = acc[0];
@@ -546,6 +581,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
   s_part[cg][g + 8][tile * 8 + 2 * t] = acc[2];
   s_part[cg][g + 8][tile * 8 + 2 * t + 1] = acc[3];
   __syncthreads();
+  GBR_SPLIT_STAMP(sslot, scta, 4);
   for (int i = tid; i < 16 * NTOK; i += kSplitWarps * 32) {
     const int el = i / NTOK, m = i % NTOK;
     float v = s_part[0][el][m];
@@ -554,6 +590,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
     s_cta[el][m] = v;
   }
   cluster_sync_all();
+  GBR_SPLIT_STAMP(sslot, scta, 5);
 
   // cluster reduction over the CL slices of H; item i = m * 16 + el
   for (int i = rank + CL * tid; i < 16 * M; i += CL * kSplitWarps * 32) {
@@ -570,11 +607,13 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
     cluster_sync_all();  // keep shared memory alive until every peer has read it
     return;
   }
+  GBR_SPLIT_STAMP(sslot, scta, 6);
   // The cluster barrier (release/acquire) orders every peer's logits stores
   // before rank 0's acq_rel arrival on the ticket; the arrivals form one
   // release sequence, so the cluster that arrives last observes all logits
   // and hands them to its peers through the next cluster barrier.
   cluster_sync_all();
+  GBR_SPLIT_STAMP(sslot, scta, 7);
   if (rank == 0 && tid == 0) {
     const uint32_t old = atom_add_acq_rel_gpu(a.ticket, 1u);
     const uint32_t last = (old == gridDim.y - 1) ? 1u : 0u;
@@ -582,6 +621,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
     for (int q = 0; q < CL; ++q) dsmem_st_u32(&s_flag, (uint32_t)q, last);
   }
   cluster_sync_all();
+  GBR_SPLIT_STAMP(sslot, scta, 8);
   if (!s_flag) return;
 
   // the last cluster selects: warp w of CTA r takes rows r*8 + w, then
@@ -604,6 +644,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
       __syncthreads();
     }
   }
+  GBR_SPLIT_STAMP(sslot, scta, 9);
 }
 
 // Generic router: one CTA per row (two rows when a table is fused), any
@@ -840,6 +881,18 @@ bool gemv1c_eligible(int M, int H, int E, bool fp4) {
 }
 
 #ifdef GBR_PHASE_STAMPS
+// The split-cluster kernel's stamps [kSplitStampCalls][kSplitStampCtas]
+// [kSplitStampPhases], copied to host memory; the launch counters cleared.
+extern "C" int router_split_phase_stamps(unsigned long long* host, int* calls, int* ctas,
+                                         int* phases) {
+  *calls = kSplitStampCalls, *ctas = kSplitStampCtas, *phases = kSplitStampPhases;
+  if (!host) return 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return 3;
+  if (cudaMemcpyFromSymbol(host, g_split_stamps, sizeof(g_split_stamps)) != cudaSuccess) return 3;
+  static const unsigned zero[kSplitStampCtas] = {};
+  return cudaMemcpyToSymbol(g_split_seq, zero, sizeof(zero)) == cudaSuccess ? 0 : 3;
+}
+
 // Copies the stamps [kStampCalls][16][kStampPhases] to host memory and
 // clears the launch counters (measurement build only).
 extern "C" int router_phase_stamps(unsigned long long* host, int* calls, int* ctas, int* phases) {

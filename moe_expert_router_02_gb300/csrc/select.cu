@@ -101,9 +101,20 @@ __global__ void __launch_bounds__(kLaneWarps * 32)
   const uint32_t inv_n = (65536u + (uint32_t)n - 1u) / (uint32_t)n;  // i / n = (i * inv_n) >> 16, i < 512
   int32_t* in = s_in[warp];
   const int32_t* src = idx + g0 * n;
-  for (int i = lane; i < total; i += 32) {
-    const int gl = (int)(((uint32_t)i * inv_n) >> 16);
-    in[gl * kLaneStride + (i - gl * n)] = __ldg(src + i);
+  // every load of the lane in flight at once (total <= 32 * kLaneMax)
+  int32_t r[kLaneMax];
+#pragma unroll
+  for (int u = 0; u < kLaneMax; ++u) {
+    const int i = lane + 32 * u;
+    r[u] = i < total ? __ldg(src + i) : 0;
+  }
+#pragma unroll
+  for (int u = 0; u < kLaneMax; ++u) {
+    const int i = lane + 32 * u;
+    if (i < total) {
+      const int gl = (int)(((uint32_t)i * inv_n) >> 16);
+      in[gl * kLaneStride + (i - gl * n)] = r[u];
+    }
   }
   __syncwarp();
   const int row = lane * kLaneStride;

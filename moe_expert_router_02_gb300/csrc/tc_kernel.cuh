@@ -194,6 +194,35 @@ __device__ __forceinline__ bool wait_flag(unsigned* st, const unsigned* f, unsig
   return true;
 }
 
+// Bounded wait until flags f[0..n) (n <= 8) all hold `want`: the relaxed
+// loads of a round go out together, and one acq_rel fence after the round
+// that sees them all set orders what follows after the flags' release
+// stores (an acquire pattern), so a batch costs one round trip.
+__device__ __forceinline__ bool wait_flags8(unsigned* st, const unsigned* f, int n, unsigned want) {
+  const uint64_t t0 = globaltimer();
+  uint32_t ns = 32;
+  for (;;) {
+    unsigned v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = want;
+      if (j < n) asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v[j]) : "l"(f + j) : "memory");
+    }
+    bool all = true;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) all = all && v[j] == want;
+    if (all) break;
+    __nanosleep(ns);
+    if (ns < 256) ns <<= 1;
+    if (globaltimer() - t0 > kWaitNs) {
+      if (st) atomicOr(st, 1u);
+      return false;
+    }
+  }
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  return true;
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -890,6 +919,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       }
       for (int sg = 0; sg < plan.nseg && go; ++sg) {
         const int mrow = plan.t(sg) * tile_rows + (PAIR ? crank * BM : 0);
+        int decoded_to = plan.kb0(sg);  // NVFP4: column blocks seen decoded, exclusive end
         for (int kb = plan.kb0(sg); kb < plan.kb1(sg); ++kb) {
           const int s = issued % S;  // ring position: k-steps issued so far
           const uint32_t ph = (uint32_t)(issued / S) & 1u;
@@ -905,12 +935,14 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
             if (crank == 0) mbar_expect_tx(fb, 2u * (p.a_bytes + p.b_bytes));
             tma_load_2d_pair(smem_u32(st), &tmap_x, kb * BK, mrow, fb0, pol_x);
             ++issued;
-            if (FP4) {
-              if (!wait_flag(wstat, p.wsync + 2 + kb, want)) {
+            if (FP4 && kb >= decoded_to) {  // the decoded copy: the next blocks, in batches
+              const int nb = min(kb == plan.kb0(sg) ? 1 : 8, plan.kb1(sg) - kb);  // first block alone
+              if (!wait_flags8(wstat, p.wsync + 2 + kb, nb, want)) {
                 go = false;
                 break;
               }
               asm volatile("fence.proxy.async.global;" ::: "memory");
+              decoded_to = kb + nb;
             }
             tma_load_2d_pair(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, crank * (E / 2), fb0,
                              pol_w);
@@ -919,12 +951,14 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
           mbar_expect_tx(fb, p.a_bytes + p.b_bytes);
           tma_load_2d(smem_u32(st), &tmap_x, kb * BK, mrow, fb, pol_x);
           ++issued;
-          if (FP4) {  // the decoded copy: wait for this k-step's columns
-            if (!wait_flag(wstat, p.wsync + 2 + kb, want)) {
+          if (FP4 && kb >= decoded_to) {  // the decoded copy: the next blocks, in batches
+            const int nb = min(kb == plan.kb0(sg) ? 1 : 8, plan.kb1(sg) - kb);  // first block alone
+            if (!wait_flags8(wstat, p.wsync + 2 + kb, nb, want)) {
               go = false;
               break;
             }
             asm volatile("fence.proxy.async.global;" ::: "memory");
+            decoded_to = kb + nb;
           }
           tma_load_2d(smem_u32(st + p.a_bytes), &tmap_w, kb * BK, 0, fb, pol_w);
         }

@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
                 L.router_phase_stamps.restype = I
                 L.router_tc_phase_stamps.argtypes = [P, P, P]
                 L.router_tc_phase_stamps.restype = I
+                L.router_split_phase_stamps.argtypes = [P, P, P, P]
+                L.router_split_phase_stamps.restype = I
             for f in (L.router_forward, L.router_forward_ex, L.router_regime, L.router_tc_groups,
                       L.router_select,
                       L.route_table, L.router_device_status, L.router_forward_noalloc,
@@ -235,4 +237,18 @@ def tc_phase_stamps():
     if L.router_tc_phase_stamps(out.ctypes.data_as(ctypes.c_void_p), ctypes.byref(c),
                                 ctypes.byref(p)) != 0:
         raise RuntimeError("router_tc_phase_stamps failed")
+    return out
+
+
+def split_phase_stamps():
+    """Measurement build only: the split-cluster kernel's phase stamps as a
+    numpy array [calls, ctas, phases] (%globaltimer ns, 0 = not stamped)."""
+    import numpy as np
+    L = lib()
+    c, t, p = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    L.router_split_phase_stamps(None, ctypes.byref(c), ctypes.byref(t), ctypes.byref(p))
+    out = np.zeros((c.value, t.value, p.value), dtype=np.uint64)
+    if L.router_split_phase_stamps(out.ctypes.data_as(ctypes.c_void_p), ctypes.byref(c),
+                                   ctypes.byref(t), ctypes.byref(p)) != 0:
+        raise RuntimeError("router_split_phase_stamps failed")
     return out
