@@ -621,7 +621,9 @@ def run_phase_stamps(args):
     from moe_expert_router_02_gb300 import synth
     R.use_variant("stamps")
     M = args.stamps_m
-    cfg = synth.CONFIGS[args.stamps_config]
+    cfg = dict(synth.CONFIGS[args.stamps_config])
+    if args.stamps_sigmoid:
+        cfg["act"] = synth.SIGMOID
     rs = RouterSet(cfg, M, LAYERS)
     rs.capture()
     for _ in range(args.warmup):
@@ -632,7 +634,7 @@ def run_phase_stamps(args):
     for _ in range(reps):
         rs.step()
     torch.cuda.synchronize()
-    st, sel = R.phase_stamps()
+    st, sel, refines = R.phase_stamps(with_refines=True)
     st, sel = st.astype(np.int64), sel.astype(np.int64)
     n = reps * LAYERS
     own = [c for c in range(16) if c < M]  # CTAs that select a row (no table)
@@ -659,10 +661,13 @@ def run_phase_stamps(args):
     res_sel = {n_: float(np.median(sub[:, i])) for i, n_ in
                enumerate(("sort", "rounds", "weights", "stores"))}
     res_sel["entry_to_packed"] = float(np.median(sel[own, 0] - st[n - 1][own, 6]))
-    act = {synth.SOFTMAX: "softmax", synth.SQRT_SOFTPLUS: "sqrt-softplus + bias"}[cfg["act"]]
+    act = {synth.SOFTMAX: "softmax", synth.SQRT_SOFTPLUS: "sqrt-softplus + bias",
+           synth.SIGMOID: "sigmoid + bias"}[cfg["act"]]
     print(json.dumps({"workload": f"single-cluster router M={M}, H={cfg['H']}, E={cfg['E']}, "
                                   f"k={cfg['k']}, {act}, 40-call graph",
-                      "calls": n - 1, "median_ns": res, "selection_ns": res_sel}))
+                      "calls": n - 1, "median_ns": res, "selection_ns": res_sel,
+                      "rows_selected": n * M, "rows_reranked": refines[0],
+                      "rows_fp64": refines[1]}))
 
 
 def run_phase_stamps_split(args):
@@ -680,6 +685,7 @@ def run_phase_stamps_split(args):
         rs.step()
     torch.cuda.synchronize()
     R.split_phase_stamps()  # clears the launch counters
+    R.phase_stamps()  # and the re-rank counts
     rs.step()  # 40 calls, inside the 64 stamp slots
     torch.cuda.synchronize()
     st = R.split_phase_stamps().astype(np.int64)
@@ -711,7 +717,7 @@ def run_phase_stamps_split(args):
         prev_end = end
     # the last call's selection, sub-phase by sub-phase: lane 0 of the last
     # warp of each of the selecting cluster's CTAs to select a row
-    _, ss = R.phase_stamps()
+    _, ss, refines = R.phase_stamps(with_refines=True)
     ss = ss.astype(np.int64)
     cl = int(sel.sum())
     last = st[LAYERS - 1]
@@ -726,7 +732,8 @@ def run_phase_stamps_split(args):
     print(json.dumps({"workload": "split-cluster router M=64, H=4096, E=256, k=6, "
                                   "sqrt-softplus + bias, 40-call graph",
                       "median_ns": {k: float(np.median(v)) for k, v in ph.items() if v},
-                      "selection_ns": res_sel}))
+                      "selection_ns": res_sel, "rows_selected": 64 * LAYERS,
+                      "rows_reranked": refines[0], "rows_fp64": refines[1]}))
 
 
 def run_phase_stamps_prefill(args):
@@ -773,6 +780,10 @@ def run_phase_stamps_prefill(args):
         ent["slowest"] = [{"cta": int(c), "end": float(rel[c, 9]),
                            "acc": float(rel[c, 3]), "refined": int(st[c, 10])}
                           for c in np.argsort(-rel[:, 9])[:6]]
+        if args.stamps_dump:  # per CTA: SM, plan, accumulator complete, end (us)
+            ent["per_cta"] = {"sm": st[:, 18].tolist(), "plan": st[:, 19].tolist(),
+                              "acc": [round(float(v), 3) for v in rel[:, 3]],
+                              "end": [round(float(v), 3) for v in rel[:, 9]]}
         out.append(ent)
     print(json.dumps({"workload": f"prefill M={args.stamps_prefill_m}, H=7168, E=256, k=8, "
                                   f"sqrt-softplus + bias, {'NVFP4' if w_dtype else 'BF16'} W",
@@ -828,12 +839,16 @@ def main():
     ap.add_argument("--stamps-m", type=int, default=8)
     ap.add_argument("--stamps-config", default="C1", choices=["C1", "C2"],
                     help="--phase-stamps: decode softmax (C1) or sqrt-softplus + bias (C2)")
+    ap.add_argument("--stamps-sigmoid", action="store_true",
+                    help="--phase-stamps: the sigmoid + bias score on the chosen config")
     ap.add_argument("--phase-stamps-split", action="store_true",
                     help="per-phase latency of the split-cluster kernel (measurement build)")
     ap.add_argument("--phase-stamps-prefill", action="store_true",
                     help="per-CTA phase timeline of the prefill kernel (measurement build)")
     ap.add_argument("--stamps-prefill-m", type=int, default=16384)
     ap.add_argument("--stamps-nvfp4", action="store_true")
+    ap.add_argument("--stamps-dump", action="store_true",
+                    help="--phase-stamps-prefill: add per-CTA SM, plan and times")
     ap.add_argument("--only", default=None,
                     choices=["decode", "decode_m1", "sqrtsoftplus_m64", "m2_table",
                              "prefill_bf16", "prefill_nvfp4", "table_1e5", "gather_1e3"],

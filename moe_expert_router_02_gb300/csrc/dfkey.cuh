@@ -160,10 +160,11 @@ __device__ __forceinline__ df32 sigmoid_df(float z) {
 }
 
 // Upper bound on |key32 - key| for FP32 keys whose largest activation is
-// amax and largest |key| is kabs: 2^-23 (2.25 amax + 0.5 kabs) + 2^-60,
-// every step rounded up.
-__device__ __forceinline__ float key_err_bound(float amax, float kabs, float coef = 2.25f) {
-  return __fadd_ru(__fmul_ru(__fmaf_ru(coef, amax, __fmul_ru(0.5f, kabs)), 0x1p-23f), 0x1p-60f);
+// amax and largest |key| is kabs: 2^-23 (c amax + 0.5 kabs) + 2^-59 with c
+// the activation's coefficient (act_err_coef; the absolute term covers the
+// score's 2^-60 and the rounding of tiny keys), every step rounded up.
+__device__ __forceinline__ float key_err_bound(float amax, float kabs, float coef) {
+  return __fadd_ru(__fmul_ru(__fmaf_ru(coef, amax, __fmul_ru(0.5f, kabs)), 0x1p-23f), 0x1p-59f);
 }
 
 // A near-tie key: a(z) + b as a double-float (a = sqrt-softplus or sigmoid),

@@ -53,8 +53,58 @@ cudaError_t launch_one(int kind, const void* x, int n16, unsigned* sink, cudaStr
   return cudaLaunchKernelEx(&cfg, k_diag_read_x, static_cast<const uint4*>(x), n16, sink);
 }
 
+// The scores composed of CUDA's own functions, each within its documented
+// error bound (expf 2 ulp, log1pf 1 ulp, sqrtf and division correctly
+// rounded): the reference the library's branch-free scores are swept
+// against.
+__device__ float act_libm(int act, float z) {
+  if (act == ACT_SIGMOID) return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
+  return sqrtf(fmaxf(z, 0.0f) + log1pf(expf(-fabsf(z))));
+}
+
+// out[0]: the largest |act_f32 - act_libm| / (2^-23 act_libm) over inputs
+// whose reference is at least 2^-62; out[1]: the largest |act_f32 -
+// act_libm| over the others. Both rounded up, as float bit patterns
+// (non-negative floats order like their bits).
+__global__ void __launch_bounds__(256)
+    k_diag_act_sweep(int act, unsigned long long first, unsigned long long count, unsigned* out) {
+  unsigned rel = 0u, abs_ = 0u;
+  const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+  for (unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+       i += stride) {
+    const float z = __uint_as_float((unsigned)(first + i));
+    if (!isfinite(z)) continue;
+    const float f = act_f32(act, z), r = act_libm(act, z);
+    const float d = __fsub_ru(fmaxf(f, r), fminf(f, r));
+    if (r >= 0x1p-62f)
+      rel = max(rel, __float_as_uint(__fdiv_ru(d, r * 0x1p-23f)));
+    else
+      abs_ = max(abs_, __float_as_uint(d));
+  }
+  rel = __reduce_max_sync(kFull, rel);
+  abs_ = __reduce_max_sync(kFull, abs_);
+  if ((threadIdx.x & 31) == 0) {
+    atomicMax(out, rel);
+    atomicMax(out + 1, abs_);
+  }
+}
+
 }  // namespace
 }  // namespace gbr
+
+extern "C" float gbr_diag_act_coef(int act) { return gbr::act_err_coef(act); }
+
+extern "C" int gbr_diag_act_sweep(int act, unsigned long long first, unsigned long long count,
+                                  float* out, cudaStream_t stream) {
+  if ((act != gbr::ACT_SQRT_SOFTPLUS && act != gbr::ACT_SIGMOID) || !out ||
+      first > 0x100000000ull || count > 0x100000000ull - first)
+    return 1;
+  if (cudaMemsetAsync(out, 0, 2 * sizeof(float), stream) != cudaSuccess) return 3;
+  if (count == 0) return 0;
+  gbr::k_diag_act_sweep<<<152 * 8, 256, 0, stream>>>(act, first, count,
+                                                      reinterpret_cast<unsigned*>(out));
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
 
 extern "C" int gbr_diag_chain(int kind, int n, const void* x, size_t x_bytes, unsigned* sink,
                               cudaStream_t stream) {

@@ -279,6 +279,7 @@ __global__ void __launch_bounds__(k1cWarps * 32)
   __shared__ int32_t s_sel[k1cWarps * kMaxK];
   __shared__ __align__(8) uint64_t s_bar;   // this CTA's W rows have landed
   __shared__ __align__(8) uint64_t s_join;  // every logit of this CTA's rows has landed
+  __shared__ float s_bias[kMaxE];           // the selection bias (CTAs that select)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -334,6 +335,10 @@ __global__ void __launch_bounds__(k1cWarps * 32)
                pol);
     }
   }
+  // the bias is a weight: staged before the wait (read after a later
+  // __syncthreads), so the selection does not wait on L2 for it
+  if (a.bias && nown > 0)
+    for (int e = tid; e < E; e += k1cWarps * 32) s_bias[e] = a.bias[e];
   pdl_launch_dependents();
   // every CTA of the cluster has initialised its barriers (they all arrived
   // above): the remote stores below may target them. Waiting here keeps the
@@ -458,7 +463,7 @@ __global__ void __launch_bounds__(k1cWarps * 32)
   const int k = a.k;
   const int row = own.row(rank, warp);
   if (warp < nown)
-    warp_select_row<VPL>(LdPlain{&s_all[warp][0]}, a.bias, E, k, a.act,
+    warp_select_row<VPL>(LdPlain{&s_all[warp][0]}, a.bias ? s_bias : nullptr, E, k, a.act,
                          a.out_idx + (size_t)row * k, a.out_w + (size_t)row * k,
                          s_sel + warp * k);
   GBR_STAMP(stamp, 7);
@@ -501,6 +506,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
   __shared__ float s_part[NG][16][NTOK];
   __shared__ float s_cta[16][NTOK];
   __shared__ int32_t s_sel[kSplitWarps * kMaxK];
+  __shared__ float s_bias[SELECT ? kMaxE : 1];  // the selection bias
   __shared__ uint32_t s_flag;
   __shared__ __align__(8) uint64_t s_bar;
 
@@ -532,6 +538,10 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
     const uint16_t* src = static_cast<const uint16_t*>(a.w) + (size_t)(e0 + tid) * H + h_begin;
     bulk_g2s(smem_u32(s_w) + tid * pitch, src, (uint32_t)(Hc * 2), bar, policy_evict_first());
   }
+  // any cluster may arrive last: each stages the bias (a weight) before the
+  // wait; a later __syncthreads orders it before the selection
+  if (SELECT && a.bias)
+    for (int e = tid; e < E; e += kSplitWarps * 32) s_bias[e] = a.bias[e];
   pdl_launch_dependents();
   GBR_SPLIT_STAMP(sslot, scta, 1);
   pdl_wait();  // x, the scratch and the ticket belong to the preceding call until here
@@ -631,7 +641,8 @@ __global__ void __launch_bounds__(kSplitWarps * 32)
   for (int base = rank * kSplitWarps; base < M; base += CL * kSplitWarps) {
     const int row = base + warp;
     if (row < M)
-      warp_select_row<VPL>(LdCG{a.logits + (size_t)row * E}, a.bias, E, k, a.act,
+      warp_select_row<VPL>(LdCG{a.logits + (size_t)row * E}, a.bias ? s_bias : nullptr, E, k,
+                           a.act,
                            a.out_idx + (size_t)row * k, a.out_w + (size_t)row * k,
                            s_sel + warp * k);
     if (table) {
@@ -904,6 +915,13 @@ extern "C" int router_phase_stamps(unsigned long long* host, int* calls, int* ct
   if (cudaMemcpyFromSymbol(host + kStampCalls * 16 * kStampPhases, g_sel_stamps,
                            sizeof(g_sel_stamps)) != cudaSuccess)
     return 3;
+  // then the re-rank counts since the last call (rows re-ranked, rows
+  // taken to FP64), which restart from zero
+  if (cudaMemcpyFromSymbol(host + kStampCalls * 16 * kStampPhases + 16 * 5, g_sel_refines,
+                           sizeof(g_sel_refines)) != cudaSuccess)
+    return 3;
+  static const unsigned long long zr[2] = {};
+  if (cudaMemcpyToSymbol(g_sel_refines, zr, sizeof(zr)) != cudaSuccess) return 3;
   static const unsigned zero[16] = {};
   return cudaMemcpyToSymbol(g_stamp_seq, zero, sizeof(zero)) == cudaSuccess ? 0 : 3;
 }

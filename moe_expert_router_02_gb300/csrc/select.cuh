@@ -18,12 +18,15 @@
 // Order (qwisp issue #145, "Bit-exactness"): higher key first, an equal key
 // goes to the lower expert index; -0.0 equals +0.0.
 //
-// Exactness of the biased rankings. FP32 keys carry a bounded error (CUDA
-// documents expf <= 2 ulp, log1pf <= 1 ulp, IEEE sqrtf and division):
-// following the steps gives |key32 - key| <= 2^-23 (c a + 0.5 |key|) plus a
-// tiny absolute term, c = 2.25 for sqrt-softplus and 3 for sigmoid. When two neighbouring
-// keys among the first k+1 are closer than four times that bound, the
-// candidates within the band of the k-th key are re-ranked with
+// Exactness of the biased rankings. FP32 keys carry a bounded error: the
+// branch-free scores of common.cuh are within c 2^-23 a + 2^-60 of the exact
+// score (c = act_err_coef, checked at every FP32 input against CUDA's
+// documented expf/log1pf/sqrtf composition), so |key32 - key| <=
+// 2^-23 (c a + 0.5 |key|) + 2^-59 (key_err_bound). Two keys whose exact
+// order differs from their FP32 order are then within twice that bound,
+// and so is every exact top-k member of the k-th FP32 key. When two
+// neighbouring keys among the first k+1 are that close, the candidates
+// within that band of the k-th key are re-ranked with
 // double-float keys (relative error near 2^-42, FP32 arithmetic only); a
 // pair of those still too close to call, from different inputs, is ranked
 // with FP64 keys, which decide the order the FP64 definition gives.
@@ -41,6 +44,9 @@ namespace gbr {
 // selection of each CTA rank wins.
 namespace {
 __device__ unsigned long long g_sel_stamps[16][5];
+// rows whose selection took the near-tie re-rank, and of those the rows
+// that went on to FP64 keys (warp selections of this translation unit)
+__device__ unsigned long long g_sel_refines[2];
 }
 #define SEL_STAMP(i)                                                           \
   do {                                                                         \
@@ -128,7 +134,7 @@ __device__ __noinline__ int select_fp64(const Ld ld, const float* __restrict__ b
     const int e = lane + 32 * j;
     k64[j] = 0.0;
     if ((cmask >> j) & 1u)
-      k64[j] = act_f64(act, (double)ld(e)) + (bias ? (double)__ldg(bias + e) : 0.0);
+      k64[j] = act_f64(act, (double)ld(e)) + (bias ? (double)bias[e] : 0.0);
   }
   return fp64_rounds<VPL>(k64, cmask, k);
 }
@@ -157,7 +163,7 @@ __device__ __noinline__ int select_softmax_bias_fp64(const Ld ld, const float* _
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
     const int e = lane + 32 * j;
-    k64[j] = ((cmask >> j) & 1u) ? ex[j] / part + (double)__ldg(bias + e) : 0.0;
+    k64[j] = ((cmask >> j) & 1u) ? ex[j] / part + (double)bias[e] : 0.0;
   }
   return fp64_rounds<VPL>(k64, cmask, k);
 }
@@ -200,7 +206,7 @@ __device__ __noinline__ int refine_near_ties(const Ld ld, const float* __restric
     const int e = lane + 32 * j;
     if (e < E) {
       const float a = act_f32(act, ld(e));
-      const float kv = bias ? a + __ldg(bias + e) : a;
+      const float kv = bias ? a + bias[e] : a;
       if (kv >= thr) cmask |= 1u << j;
     }
   }
@@ -214,7 +220,7 @@ __device__ __noinline__ int refine_near_ties(const Ld ld, const float* __restric
     const int j = has ? __ffs(todo) - 1 : 0;
     const int e = lane + 32 * j;
     const float z = has ? ld(e) : 0.0f;
-    const float b = (has && bias) ? __ldg(bias + e) : 0.0f;
+    const float b = (has && bias) ? bias[e] : 0.0f;
     const NearKey nk = near_key_ool(act, z, b);
 #pragma unroll
     for (int jj = 0; jj < VPL; ++jj) {
@@ -264,7 +270,7 @@ __device__ __noinline__ int refine_near_ties(const Ld ld, const float* __restric
     if (bidx == 0x7fffffff) break;  // fewer candidates than rounds
     if ((bidx & 31) == lane) left &= ~(1u << (bidx >> 5));
     const float wz = ld(bidx);
-    const float wb = bias ? __ldg(bias + bidx) : 0.0f;
+    const float wb = bias ? bias[bidx] : 0.0f;
     if (r > 0 && !near_distinct(ph, pl, psc, bh, bl, bsc) && !(pz == wz && pb == wb))
       amb = true;
     ph = bh, pl = bl, psc = bsc, pz = wz, pb = wb;
@@ -273,6 +279,9 @@ __device__ __noinline__ int refine_near_ties(const Ld ld, const float* __restric
   if (!amb) {
     if (lane < k) sel_idx = pick;
   } else {
+#ifdef GBR_PHASE_STAMPS
+    if (lane == 0) atomicAdd(&g_sel_refines[1], 1ull);
+#endif
     const int pick64 = select_fp64<VPL>(ld, bias, act, k, cmask);
     if (lane < k) sel_idx = pick64;
   }
@@ -311,6 +320,7 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
                                                  float* __restrict__ out_w, int32_t* sel_out) {
   const int lane = threadIdx.x & 31;
   uint64_t pk[VPL];  // (key << 32) | (0xffffffff - expert); 0 = empty
+  float av[VPL];     // sqrt-softplus / sigmoid: the scores, for the weights
   float amax = 0.0f, kabs = 0.0f;
   // softmax + bias: the row maximum, the FP32 denominator and the bound term
   float zmax = 0.0f, zsum = 1.0f, s1z = 0.0f;
@@ -349,28 +359,35 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
       pk[j] = 0ull;
       if (e < E) {
         const float p = __fdiv_rn(ev[j], zsum);
-        const float key = __fadd_rn(p, __ldg(bias + e));  // as softmax_bias_key32
+        const float key = __fadd_rn(p, bias[e]);  // as softmax_bias_key32
         amax = fmaxf(amax, p);
         kabs = fmaxf(kabs, fabsf(key));
         pk[j] = ((uint64_t)ord_of(key) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
       }
     }
   } else {
+    // every load first, at an index clamped into the row (no branch per
+    // value), then the scores: the chains of the VPL values interleave
+    float zv[VPL], bv[VPL];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int ec = min(lane + 32 * j, E - 1);
+      zv[j] = ld(ec);
+      bv[j] = (act != ACT_SOFTMAX && bias) ? bias[ec] : 0.0f;
+    }
 #pragma unroll
     for (int j = 0; j < VPL; ++j) {
       const int e = lane + 32 * j;
-      pk[j] = 0ull;
-      if (e < E) {
-        const float z = ld(e);
-        float key = z;
-        if (act != ACT_SOFTMAX) {
-          const float a = act_f32(act, z);
-          key = bias ? a + __ldg(bias + e) : a;
-          amax = fmaxf(amax, a);
-          kabs = fmaxf(kabs, fabsf(key));
-        }
-        pk[j] = ((uint64_t)ord_of(key) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e);
+      const bool in = e < E;
+      float key = zv[j];
+      if (act != ACT_SOFTMAX) {
+        const float a = act_f32(act, zv[j]);
+        key = a + bv[j];  // a >= +0: adding +0 (no bias) leaves it unchanged
+        av[j] = a;
+        amax = in ? fmaxf(amax, a) : amax;
+        kabs = in ? fmaxf(kabs, fabsf(key)) : kabs;
       }
+      pk[j] = in ? (((uint64_t)ord_of(key) << 32) | (uint64_t)(0xffffffffu - (uint32_t)e)) : 0ull;
     }
   }
   SEL_STAMP(0);
@@ -403,13 +420,19 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
     // FP32 key error bound; non-negative floats order like their bit patterns
     const float amax_w = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(amax)));
     const float kabs_w = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(kabs)));
-    const float band = 4.0f * (act == ACT_SOFTMAX_BIAS
-                                   ? softmax_bias_err_bound(VPL, amax_w, s1z, zsum, kabs_w)
-                                   : key_err_bound(amax_w, kabs_w, act_err_coef(act)));
+    // two FP32 keys in the wrong exact order lie within 2 err of each
+    // other, and every exact top-k member within 2 err of the k-th FP32 key;
+    // the softmax + bias bound keeps a factor of 2 on top
+    const float band = act == ACT_SOFTMAX_BIAS
+                           ? 4.0f * softmax_bias_err_bound(VPL, amax_w, s1z, zsum, kabs_w)
+                           : 2.0f * key_err_bound(amax_w, kabs_w, act_err_coef(act));
     const float next_key = __shfl_down_sync(kFull, sel_key, 1);
     // the difference rounded down: a gap of at most band is never missed
     const bool close = (lane < kk - 1) && __fsub_rd(sel_key, next_key) <= band;
     if (__any_sync(kFull, close)) {
+#ifdef GBR_PHASE_STAMPS
+      if (lane == 0) atomicAdd(&g_sel_refines[0], 1ull);
+#endif
       if (act == ACT_SOFTMAX_BIAS) {
         // FP64 keys for every expert within the band of the k-th key
         const float thr = __fsub_rd(__shfl_sync(kFull, sel_key, k - 1), band);
@@ -417,7 +440,7 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
           const int e = lane + 32 * j;
-          if (e < E && softmax_bias_key32(ld(e), zmax, zsum, __ldg(bias + e)) >= thr)
+          if (e < E && softmax_bias_key32(ld(e), zmax, zsum, bias[e]) >= thr)
             cmask |= 1u << j;
         }
         const int pick = select_softmax_bias_fp64<VPL>(ld, bias, E, k, zmax, cmask);
@@ -441,7 +464,15 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
     const float zc = float_of_ord(__reduce_max_sync(kFull, lane < k ? ord_of(zj) : 0u));
     if (lane < k) s = expf(zj - zc);
   } else {
-    if (lane < k) s = act_f32(act, ld(sel_idx));
+    // the chosen scores come from the lanes that hold them (no reload)
+    const int src = sel_idx & 31, js = sel_idx >> 5;  // lanes >= k: js = -1, no match
+    float sv = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const float v = __shfl_sync(kFull, av[j], src);
+      sv = j == js ? v : sv;
+    }
+    if (lane < k) s = sv;
     const float smax = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(s)));
     if (!(smax >= 0x1p-50f)) {
       // every chosen activation is tiny (FP32 keeps few or no bits of it):

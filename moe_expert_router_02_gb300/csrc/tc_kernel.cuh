@@ -733,8 +733,9 @@ struct TcParams {
 // CTA re-ranked near ties, slot 11 the time the first MMA was issued (even
 // CTAs), 12 threshold computed, 13 pass B masks built, 14 pooled
 // activations done, 15 insertion done; slots 16 and 17 hold thread 0's
-// candidate count and its warp's pooled total.
-constexpr int kTcStamps = 18;
+// candidate count and its warp's pooled total, 18 the SM the CTA ran on,
+// 19 its plan (2 x segments + 1 if it finishes a tile).
+constexpr int kTcStamps = 20;
 
 namespace {
 
@@ -858,6 +859,14 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
   const bool has_part = !plan.f0;  // a partial segment always comes first
   // first row of this CTA's 128 rows of the finished tile
   const int m0 = (plan.f0 ? plan.t0 : plan.t1) * tile_rows + (PAIR ? crank * BM : 0);
+#ifdef GBR_PHASE_STAMPS
+  if (threadIdx.x == 0 && p.stamps) {
+    unsigned sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    p.stamps[blockIdx.x * kTcStamps + 18] = sm;
+    p.stamps[blockIdx.x * kTcStamps + 19] = (unsigned)(2 * plan.nseg + (has_fin ? 1 : 0));
+  }
+#endif
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -1376,9 +1385,10 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       if (!kSepLbx) asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
       TC_STAMP(5);
       // The threshold. Margins: the FP32 keys are within
-      // err = 2^-23 (2.25 a + 0.5 |key|) of the exact ones and the band the
-      // list must also hold reaches 8 err below the k-th FP32 key, so the
-      // exact keys to keep reach L - 10 err; with a <= A = (largest LB) -
+      // err = 2^-23 (c a + 0.5 |key|) + 2^-59 of the exact ones (c =
+      // act_err_coef <= 6); the band is 2 err and the list must hold keys
+      // down to two bands below the k-th FP32 key, so the exact keys to
+      // keep reach L - 6 err (the margin below allows 10); with a <= A = (largest LB) -
       // b_min + 0.84 (a(z) <= sqrt(max(z, 0)) + sqrt(ln 2)) the margin
       // 2^-16 (4 A + |b|max + 1) covers that many times over. a^-1(y) =
       // log(expm1(y^2)) is then taken on y shrunk by 2^-18 and the result
@@ -1558,7 +1568,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       bool close = false;
       float band = 0.0f;
       if (sp) {
-        band = 4.0f * key_err_bound(amax, kabs, act_err_coef(act));
+        band = 2.0f * key_err_bound(amax, kabs, act_err_coef(act));  // as in select.cuh
         const int kk = min(k + 1, E);
 #pragma unroll
         for (int j = 0; j + 1 < KC; ++j)

@@ -24,7 +24,8 @@ GBR_REGIME_GENERIC, GBR_REGIME_GEMV, GBR_REGIME_TC, GBR_REGIME_UNFUSED, GBR_REGI
 
 EXPORTS = ("router_forward", "router_forward_ex", "router_workspace_size", "router_regime",
            "router_tc_groups", "router_select", "route_table", "router_strerror", "router_device_status",
-           "router_forward_noalloc", "router_near_tie_keys", "route_gather_add", "gbr_diag_chain")
+           "router_forward_noalloc", "router_near_tie_keys", "route_gather_add", "gbr_diag_chain",
+           "gbr_diag_act_sweep", "gbr_diag_act_coef")
 
 
 class RouterError(RuntimeError):
@@ -85,6 +86,10 @@ def lib() -> ctypes.CDLL:
             L.router_device_status.argtypes = [I]
             L.gbr_diag_chain.argtypes = [I, I, P, S, P, P]
             L.gbr_diag_chain.restype = I
+            L.gbr_diag_act_sweep.argtypes = [I, ctypes.c_ulonglong, ctypes.c_ulonglong, P, P]
+            L.gbr_diag_act_sweep.restype = I
+            L.gbr_diag_act_coef.argtypes = [I]
+            L.gbr_diag_act_coef.restype = ctypes.c_float
             if _variant == "stamps":
                 L.router_phase_stamps.argtypes = [P, P, P, P]
                 L.router_phase_stamps.restype = I
@@ -210,20 +215,39 @@ def diag_chain(kind, n, x, sink, stream=None):
         raise RuntimeError(f"gbr_diag_chain failed ({rc})")
 
 
-def phase_stamps():
+def diag_act_sweep(act, first, count, out, stream=None):
+    """Error sweep of the FP32 score ``act`` over the FP32 bit patterns
+    [first, first + count) (``include/gbrouter_diag.h``); out: device float32
+    tensor of 2, written asynchronously."""
+    rc = lib().gbr_diag_act_sweep(int(act), int(first), int(count), _ptr(out), _stream(stream))
+    if rc != 0:
+        raise RuntimeError(f"gbr_diag_act_sweep failed ({rc})")
+
+
+def diag_act_coef(act):
+    """The coefficient c of the kernels' FP32 score bound c 2^-23 a + 2^-60."""
+    return float(lib().gbr_diag_act_coef(int(act)))
+
+
+def phase_stamps(with_refines=False):
     """Measurement build only: the single-cluster kernel's phase stamps as a
     numpy array [calls, ctas, phases] of %globaltimer ns (0 = not stamped),
-    and the last selection's sub-phase stamps per CTA rank [16, 5]."""
+    and the last selection's sub-phase stamps per CTA rank [16, 5]; with
+    with_refines, also the counts of warp selections (small-M kernels) that
+    re-ranked near ties and that went on to FP64 since the previous read."""
     import numpy as np
     L = lib()
     c, t, p = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     L.router_phase_stamps(None, ctypes.byref(c), ctypes.byref(t), ctypes.byref(p))
     n = c.value * t.value * p.value
-    buf = np.zeros(n + 16 * 5, dtype=np.uint64)
+    buf = np.zeros(n + 16 * 5 + 2, dtype=np.uint64)
     if L.router_phase_stamps(buf.ctypes.data_as(ctypes.c_void_p), ctypes.byref(c), ctypes.byref(t),
                              ctypes.byref(p)) != 0:
         raise RuntimeError("router_phase_stamps failed")
-    return buf[:n].reshape(c.value, t.value, p.value), buf[n:].reshape(16, 5)
+    st, sel = buf[:n].reshape(c.value, t.value, p.value), buf[n:n + 80].reshape(16, 5)
+    if with_refines:
+        return st, sel, (int(buf[n + 80]), int(buf[n + 81]))
+    return st, sel
 
 
 def tc_phase_stamps():

@@ -149,3 +149,17 @@ def test_prefill_workspace_layout():
     # stream-K groups: none outside the prefill kernel, -1 for rejected shapes
     assert R.router_tc_groups(8, 2048, 256, 8) == 0
     assert R.router_tc_groups(1, 64, 16, 17) == -1
+
+
+def test_act_sweep_argument_errors_and_coefficients():
+    """The score sweep rejects bad calls before any CUDA call; the kernels'
+    score-bound coefficients leave room above the reference compositions'
+    own bounds (2.25 and 3)."""
+    L = R.lib()
+    fake = ctypes.c_void_p(16)
+    assert L.gbr_diag_act_sweep(R.GBR_ACT_SOFTMAX, 0, 16, fake, None) == 1
+    assert L.gbr_diag_act_sweep(R.GBR_ACT_SIGMOID, 0, 16, None, None) == 1
+    assert L.gbr_diag_act_sweep(R.GBR_ACT_SIGMOID, 1 << 32, 1, fake, None) == 1
+    assert L.gbr_diag_act_sweep(R.GBR_ACT_SIGMOID, 5, (1 << 32) - 4, fake, None) == 1
+    assert R.diag_act_coef(R.GBR_ACT_SQRT_SOFTPLUS) > 2.25
+    assert R.diag_act_coef(R.GBR_ACT_SIGMOID) > 3.0
