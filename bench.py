@@ -781,9 +781,19 @@ def run_phase_stamps_prefill(args):
                            "acc": float(rel[c, 3]), "refined": int(st[c, 10])}
                           for c in np.argsort(-rel[:, 9])[:6]]
         if args.stamps_dump:  # per CTA: SM, plan, accumulator complete, end (us)
+            def us(col):
+                return [round(float(v - t0) / 1e3, 3) if v > 0 else None for v in st[:, col]]
             ent["per_cta"] = {"sm": st[:, 18].tolist(), "plan": st[:, 19].tolist(),
                               "acc": [round(float(v), 3) for v in rel[:, 3]],
-                              "end": [round(float(v), 3) for v in rel[:, 9]]}
+                              "parts": [round(float(v), 3) for v in rel[:, 4]],
+                              "end": [round(float(v), 3) for v in rel[:, 9]],
+                              "accp": us(20), "published": us(21), "prefetched": us(22),
+                              "last_mma": us(23), "b0_flag": us(24), "b0_landed": us(25),
+                              "b0_added": us(26), "bl_flag": us(27), "bl_landed": us(28),
+                              "bl_added": us(29),
+                              "refine": [[us(30 + 4 * q)[c], us(31 + 4 * q)[c], us(32 + 4 * q)[c],
+                                          int(st[c, 33 + 4 * q])] for c in range(len(st))
+                                         for q in range(4) if st[c, 30 + 4 * q] > 0]}
         out.append(ent)
     print(json.dumps({"workload": f"prefill M={args.stamps_prefill_m}, H=7168, E=256, k=8, "
                                   f"sqrt-softplus + bias, {'NVFP4' if w_dtype else 'BF16'} W",

@@ -31,6 +31,12 @@
  * a sweep maximum plus the reference composition's own bound (2.25 for
  * sqrt-softplus, 3 for the sigmoid) must stay below it.
  *
+ * gbr_diag_near_key_cycles times the near-tie key (the double-float score
+ * plus bias the selection re-ranks close keys with) for `act`: one warp
+ * evaluates it `reps` times per lane in a dependent chain and writes the SM
+ * cycles per evaluation to out[0] (device, 2 long longs, caller-owned).
+ * Returns 0, 1 for a bad argument, 3 for a CUDA error.
+ *
  * The measurement build of the library (build.py variant "stamps",
  * -DGBR_PHASE_STAMPS) also exports router_phase_stamps(), which copies the
  * single-cluster kernel's per-phase %globaltimer stamps to host memory;
@@ -52,6 +58,7 @@ int gbr_diag_chain(int kind, int n, const void* x, size_t x_bytes, unsigned* sin
 int gbr_diag_act_sweep(int act, unsigned long long first, unsigned long long count, float* out,
                        cudaStream_t stream);
 float gbr_diag_act_coef(int act);
+int gbr_diag_near_key_cycles(int act, int reps, long long* out, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

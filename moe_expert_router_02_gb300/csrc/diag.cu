@@ -7,6 +7,7 @@
 
 #include "../../include/gbrouter_diag.h"
 #include "common.cuh"
+#include "dfkey.cuh"
 
 namespace gbr {
 namespace {
@@ -89,8 +90,31 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Latency of one near-tie key evaluation: a single warp evaluates it `reps`
+// times per lane in a dependent chain; out[0] = SM cycles per evaluation
+// (lane 0's clock64 difference / reps).
+__global__ void k_diag_near_key_cycles(int act, int reps, long long* out) {
+  float z = -3.0f + 0.2f * (float)threadIdx.x;
+  float acc = 0.0f;
+  const long long t0 = clock64();
+  for (int r = 0; r < reps; ++r) {
+    const NearKey nk = near_key(act, z, 0.01f);
+    acc += nk.lo;
+    z += nk.lo * 0x1p-100f;  // a dependence on the previous evaluation, value unchanged
+  }
+  const long long t1 = clock64();
+  if (threadIdx.x == 0) out[0] = (t1 - t0) / (reps > 0 ? reps : 1);
+  if (acc == 12345.0f) out[1] = 1;  // keeps the chain live
+}
+
 }  // namespace
 }  // namespace gbr
+
+extern "C" int gbr_diag_near_key_cycles(int act, int reps, long long* out, cudaStream_t stream) {
+  if ((act != gbr::ACT_SQRT_SOFTPLUS && act != gbr::ACT_SIGMOID) || !out || reps < 1) return 1;
+  gbr::k_diag_near_key_cycles<<<1, 32, 0, stream>>>(act, reps, out);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
 
 extern "C" float gbr_diag_act_coef(int act) { return gbr::act_err_coef(act); }
 

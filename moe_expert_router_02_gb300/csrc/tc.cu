@@ -252,13 +252,18 @@ int tc_read_status(int clear) {
 }
 
 #ifdef GBR_PHASE_STAMPS
-// Measurement build only: the last prefill launch's stamps [160][kTcStamps]
-// (zeros for CTAs the launch did not have), copied to host memory.
+// Measurement build only: the stamps [160][kTcStamps] of the prefill
+// launches since the previous read (zeros where nothing stamped), copied to
+// host memory; the buffer is then cleared.
 extern "C" int router_tc_phase_stamps(unsigned long long* host, int* ctas, int* phases) {
   *ctas = kTcStampCtas, *phases = kTcStamps;
   if (!host) return 0;
   if (cudaDeviceSynchronize() != cudaSuccess) return 3;
-  return cudaMemcpyFromSymbol(host, g_tc_stamps, sizeof(g_tc_stamps)) == cudaSuccess ? 0 : 3;
+  if (cudaMemcpyFromSymbol(host, g_tc_stamps, sizeof(g_tc_stamps)) != cudaSuccess) return 3;
+  void* d = nullptr;
+  if (cudaGetSymbolAddress(&d, g_tc_stamps) != cudaSuccess) return 3;
+  if (cudaMemset(d, 0, sizeof(g_tc_stamps)) != cudaSuccess) return 3;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : 3;
 }
 #endif
 

@@ -577,27 +577,28 @@ __device__ __noinline__ bool refine_in_list(int act, const uint32_t* l_o, int32_
   bool in_list = false;
   uint32_t need = 0u;
   if (close) {
+    // the whole list at once (one shared-memory round trip), then the
+    // entries next to a gap of at most `band`; empty entries (0) sort last
+    uint32_t o[KC];
+#pragma unroll
+    for (int j = 0; j < KC; ++j) o[j] = l_o[j * BM];
     const float lo = __fsub_rd(thr, band);
-    in_list = l_o[(KC - 1) * BM] == 0u || float_of_ord(l_o[(KC - 1) * BM]) < lo;
+    in_list = o[KC - 1] == 0u || float_of_ord(o[KC - 1]) < lo;
     if (in_list) {
-      float prev = INFINITY;
-#pragma unroll 1
+#pragma unroll
       for (int j = 0; j < KC; ++j) {
-        const uint32_t o = l_o[j * BM];
-        if (o == 0u) break;  // empty entries sort last
-        const float kj = float_of_ord(o);
-        const uint32_t on = j + 1 < KC ? l_o[(j + 1) * BM] : 0u;
-        const bool up = j > 0 && __fsub_rd(prev, kj) <= band;
-        const bool dn = on != 0u && __fsub_rd(kj, float_of_ord(on)) <= band;
-        if (kj >= lo && (up || dn)) need |= 1u << j;
-        prev = kj;
+        const float kj = float_of_ord(o[j]);
+        const bool up = j > 0 && __fsub_rd(float_of_ord(o[j > 0 ? j - 1 : 0]), kj) <= band;
+        const bool dn = j + 1 < KC && o[j + 1 < KC ? j + 1 : j] != 0u &&
+                        __fsub_rd(kj, float_of_ord(o[j + 1 < KC ? j + 1 : j])) <= band;
+        if (o[j] != 0u && kj >= lo && (up || dn)) need |= 1u << j;
       }
     }
   }
   // pool (expert, owner lane, slot) items of the needed entries
   const int nneed = __popc(need);
   int qoff = nneed;
-#pragma unroll 1
+#pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
     const int t = __shfl_up_sync(kFull, qoff, d);
     if (lane >= d) qoff += t;
@@ -614,7 +615,7 @@ __device__ __noinline__ bool refine_in_list(int act, const uint32_t* l_o, int32_
   float* it_s = reinterpret_cast<float*>(wl + 768);
   {
     int q = qoff;
-#pragma unroll 1
+#pragma unroll
     for (int j = 0; j < KC; ++j)
       if ((need >> j) & 1u)
         it_e[q++] = ((uint32_t)l_i[j * BM] << 16) | ((uint32_t)lane << 5) | (uint32_t)j;
@@ -679,16 +680,24 @@ __device__ __noinline__ bool refine_in_list(int act, const uint32_t* l_o, int32_
     refine_fp64<KC>(act, l_o, l_i, l_z, need, amb, qoff, qtotal, zq, sb, wl);
   }
   if (need != 0u && !amb) {
-    // the sorted items' scores (from their original slots), then the refill
-#pragma unroll 1
-    for (int q = qoff; q < qoff + nneed; ++q) it_s[q] = l_z[(int)(it_e[q] & 31u) * BM];
-    int q = qoff;
-#pragma unroll 1
+    // the sorted items and their scores (from their original slots), all
+    // read before the needed slots are refilled in order
+    uint32_t ev[KC];
+    float sv[KC];
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      ev[j] = 0u;
+      sv[j] = 0.0f;
+      if ((need >> j) & 1u) {
+        ev[j] = it_e[qoff + __popc(need & ((1u << j) - 1u))];
+        sv[j] = l_z[(int)(ev[j] & 31u) * BM];
+      }
+    }
+#pragma unroll
     for (int j = 0; j < KC; ++j) {
       if ((need >> j) & 1u) {
-        l_i[j * BM] = (int)(it_e[q] >> 16);
-        l_z[j * BM] = it_s[q];
-        ++q;
+        l_i[j * BM] = (int)(ev[j] >> 16);
+        l_z[j * BM] = sv[j];
       }
     }
   }
@@ -734,8 +743,15 @@ struct TcParams {
 // CTAs), 12 threshold computed, 13 pass B masks built, 14 pooled
 // activations done, 15 insertion done; slots 16 and 17 hold thread 0's
 // candidate count and its warp's pooled total, 18 the SM the CTA ran on,
-// 19 its plan (2 x segments + 1 if it finishes a tile).
-constexpr int kTcStamps = 20;
+// 19 its plan (2 x segments + 1 if it finishes a tile), 20 its partial
+// accumulator complete, 21 that partial published, 22 the early partials
+// of its tile streamed in, 23 its last MMA issued (even CTAs); of the
+// partials added after the main loop, the first one's flag seen (24),
+// copy landed (25) and sum stored (26), and the same for the last (27-29);
+// per first-half warp q (0..3) that re-ranked near ties, slots 30 + 4q..:
+// re-rank start, list re-ranked, every-column pass done (0: none), and
+// whether that pass ran.
+constexpr int kTcStamps = 46;
 
 namespace {
 
@@ -1016,6 +1032,9 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         if (PAIR) mma_commit_pair(done);
         else mma_commit(done);
       }
+#ifdef GBR_PHASE_STAMPS
+      if (p.stamps) p.stamps[blockIdx.x * kTcStamps + 23] = globaltimer();
+#endif
     }
   } else if (warp < kEpiWarps) {
     // epilogue: warp w reads TMEM lanes 32(w%4).. of columns half w/4
@@ -1152,17 +1171,31 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       // [E/4][BM][4] (a warp stores 512 contiguous bytes per 4 columns), then
       // the flag; finishers fetch it with one bulk copy
       const bool okp = mbar_wait_warp(wstat, smem_u32(accp), 0);
+      TC_STAMP(20);
       tc_fence_after();
       if (okp) {
+        // two 32-column loads in flight per round
         float* part = p.sk_part + (size_t)blockIdx.x * E * BM + row * 4;
-        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-          float v[32];
-          tmem_ld32(trow + (uint32_t)p.acc2 + c0, v);
+        for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
+          const bool two = c0 + 32 < c_hi;
+          uint32_t r0[32], r1[32];
+          tmem_ld32_issue(trow + (uint32_t)p.acc2 + c0, r0);
+          if (two) tmem_ld32_issue(trow + (uint32_t)p.acc2 + c0 + 32, r1);
+          tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 8; ++i)  // E % 16 == 0: a group of 4 is all in or all out
             if (c0 + 4 * i < c_hi)
-              st_cg_v4(part + (size_t)(c0 / 4 + i) * BM * 4, v[4 * i], v[4 * i + 1],
-                       v[4 * i + 2], v[4 * i + 3]);
+              st_cg_v4(part + (size_t)(c0 / 4 + i) * BM * 4, __uint_as_float(r0[4 * i]),
+                       __uint_as_float(r0[4 * i + 1]), __uint_as_float(r0[4 * i + 2]),
+                       __uint_as_float(r0[4 * i + 3]));
+          if (two) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (c0 + 32 + 4 * i < c_hi)
+                st_cg_v4(part + (size_t)((c0 + 32) / 4 + i) * BM * 4, __uint_as_float(r1[4 * i]),
+                         __uint_as_float(r1[4 * i + 1]), __uint_as_float(r1[4 * i + 2]),
+                         __uint_as_float(r1[4 * i + 3]));
+          }
         }
       }
       asm volatile("fence.proxy.async.global;" ::: "memory");  // read by bulk copies
@@ -1173,6 +1206,7 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
                      "r"(sk_want)
                      : "memory");
       }
+      TC_STAMP(21);
     }
     // The finished tile's other partials P_q (groups p0 .. grp-1) are summed
     // in group order into S in the spare accumulator columns, and the tile's
@@ -1192,11 +1226,14 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         const uint64_t t0 = globaltimer();
         uint32_t ns = 64;
         for (;;) {
+          // once the main loop is done the bulk copies win, even for a
+          // partial that is already out
+          if (mbar_try(smem_u32(accf), 0)) break;
           if (ld_acquire_u32(p.sk_flag + slot) == sk_want) {
             go = 1;
             break;
           }
-          if (mbar_try(smem_u32(accf), 0) || globaltimer() - t0 > kWaitNs) break;
+          if (globaltimer() - t0 > kWaitNs) break;
           __nanosleep(ns);
           if (ns < 512) ns <<= 1;
         }
@@ -1208,26 +1245,36 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       if (!go) break;
       wait_flag(wstat, p.sk_flag + slot, sk_want);  // set: this thread's own acquire
       const float* part = p.sk_part + (size_t)slot * E * BM + row * 4;
-      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-        float v[32];
+      for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
+        // two 32-column groups of loads in flight per round
+        float v[2][32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          // E % 16 == 0: a group of 4 columns is all in or all out
-          const int g4 = min(c0 / 4 + i, E / 4 - 1);
-          const float4 u = __ldcg(reinterpret_cast<const float4*>(part + (size_t)g4 * BM * 4));
-          v[4 * i] = u.x, v[4 * i + 1] = u.y, v[4 * i + 2] = u.z, v[4 * i + 3] = u.w;
-        }
-        if (pre > 0) {
-          float w[32];
-          tmem_ld32(tS + c0, w);
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = w[j] + v[j];
+          for (int i = 0; i < 8; ++i) {
+            // E % 16 == 0: a group of 4 columns is all in or all out
+            const int g4 = min((c0 + 32 * h) / 4 + i, E / 4 - 1);
+            const float4 u = __ldcg(reinterpret_cast<const float4*>(part + (size_t)g4 * BM * 4));
+            v[h][4 * i] = u.x, v[h][4 * i + 1] = u.y, v[h][4 * i + 2] = u.z, v[h][4 * i + 3] = u.w;
+          }
         }
-        tmem_st32(tS + c0, v);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (c0 + 32 * h < c_hi) {
+            if (pre > 0) {
+              float w[32];
+              tmem_ld32(tS + c0 + 32 * h, w);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[h][j] = w[j] + v[h][j];
+            }
+            tmem_st32(tS + c0 + 32 * h, v[h]);
+          }
+        }
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       ++pre;
     }
+    TC_STAMP(22);
     // a CTA whose range ends inside a tile has no rows to finish
     const bool ok = has_fin && mbar_wait_warp(wstat, smem_u32(accf), 0);
     TC_STAMP(3);
@@ -1241,9 +1288,16 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         const bool last = q >= grp - 1;
         const bool have = q < grp;
         bool okq = true;
+#ifdef GBR_PHASE_STAMPS
+        const int sfirst = q == plan.p0 + pre ? 24 : -1, slast = last ? 27 : -1;
+#endif
         if (have) {
           const int slot = q * (PAIR ? 2 : 1) + crank;
           wait_flag(wstat, p.sk_flag + slot, sk_want);
+#ifdef GBR_PHASE_STAMPS
+          if (sfirst >= 0) TC_STAMP(24);
+          if (slast >= 0) TC_STAMP(27);
+#endif
           if (threadIdx.x == 0) {
             asm volatile("fence.proxy.async.global;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1252,6 +1306,10 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
                      smem_u32(&s_pbar));
           }
           okq = mbar_wait_warp(wstat, smem_u32(&s_pbar), (uint32_t)(q - plan.p0 - pre) & 1u);
+#ifdef GBR_PHASE_STAMPS
+          if (sfirst >= 0) TC_STAMP(25);
+          if (slast >= 0) TC_STAMP(28);
+#endif
         }
         if (okq) {
           const bool hasS = q > plan.p0;  // S holds P_p0 .. P_(q-1)
@@ -1286,6 +1344,10 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         // every warp is done with the staged partial before the next lands
         // (or, after the last, before pass A writes over the ring)
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+#ifdef GBR_PHASE_STAMPS
+        if (sfirst >= 0 && have) TC_STAMP(26);
+        if (slast >= 0 && have) TC_STAMP(29);
+#endif
         if (last) break;
       }
     }
@@ -1598,8 +1660,14 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         }
         uint32_t* wl = reinterpret_cast<uint32_t*>(tiles + kCandOffset + (size_t)E * BM * 4) +
                        warp * kListCap;  // this warp's candidate list is spent
+#ifdef GBR_PHASE_STAMPS
+        if (lane == 0 && p.stamps) p.stamps[blockIdx.x * kTcStamps + 30 + 4 * quad] = globaltimer();
+#endif
         slow = refine_in_list<KC>(act, xo + row, xi + row, xz + row, close, band, thr,
                                   zbuf + quad * 32, has_bias ? s_bias : nullptr, wl);
+#ifdef GBR_PHASE_STAMPS
+        if (lane == 0 && p.stamps) p.stamps[blockIdx.x * kTcStamps + 31 + 4 * quad] = globaltimer();
+#endif
         if (close) {
 #pragma unroll
           for (int j = 0; j < KC; ++j) {
@@ -1610,6 +1678,12 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
       }
       if (__any_sync(kFull, slow)) {  // near ties reaching past the list: every column
         refine_row<KC, FP4>(trow, E, g, a.bias, act, thr, slow, xi + row, xz + row);
+#ifdef GBR_PHASE_STAMPS
+        if (lane == 0 && p.stamps) {
+          p.stamps[blockIdx.x * kTcStamps + 32 + 4 * quad] = globaltimer();
+          p.stamps[blockIdx.x * kTcStamps + 33 + 4 * quad] = 1;
+        }
+#endif
         if (slow) {
 #pragma unroll
           for (int j = 0; j < KC; ++j) {

@@ -25,7 +25,7 @@ GBR_REGIME_GENERIC, GBR_REGIME_GEMV, GBR_REGIME_TC, GBR_REGIME_UNFUSED, GBR_REGI
 EXPORTS = ("router_forward", "router_forward_ex", "router_workspace_size", "router_regime",
            "router_tc_groups", "router_select", "route_table", "router_strerror", "router_device_status",
            "router_forward_noalloc", "router_near_tie_keys", "route_gather_add", "gbr_diag_chain",
-           "gbr_diag_act_sweep", "gbr_diag_act_coef")
+           "gbr_diag_act_sweep", "gbr_diag_act_coef", "gbr_diag_near_key_cycles")
 
 
 class RouterError(RuntimeError):
@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
             L.gbr_diag_act_sweep.restype = I
             L.gbr_diag_act_coef.argtypes = [I]
             L.gbr_diag_act_coef.restype = ctypes.c_float
+            L.gbr_diag_near_key_cycles.argtypes = [I, I, P, P]
+            L.gbr_diag_near_key_cycles.restype = I
             if _variant == "stamps":
                 L.router_phase_stamps.argtypes = [P, P, P, P]
                 L.router_phase_stamps.restype = I
@@ -224,6 +226,17 @@ def diag_act_sweep(act, first, count, out, stream=None):
         raise RuntimeError(f"gbr_diag_act_sweep failed ({rc})")
 
 
+def diag_near_key_cycles(act, reps=64):
+    """SM cycles per near-tie key evaluation (one warp, dependent chain)."""
+    import torch
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    rc = lib().gbr_diag_near_key_cycles(int(act), int(reps), _ptr(out), _stream(None))
+    if rc != 0:
+        raise RuntimeError(f"gbr_diag_near_key_cycles failed ({rc})")
+    torch.cuda.synchronize()
+    return int(out[0])
+
+
 def diag_act_coef(act):
     """The coefficient c of the kernels' FP32 score bound c 2^-23 a + 2^-60."""
     return float(lib().gbr_diag_act_coef(int(act)))
@@ -251,8 +264,9 @@ def phase_stamps(with_refines=False):
 
 
 def tc_phase_stamps():
-    """Measurement build only: the last prefill launch's phase stamps as a
-    numpy array [ctas, phases] (%globaltimer ns; see the prefill kernel)."""
+    """Measurement build only: the phase stamps of the prefill launches since
+    the previous read as a numpy array [ctas, phases] (%globaltimer ns, 0 =
+    not stamped; see the prefill kernel); reading clears them."""
     import numpy as np
     L = lib()
     c, p = ctypes.c_int(), ctypes.c_int()
