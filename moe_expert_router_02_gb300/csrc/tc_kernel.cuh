@@ -1178,23 +1178,20 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
         float* part = p.sk_part + (size_t)blockIdx.x * E * BM + row * 4;
         for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
           const bool two = c0 + 32 < c_hi;
-          uint32_t r0[32], r1[32];
-          tmem_ld32_issue(trow + (uint32_t)p.acc2 + c0, r0);
-          if (two) tmem_ld32_issue(trow + (uint32_t)p.acc2 + c0 + 32, r1);
+          uint32_t r[2][32];
+          tmem_ld32_issue(trow + (uint32_t)p.acc2 + c0, r[0]);
+          if (two) tmem_ld32_issue(trow + (uint32_t)p.acc2 + c0 + 32, r[1]);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; ++i)  // E % 16 == 0: a group of 4 is all in or all out
-            if (c0 + 4 * i < c_hi)
-              st_cg_v4(part + (size_t)(c0 / 4 + i) * BM * 4, __uint_as_float(r0[4 * i]),
-                       __uint_as_float(r0[4 * i + 1]), __uint_as_float(r0[4 * i + 2]),
-                       __uint_as_float(r0[4 * i + 3]));
-          if (two) {
+          for (int h = 0; h < 2; ++h) {
+            if (h == 0 || two) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (c0 + 32 + 4 * i < c_hi)
-                st_cg_v4(part + (size_t)((c0 + 32) / 4 + i) * BM * 4, __uint_as_float(r1[4 * i]),
-                         __uint_as_float(r1[4 * i + 1]), __uint_as_float(r1[4 * i + 2]),
-                         __uint_as_float(r1[4 * i + 3]));
+              for (int i = 0; i < 8; ++i)  // E % 16 == 0: a group of 4 is all in or all out
+                if (c0 + 32 * h + 4 * i < c_hi)
+                  st_cg_v4(part + (size_t)((c0 + 32 * h) / 4 + i) * BM * 4,
+                           __uint_as_float(r[h][4 * i]), __uint_as_float(r[h][4 * i + 1]),
+                           __uint_as_float(r[h][4 * i + 2]), __uint_as_float(r[h][4 * i + 3]));
+            }
           }
         }
       }
@@ -1302,8 +1299,12 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
             asm volatile("fence.proxy.async.global;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_expect_tx(smem_u32(&s_pbar), pbytes);
-            bulk_g2s(smem_u32(tiles), p.sk_part + (size_t)slot * E * BM, pbytes,
-                     smem_u32(&s_pbar));
+            // eight copies in flight rather than one (pbytes / 8 = 64 E bytes)
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.sk_part + (size_t)slot * E * BM);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              bulk_g2s(smem_u32(tiles) + c * (pbytes / 8), src + c * (pbytes / 8), pbytes / 8,
+                       smem_u32(&s_pbar));
           }
           okq = mbar_wait_warp(wstat, smem_u32(&s_pbar), (uint32_t)(q - plan.p0 - pre) & 1u);
 #ifdef GBR_PHASE_STAMPS
