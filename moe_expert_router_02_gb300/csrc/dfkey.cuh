@@ -13,12 +13,14 @@
 // Methods: error-free sum and product (Knuth's TwoSum, Dekker's Fast2Sum,
 // the FMA product residual) and Dekker's double-length multiplication;
 // exp by Cody and Waite's argument reduction with ln 2 split in three
-// parts, the Taylor series of expm1 in double-float on x / 16 and four
-// doublings expm1(2y) = expm1(y) (expm1(y) + 2); log1p by one Newton step
-// on e^y - 1 - u from the FP32 log1pf; sqrt by one Newton (Heron) step.
-// The constants are ln 2 and 1/k! rounded to float: C1 is ln 2 to 15
-// significant bits (n * C1 is exact for n < 2^8), C2 and C3 the next
-// float-rounded parts (C1 + C2 + C3 - ln 2 = -1.3e-21).
+// parts, the Taylor series of expm1 on x / 4 (double-float terms through
+// y^5/120, the rest in FP32) and two doublings expm1(2y) = expm1(y)
+// (expm1(y) + 2); log1p(u) as 2 atanh(u / (2 + u)) by its power series
+// (double-float terms through w^5/11 in w = s^2 <= 1/9, the rest in FP32);
+// sqrt by one Newton (Heron) step. The constants are ln 2, 1/k! and
+// 1/(2k+1) rounded to float, or split into two floats where a term needs
+// more: C1 is ln 2 to 15 significant bits (n * C1 is exact for n < 2^8), C2
+// and C3 the next float-rounded parts (C1 + C2 + C3 - ln 2 = -1.3e-21).
 #pragma once
 
 #include <cstdint>
@@ -64,6 +66,14 @@ __device__ __forceinline__ df32 df_add_f(df32 x, float b) {
   return fast_two_sum(s.hi, s.lo);
 }
 
+// x + y for |x.hi| >= |y.hi| (Fast2Sum on the leading parts): the Horner
+// steps below, whose coefficient dominates the running product.
+__device__ __forceinline__ df32 df_add_big(df32 x, df32 y) {
+  df32 s = fast_two_sum(x.hi, y.hi);
+  s.lo = __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo));
+  return fast_two_sum(s.hi, s.lo);
+}
+
 __device__ __forceinline__ df32 df_mul(df32 x, df32 y) {
   df32 p = two_prod(x.hi, y.hi);
   p.lo = __fmaf_rn(x.hi, y.lo, p.lo);
@@ -75,32 +85,27 @@ __device__ __forceinline__ df32 df_scale(df32 x, float pow2) {  // exact for pow
   return {__fmul_rn(x.hi, pow2), __fmul_rn(x.lo, pow2)};
 }
 
-// 1/k! for k = 1..9 as double-floats.
-static __constant__ float2 c_inv_fact[9] = {
-    {0x1p+0f, 0.0f},
-    {0x1p-1f, 0.0f},
-    {0x1.555556p-3f, -0x1.555556p-28f},
-    {0x1.555556p-5f, -0x1.555556p-30f},
-    {0x1.111112p-7f, -0x1.dddddep-32f},
-    {0x1.6c16c2p-10f, -0x1.27d27ep-35f},
-    {0x1.a01a02p-13f, -0x1.7f97fap-39f},
-    {0x1.a01a02p-16f, -0x1.7f97fap-42f},
-    {0x1.71de3ap-19f, 0x1.55b1ccp-45f}};
-
-// expm1(x) for |x| <= 0.75, relative error about 2^-44: the Taylor series
-// to degree 9 on y = x / 16 (the first dropped term is below 2^-55 of the
-// result), then four doublings. This path only runs for near ties, so its
-// code is cold whenever it runs: the loops stay rolled and the function
-// out of line, which keeps the instruction fetches few.
+// expm1(x) for |x| <= 0.75, relative error below 2^-44: y = x / 4 (|y| <=
+// 0.1875), the Taylor series y (1 + y/2 + y^2/6 + y^3/24 + y^4/120 + y^5 t)
+// by Horner's rule in double-float, with t = 1/720 + ... + y^4/3628800 in
+// FP32 (its terms are below 2^-21 of the result, and the first one dropped
+// below 2^-47), then two doublings. This path only runs for near ties, so
+// its code is cold whenever it runs: the function stays out of line, which
+// keeps the instruction fetches few.
 static __device__ __noinline__ df32 expm1_df(df32 x) {
-  const df32 y = df_scale(x, 0x1p-4f);  // |y| <= 0.047
-  df32 p = df32{c_inv_fact[8].x, c_inv_fact[8].y};
-#pragma unroll 1
-  for (int i = 7; i >= 0; --i) p = df_add(df_mul(p, y), df32{c_inv_fact[i].x, c_inv_fact[i].y});
-  df32 e = df_mul(p, y);
-#pragma unroll 1
-  for (int i = 0; i < 4; ++i) e = df_mul(e, df_add_f(e, 2.0f));  // expm1(2v) from expm1(v)
-  return e;
+  const df32 y = df_scale(x, 0x1p-2f);
+  float t = __fmaf_rn(y.hi, 0x1.27e4fcp-22f, 0x1.71de3ap-19f);  // 1/10!, 1/9!
+  t = __fmaf_rn(t, y.hi, 0x1.a01a02p-16f);                      // 1/8!
+  t = __fmaf_rn(t, y.hi, 0x1.a01a02p-13f);                      // 1/7!
+  t = __fmaf_rn(t, y.hi, 0x1.6c16c2p-10f);                      // 1/6!
+  df32 p = fast_two_sum(0x1.111112p-7f, __fmaf_rn(y.hi, t, -0x1.dddddep-32f));  // 1/120 + y t
+  p = df_add_big(df32{0x1.555556p-5f, -0x1.555556p-30f}, df_mul(y, p));       // 1/24 + y p
+  p = df_add_big(df32{0x1.555556p-3f, -0x1.555556p-28f}, df_mul(y, p));       // 1/6 + y p
+  p = df_add_big(df32{0.5f, 0.0f}, df_mul(y, p));                              // 1/2 + y p
+  p = df_add_big(df32{1.0f, 0.0f}, df_mul(y, p));                              // 1 + y p
+  df32 e = df_mul(y, p);
+  e = df_mul(e, df_add_f(e, 2.0f));  // expm1(2v) from expm1(v)
+  return df_mul(e, df_add_f(e, 2.0f));
 }
 
 // Largest |z| the double-float path takes; beyond it the callers use FP64.
@@ -125,12 +130,32 @@ __device__ __forceinline__ df32 sqrt_softplus_df(float z) {
   const df32 em = expm1_df(df32{-r.hi, -r.lo});
   df32 u = df_add_f(em, 1.0f);
   u = df_scale(u, __int_as_float((127 - (int)n) << 23));  // 2^-n, n in 0..44
-  // log1p(u): y0 from FP32, one Newton step y1 = y0 + (u - expm1(y0)) / (1 + expm1(y0))
-  const float y0 = log1pf(u.hi);
-  const df32 e1 = expm1_df(df32{y0, 0.0f});
-  const df32 d = df_add(u, df32{-e1.hi, -e1.lo});
-  const float delta = __fdiv_rn(__fadd_rn(d.hi, d.lo), __fadd_rn(1.0f, e1.hi));
-  df32 sp = fast_two_sum(y0, delta);
+  // log1p(u) = 2 atanh(s), s = u / (2 + u) in (0, 1/3]: s to FP32, then
+  // the remainder u - s (2 + u), whose leading part cancels exactly
+  const df32 dd = df_add_f(u, 2.0f);
+  const float q0 = __fdividef(u.hi, dd.hi);
+  const df32 qd = two_prod(q0, dd.hi);
+  const float rem = __fadd_rn(__fsub_rn(__fsub_rn(u.hi, qd.hi), qd.lo),
+                              __fsub_rn(u.lo, __fmul_rn(q0, dd.lo)));
+  const df32 sv = fast_two_sum(q0, __fdividef(rem, dd.hi));
+  df32 w = two_prod(sv.hi, sv.hi);  // w = s^2 <= 1/9
+  w = fast_two_sum(w.hi, __fmaf_rn(2.0f * sv.hi, sv.lo, w.lo));
+  // 1 + w/3 + w^2/5 + ...: terms from w^6/13 on in FP32 (below 2^-22 of the
+  // sum; the first one dropped, w^14/29, below 2^-48)
+  float t = __fmaf_rn(w.hi, 0x1.2f684cp-5f, 0x1.47ae14p-5f);  // 1/27, 1/25
+  t = __fmaf_rn(t, w.hi, 0x1.642c86p-5f);                     // 1/23
+  t = __fmaf_rn(t, w.hi, 0x1.861862p-5f);                     // 1/21
+  t = __fmaf_rn(t, w.hi, 0x1.af286cp-5f);                     // 1/19
+  t = __fmaf_rn(t, w.hi, 0x1.e1e1e2p-5f);                     // 1/17
+  t = __fmaf_rn(t, w.hi, 0x1.111112p-4f);                     // 1/15
+  t = __fmaf_rn(t, w.hi, 0x1.3b13b2p-4f);                     // 1/13
+  df32 P = fast_two_sum(0x1.745d18p-4f, __fmaf_rn(w.hi, t, -0x1.745d18p-29f));  // 1/11 + w t
+  P = df_add_big(df32{0x1.c71c72p-4f, -0x1.c71c72p-31f}, df_mul(w, P));  // 1/9 + w P
+  P = df_add_big(df32{0x1.24924ap-3f, -0x1.b6db6ep-28f}, df_mul(w, P));  // 1/7 + w P
+  P = df_add_big(df32{0x1.99999ap-3f, -0x1.99999ap-29f}, df_mul(w, P));  // 1/5 + w P
+  P = df_add_big(df32{0x1.555556p-2f, -0x1.555556p-27f}, df_mul(w, P));  // 1/3 + w P
+  P = df_add_big(df32{1.0f, 0.0f}, df_mul(w, P));                        // 1 + w P
+  df32 sp = df_scale(df_mul(sv, P), 2.0f);
   if (z > 0.0f) sp = df_add_f(sp, z);
   // sqrt: s0 = RN(sqrt(sp.hi)); s = s0 + (sp - s0^2) / (2 s0), s0^2 exact as a product pair
   const float s0 = __fsqrt_rn(sp.hi);
