@@ -1316,6 +1316,11 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
           const bool hasS = q > plan.p0;  // S holds P_p0 .. P_(q-1)
           const float4* sp4 = reinterpret_cast<const float4*>(tiles) + row;
           for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+            // the tensor-memory loads (S, and the accumulator on the last
+            // round) are in flight together while the staged partial is read
+            uint32_t ws[32], fs[32];
+            if (hasS) tmem_ld32_issue(tS + c0, ws);
+            if (last) tmem_ld32_issue(trow + c0, fs);
             float v[32];
             if (have) {
 #pragma unroll
@@ -1324,17 +1329,15 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
                 v[4 * i] = u.x, v[4 * i + 1] = u.y, v[4 * i + 2] = u.z, v[4 * i + 3] = u.w;
               }
             }
+            if (hasS || last) tmem_wait_ld();
             if (hasS) {
-              float w[32];
-              tmem_ld32(tS + c0, w);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = have ? w[j] + v[j] : w[j];
+              for (int j = 0; j < 32; ++j)
+                v[j] = have ? __uint_as_float(ws[j]) + v[j] : __uint_as_float(ws[j]);
             }
             if (last) {
-              float f[32];
-              tmem_ld32(trow + c0, f);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = f[j] + v[j];
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(fs[j]) + v[j];
               tmem_st32(trow + c0, v);
             } else {
               tmem_st32(tS + c0, v);
