@@ -68,7 +68,8 @@ __device__ __forceinline__ void atom_exch_relaxed_gpu(uint32_t* p, uint32_t v) {
 }
 
 // ---------------------------------------------------------------------------
-// Single-cluster small-M router (M <= 16, E <= 256). One cluster of E/16
+// Single-cluster small-M router (M <= 64, E <= 256; one cluster per 16
+// rows, each routing its rows on its own). One cluster of E/16
 // CTAs holds all of W_gate in shared memory: CTA r owns experts
 // [16r, 16r+16) over the whole H, so there are no partial sums to combine
 // and no logits leave the cluster. Each CTA starts bulk copies of its 16 W
@@ -258,6 +259,28 @@ struct RowOwner {
   }
 };
 
+// Row groups: above 16 rows the single-cluster kernel runs one cluster per
+// 16 rows (blockIdx.y), each a complete router for its rows that stages all
+// of W itself; this is the sub-problem of group rg.
+constexpr int k1cRows = 16;
+__device__ __forceinline__ RouterArgs row_group(RouterArgs a, int rg) {
+  if (rg == 0 && a.M <= k1cRows) return a;
+  const int m0 = k1cRows * rg;
+  a.M = min(k1cRows, a.M - m0);
+  a.x = static_cast<const uint16_t*>(a.x) + (size_t)m0 * a.H;
+  a.out_idx += (size_t)m0 * a.k;
+  a.out_w += (size_t)m0 * a.k;
+  if (a.logits) a.logits += (size_t)m0 * a.E;
+  if (a.tbl_unique) {  // row pairs: m0 is even
+    const size_t g0 = (size_t)(m0 / 2);
+    a.tbl_unique += g0 * 2 * a.k;
+    a.tbl_mask += g0 * 2 * a.k;
+    a.tbl_map += g0 * 2 * a.k;
+    a.tbl_count += g0;
+  }
+  return a;
+}
+
 // NVFP4 weights: the CTA stages its 16 packed rows (fpitch bytes apart) and
 // their E4M3 block scales. With PREDEC the rows are decoded to BF16 in
 // shared memory before the wait on the preceding kernel, so the contraction
@@ -267,7 +290,8 @@ struct RowOwner {
 // the block scale) and g multiplies the FP32 sums.
 template <int NT, int VPL, bool FP4, bool PREDEC>
 __global__ void __launch_bounds__(k1cWarps * 32)
-    k_gemv1c_router(const RouterArgs a, int pitch, int fpitch) {
+    k_gemv1c_router(const RouterArgs a_all, int pitch, int fpitch) {
+  const RouterArgs a = row_group(a_all, (int)blockIdx.y);
   constexpr int NTOK = 8 * NT;
   constexpr bool kFrag4 = FP4 && !PREDEC;  // NVFP4 fragments decoded in the MMA loop
   // BF16 rows [16][pitch] (BF16 weights, or NVFP4 decoded there); NVFP4:
@@ -827,7 +851,7 @@ cudaError_t launch_1c_inst(const RouterArgs& a, bool pdl, cudaStream_t stream, b
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL);
+  cfg.gridDim = dim3(CL, (a.M + k1cRows - 1) / k1cRows);  // a cluster per 16 rows
   cfg.blockDim = dim3(k1cWarps * 32);
   cfg.dynamicSmemBytes = dsmem;
   cfg.stream = stream;
@@ -869,7 +893,7 @@ cudaError_t launch_1c(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe,
 }  // namespace
 
 bool gemv1c_eligible(int M, int H, int E, bool fp4) {
-  if (M < 1 || M > 16 || E % 16 != 0 || E < 16 || E > 256 || H % (fp4 ? 256 : 32) != 0)
+  if (M < 1 || M > 4 * k1cRows || E % 16 != 0 || E < 16 || E > 256 || H % (fp4 ? 256 : 32) != 0)
     return false;
   if (gemv1c_smem(H, fp4, fp4 && gemv1c_predec(H)) > k1cMaxDynSmem) return false;
   // the cluster must be schedulable with this much shared memory per CTA
@@ -877,7 +901,7 @@ bool gemv1c_eligible(int M, int H, int E, bool fp4) {
   static std::map<std::tuple<int, int, int, int>, bool> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  const auto key = std::make_tuple(dev, (M <= 8 ? 1 : 2) + (fp4 ? 2 : 0), E, H);
+  const auto key = std::make_tuple(dev, (M <= 8 ? 1 : 2) + (fp4 ? 2 : 0), E, H);  // one cluster's fit
   std::lock_guard<std::mutex> lk(mu);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;

@@ -27,7 +27,8 @@ cudaError_t launch_route_table(const int32_t* idx, int groups, int T, int k, int
 int gemv_cluster_size(int H);
 cudaError_t launch_gemv(const RouterArgs& a, bool select, bool pdl, cudaStream_t stream);
 
-// Small-M single-cluster router (M <= 16, E <= 256, W_gate in shared memory).
+// Small-M single-cluster router (E <= 256, W_gate in shared memory): one
+// cluster per 16 rows, M <= 64.
 bool gemv1c_eligible(int M, int H, int E, bool fp4);
 cudaError_t launch_gemv1c(const RouterArgs& a, bool pdl, cudaStream_t stream);
 

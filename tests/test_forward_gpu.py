@@ -107,7 +107,8 @@ def test_decode_softmax(M, dup):
 @pytest.mark.parametrize("M", [1, 16, 64])
 def test_sqrt_softplus_bias(M):
     case = synth.make_case(C["C2"], M=M, seed=10 + M, dup_frac=0.1)
-    check_case(case, expect_regime=R.GBR_REGIME_GEMV1C if M <= 16 else R.GBR_REGIME_GEMV)
+    # above 16 rows: one cluster per 16 rows
+    check_case(case, expect_regime=R.GBR_REGIME_GEMV1C)
     check_case(case, flags=R.GBR_FLAG_NO_SINGLE_CLUSTER, expect_regime=R.GBR_REGIME_GEMV)
 
 
@@ -191,9 +192,12 @@ def test_nvfp4_weights_small_M(M):
 
 
 def test_nvfp4_small_M_other_paths():
-    # 16 < M <= 64 and H not a multiple of 256 take the generic kernel
+    # 16 < M <= 64: a cluster per 16 rows (the last one ragged); H not a
+    # multiple of 256 takes the generic kernel
     check_case(synth.make_case(C["C2"], M=33, seed=1, w_dtype=synth.NVFP4),
-               expect_regime=R.GBR_REGIME_GENERIC)
+               expect_regime=R.GBR_REGIME_GEMV1C)
+    check_case(synth.make_case(C["C2"], M=64, seed=7, w_dtype=synth.NVFP4), table=True,
+               expect_regime=R.GBR_REGIME_GEMV1C)
     check_case(synth.make_case(dict(C["C2"], H=1056), M=4, seed=2, w_dtype=synth.NVFP4),
                expect_regime=R.GBR_REGIME_GENERIC)
 

@@ -163,7 +163,8 @@ def encode_exact(Z):
 
 @pytest.mark.parametrize("M,flags,regimes", [
     (8, 0, (R.GBR_REGIME_GEMV1C, R.GBR_REGIME_GEMV)),
-    (40, 0, (R.GBR_REGIME_GEMV,)),
+    (40, 0, (R.GBR_REGIME_GEMV1C,)),
+    (40, R.GBR_FLAG_NO_SINGLE_CLUSTER, (R.GBR_REGIME_GEMV,)),
     (130, 0, (R.GBR_REGIME_TC,)),
 ])
 def test_fused_cross_input_near_ties(M, flags, regimes):

@@ -45,7 +45,9 @@ def test_decode_single_cluster(M):
 
 
 def test_decode_split_clusters_and_table():
-    check_case(sig_case("C2", 40, seed=3), expect_regime=R.GBR_REGIME_GEMV)
+    check_case(sig_case("C2", 40, seed=3), expect_regime=R.GBR_REGIME_GEMV1C)
+    check_case(sig_case("C2", 40, seed=3), flags=R.GBR_FLAG_NO_SINGLE_CLUSTER,
+               expect_regime=R.GBR_REGIME_GEMV)
     check_case(sig_case("C4", 2, seed=4), table=True)
 
 

@@ -73,7 +73,9 @@ def test_decode_every_small_M_kernel(M):
 
 
 def test_split_clusters_table_and_nvfp4():
-    check_case(sm_case("C2", 40, seed=4), expect_regime=R.GBR_REGIME_GEMV)
+    check_case(sm_case("C2", 40, seed=4), expect_regime=R.GBR_REGIME_GEMV1C)
+    check_case(sm_case("C2", 40, seed=4), flags=R.GBR_FLAG_NO_SINGLE_CLUSTER,
+               expect_regime=R.GBR_REGIME_GEMV)
     check_case(sm_case("C4", 2, seed=5), table=True)
     cfg = dict(C["C2"], act=SM, bias=True)
     check_case(synth.make_case(cfg, M=8, seed=6, w_dtype=synth.NVFP4),
