@@ -289,9 +289,7 @@ __device__ __forceinline__ RouterArgs row_group(RouterArgs a, int rg) {
 // sees W / g exactly (a byte -> two-BF16 table, one exact BF16 multiply by
 // the block scale) and g multiplies the FP32 sums.
 template <int NT, int VPL, bool FP4, bool PREDEC>
-__global__ void __launch_bounds__(k1cWarps * 32)
-    k_gemv1c_router(const RouterArgs a_all, int pitch, int fpitch) {
-  const RouterArgs a = row_group(a_all, (int)blockIdx.y);
+__device__ __forceinline__ void gemv1c_body(const RouterArgs& a, int pitch, int fpitch) {
   constexpr int NTOK = 8 * NT;
   constexpr bool kFrag4 = FP4 && !PREDEC;  // NVFP4 fragments decoded in the MMA loop
   // BF16 rows [16][pitch] (BF16 weights, or NVFP4 decoded there); NVFP4:
@@ -500,6 +498,23 @@ __global__ void __launch_bounds__(k1cWarps * 32)
     }
   }
 }
+
+// One cluster (M <= 16): the body reads the launch parameters in place.
+template <int NT, int VPL, bool FP4, bool PREDEC>
+__global__ void __launch_bounds__(k1cWarps * 32)
+    k_gemv1c_router(const RouterArgs a, int pitch, int fpitch) {
+  gemv1c_body<NT, VPL, FP4, PREDEC>(a, pitch, fpitch);
+}
+
+// A cluster per 16 rows (16 < M <= 64): each cluster takes its row group's
+// sub-problem (a copy of the parameters with its rows' pointers).
+template <int NT, int VPL, bool FP4, bool PREDEC>
+__global__ void __launch_bounds__(k1cWarps * 32)
+    k_gemv1c_router_rows(const RouterArgs a, int pitch, int fpitch) {
+  const RouterArgs g = row_group(a, (int)blockIdx.y);
+  gemv1c_body<NT, VPL, FP4, PREDEC>(g, pitch, fpitch);
+}
+
 
 // ---------------------------------------------------------------------------
 // Split-cluster small-M router (M <= 64; used where the single-cluster
@@ -841,6 +856,9 @@ template <int NT, int VPL, bool FP4, bool PREDEC>
 cudaError_t launch_1c_inst(const RouterArgs& a, bool pdl, cudaStream_t stream, bool probe,
                            bool* fits) {
   auto kern = k_gemv1c_router<NT, VPL, FP4, PREDEC>;
+  if constexpr (NT == 2) {  // above 16 rows (only with two token tiles)
+    if (a.M > k1cRows) kern = k_gemv1c_router_rows<NT, VPL, FP4, PREDEC>;
+  }
   const int CL = a.E / 16;
   const size_t dsmem = gemv1c_smem(a.H, FP4, PREDEC);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
