@@ -36,7 +36,7 @@ LAYERS = 40          # router calls per decode token (one per MoE layer)
 # decode workload, valid only for the sources that kernel is built from: its
 # file (kernel and launcher) and the headers that file includes.
 DECODE_SOURCES = ("gemv.cu", "kernels.h", "select.cuh", "dfkey.cuh", "common.cuh")
-TRAFFIC = {"decode": {"bytes": 1160192, "src_sha": "a2807d03aaa15a5a"}}
+TRAFFIC = {"decode": {"bytes": 1159424, "src_sha": "c305d944da2c40d1"}}
 
 
 def kernel_src_sha(files=DECODE_SOURCES):
@@ -637,7 +637,10 @@ def run_phase_stamps(args):
     st, sel, refines = R.phase_stamps(with_refines=True)
     st, sel = st.astype(np.int64), sel.astype(np.int64)
     n = reps * LAYERS
-    own = [c for c in range(16) if c < M]  # CTAs that select a row (no table)
+    # the measurement build stamps the first row group's cluster (4 rows up
+    # to M=24, 8 up to M=32, else 16); its CTAs c < rows select a row each
+    rows = min(M, 4 if M <= 24 else 8 if M <= 32 else 16)
+    own = [c for c in range(16) if c < rows]
     ph = {k: [] for k in ("prev_end_to_wait_return", "wait_return_to_w_ready",
                           "w_ready_to_partials", "partials_to_sent", "sent_to_rows_landed",
                           "rows_landed_to_selected", "wait_return_to_last_selected",
@@ -664,7 +667,8 @@ def run_phase_stamps(args):
     act = {synth.SOFTMAX: "softmax", synth.SQRT_SOFTPLUS: "sqrt-softplus + bias",
            synth.SIGMOID: "sigmoid + bias"}[cfg["act"]]
     print(json.dumps({"workload": f"single-cluster router M={M}, H={cfg['H']}, E={cfg['E']}, "
-                                  f"k={cfg['k']}, {act}, 40-call graph",
+                                  f"k={cfg['k']}, {act}, 40-call graph, first row group "
+                                  f"({rows} rows)",
                       "calls": n - 1, "median_ns": res, "selection_ns": res_sel,
                       "rows_selected": n * M, "rows_reranked": refines[0],
                       "rows_fp64": refines[1]}))

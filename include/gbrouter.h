@@ -93,7 +93,7 @@ enum {
   GBR_REGIME_GEMV = 1,    /* M <= 64: clusters split H, last cluster selects */
   GBR_REGIME_TC = 2,      /* M > 64: tcgen05 GEMM with the selection in its epilogue */
   GBR_REGIME_UNFUSED = 3, /* logits kernel + router_select (A/B baseline) */
-  GBR_REGIME_GEMV1C = 4   /* M <= 64, E <= 256: a cluster per 16 rows holds W_gate in shared memory */
+  GBR_REGIME_GEMV1C = 4   /* M <= 64, E <= 256: a cluster per 4, 8 or 16 rows holds W_gate in shared memory */
 };
 
 typedef struct {

@@ -68,8 +68,8 @@ __device__ __forceinline__ void atom_exch_relaxed_gpu(uint32_t* p, uint32_t v) {
 }
 
 // ---------------------------------------------------------------------------
-// Single-cluster small-M router (M <= 64, E <= 256; one cluster per 16
-// rows, each routing its rows on its own). One cluster of E/16
+// Single-cluster small-M router (M <= 64, E <= 256; one cluster per group
+// of 4, 8 or 16 rows, each routing its rows on its own). One cluster of E/16
 // CTAs holds all of W_gate in shared memory: CTA r owns experts
 // [16r, 16r+16) over the whole H, so there are no partial sums to combine
 // and no logits leave the cluster. Each CTA starts bulk copies of its 16 W
@@ -86,8 +86,9 @@ __device__ __forceinline__ void atom_exch_relaxed_gpu(uint32_t* p, uint32_t v) {
 
 #ifdef GBR_PHASE_STAMPS
 // Measurement build only: %globaltimer stamps (ns) that thread 0 of each
-// CTA of the single-cluster kernel takes at phase boundaries, kept for the
-// last kStampCalls launches (slot = launch count of that CTA rank):
+// CTA of the single-cluster kernel's first row group takes at phase
+// boundaries, kept for the last kStampCalls launches (slot = launch count of
+// that CTA rank):
 //   0 entry, 1 W copies issued and dependents released, 2 wait on the
 //   preceding kernel returned, 3 W in shared memory, 4 warps' partials
 //   stored, 5 logits sent, 6 (selecting CTAs) this CTA's rows landed,
@@ -113,7 +114,7 @@ __device__ unsigned g_split_seq[kSplitStampCtas];
   } while (0)
 #define GBR_STAMP(slot, i)                                                  \
   do {                                                                      \
-    if (threadIdx.x == 0) {                                                 \
+    if (threadIdx.x == 0 && blockIdx.y == 0) {                              \
       unsigned long long t_;                                                \
       asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_)::"memory");      \
       g_stamps[slot][blockIdx.x][i] = t_;                                   \
@@ -259,14 +260,15 @@ struct RowOwner {
   }
 };
 
-// Row groups: above 16 rows the single-cluster kernel runs one cluster per
-// 16 rows (blockIdx.y), each a complete router for its rows that stages all
-// of W itself; this is the sub-problem of group rg.
-constexpr int k1cRows = 16;
-__device__ __forceinline__ RouterArgs row_group(RouterArgs a, int rg) {
-  if (rg == 0 && a.M <= k1cRows) return a;
-  const int m0 = k1cRows * rg;
-  a.M = min(k1cRows, a.M - m0);
+// Row groups: the single-cluster kernel runs one cluster per group of rows
+// (blockIdx.y), each a complete router for its rows that stages all of W
+// itself; this is the sub-problem of group rg (rows a multiple of 2, so a
+// table's row pairs stay in one group).
+constexpr int k1cMaxM = 64;
+__device__ __forceinline__ RouterArgs row_group(RouterArgs a, int rg, int rows) {
+  if (rg == 0 && a.M <= rows) return a;
+  const int m0 = rows * rg;
+  a.M = min(rows, a.M - m0);
   a.x = static_cast<const uint16_t*>(a.x) + (size_t)m0 * a.H;
   a.out_idx += (size_t)m0 * a.k;
   a.out_w += (size_t)m0 * a.k;
@@ -315,8 +317,9 @@ __device__ __forceinline__ void gemv1c_body(const RouterArgs& a, int pitch, int 
   const uint32_t bar = smem_u32(&s_bar), join = smem_u32(&s_join);
   const uint32_t wsm = smem_u32(s_w);
 #ifdef GBR_PHASE_STAMPS
-  const int stamp =
-      threadIdx.x == 0 ? (int)(atomicAdd(&g_stamp_seq[blockIdx.x], 1u) % kStampCalls) : 0;
+  const int stamp = threadIdx.x == 0 && blockIdx.y == 0
+                        ? (int)(atomicAdd(&g_stamp_seq[blockIdx.x], 1u) % kStampCalls)
+                        : 0;
 #endif
   GBR_STAMP(stamp, 0);
 
@@ -499,19 +502,19 @@ __device__ __forceinline__ void gemv1c_body(const RouterArgs& a, int pitch, int 
   }
 }
 
-// One cluster (M <= 16): the body reads the launch parameters in place.
+// One cluster (one row group): the body reads the launch parameters in place.
 template <int NT, int VPL, bool FP4, bool PREDEC>
 __global__ void __launch_bounds__(k1cWarps * 32)
     k_gemv1c_router(const RouterArgs a, int pitch, int fpitch) {
   gemv1c_body<NT, VPL, FP4, PREDEC>(a, pitch, fpitch);
 }
 
-// A cluster per 16 rows (16 < M <= 64): each cluster takes its row group's
+// A cluster per group of `rows` rows: each cluster takes its row group's
 // sub-problem (a copy of the parameters with its rows' pointers).
 template <int NT, int VPL, bool FP4, bool PREDEC>
 __global__ void __launch_bounds__(k1cWarps * 32)
-    k_gemv1c_router_rows(const RouterArgs a, int pitch, int fpitch) {
-  const RouterArgs g = row_group(a, (int)blockIdx.y);
+    k_gemv1c_router_rows(const RouterArgs a, int pitch, int fpitch, int rows) {
+  const RouterArgs g = row_group(a, (int)blockIdx.y, rows);
   gemv1c_body<NT, VPL, FP4, PREDEC>(g, pitch, fpitch);
 }
 
@@ -853,14 +856,13 @@ bool gemv1c_predec(int H) { return gemv1c_smem(H, true, true) <= k1cMaxDynSmem; 
 
 // Launches (or, with probe, only sizes) the single-cluster kernel.
 template <int NT, int VPL, bool FP4, bool PREDEC>
-cudaError_t launch_1c_inst(const RouterArgs& a, bool pdl, cudaStream_t stream, bool probe,
-                           bool* fits) {
-  auto kern = k_gemv1c_router<NT, VPL, FP4, PREDEC>;
-  if constexpr (NT == 2) {  // above 16 rows (only with two token tiles)
-    if (a.M > k1cRows) kern = k_gemv1c_router_rows<NT, VPL, FP4, PREDEC>;
-  }
+cudaError_t launch_1c_inst(const RouterArgs& a, int rows, bool pdl, cudaStream_t stream,
+                           bool probe, bool* fits) {
+  const bool grouped = a.M > rows;
   const int CL = a.E / 16;
   const size_t dsmem = gemv1c_smem(a.H, FP4, PREDEC);
+  const void* kern = grouped ? (const void*)k_gemv1c_router_rows<NT, VPL, FP4, PREDEC>
+                             : (const void*)k_gemv1c_router<NT, VPL, FP4, PREDEC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dsmem);
   if (e != cudaSuccess) return e;
@@ -869,7 +871,7 @@ cudaError_t launch_1c_inst(const RouterArgs& a, bool pdl, cudaStream_t stream, b
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL, (a.M + k1cRows - 1) / k1cRows);  // a cluster per 16 rows
+  cfg.gridDim = dim3(CL, (a.M + rows - 1) / rows);  // a cluster per row group
   cfg.blockDim = dim3(k1cWarps * 32);
   cfg.dynamicSmemBytes = dsmem;
   cfg.stream = stream;
@@ -888,30 +890,53 @@ cudaError_t launch_1c_inst(const RouterArgs& a, bool pdl, cudaStream_t stream, b
     *fits = (e == cudaSuccess && n > 0);
     return cudaSuccess;
   }
-  return cudaLaunchKernelEx(&cfg, kern, a, gemv1c_pitch(a.H), gemv1c_fpitch(a.H));
+  const int pitch = gemv1c_pitch(a.H), fpitch = gemv1c_fpitch(a.H);
+  if (grouped)
+    return cudaLaunchKernelEx(&cfg, k_gemv1c_router_rows<NT, VPL, FP4, PREDEC>, a, pitch, fpitch,
+                              rows);
+  return cudaLaunchKernelEx(&cfg, k_gemv1c_router<NT, VPL, FP4, PREDEC>, a, pitch, fpitch);
 }
 
 template <int NT, bool FP4, bool PREDEC>
-cudaError_t launch_1c_vpl(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe, bool* fits) {
-  if (a.E <= 128) return launch_1c_inst<NT, 4, FP4, PREDEC>(a, pdl, s, probe, fits);
-  return launch_1c_inst<NT, 8, FP4, PREDEC>(a, pdl, s, probe, fits);
+cudaError_t launch_1c_vpl(const RouterArgs& a, int rows, bool pdl, cudaStream_t s, bool probe,
+                          bool* fits) {
+  if (a.E <= 128) return launch_1c_inst<NT, 4, FP4, PREDEC>(a, rows, pdl, s, probe, fits);
+  return launch_1c_inst<NT, 8, FP4, PREDEC>(a, rows, pdl, s, probe, fits);
 }
 
 template <int NT>
-cudaError_t launch_1c_nt(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe, bool* fits) {
-  if (a.w_dtype != DT_NVFP4) return launch_1c_vpl<NT, false, false>(a, pdl, s, probe, fits);
-  if (gemv1c_predec(a.H)) return launch_1c_vpl<NT, true, true>(a, pdl, s, probe, fits);
-  return launch_1c_vpl<NT, true, false>(a, pdl, s, probe, fits);
+cudaError_t launch_1c_nt(const RouterArgs& a, int rows, bool pdl, cudaStream_t s, bool probe,
+                         bool* fits) {
+  if (a.w_dtype != DT_NVFP4) return launch_1c_vpl<NT, false, false>(a, rows, pdl, s, probe, fits);
+  if (gemv1c_predec(a.H)) return launch_1c_vpl<NT, true, true>(a, rows, pdl, s, probe, fits);
+  return launch_1c_vpl<NT, true, false>(a, rows, pdl, s, probe, fits);
+}
+
+// Rows per cluster. Every CTA of a cluster reads all of its rows' x from L2
+// (about 0.1 TB/s per SM), so fewer rows per cluster shorten the dependent
+// chain, but a call of eight clusters (128 CTAs) took about twice as long as
+// one of four: BF16 takes four rows up to six clusters, then eight rows up
+// to four clusters, then sixteen. NVFP4 W, whose rows are decoded before
+// the wait, lost from four clusters on (the fewer calls fit the GPU at
+// once, the less time a call has to stage and decode W before its
+// predecessor ends): four rows up to two clusters, eight up to three, then
+// sixteen (all measured on GB300 at M = 1..64). Four and eight rows take one
+// token tile (NT = 1), sixteen two.
+int rows_per_cluster(int M, bool fp4) {
+  if (fp4) return M <= 8 ? 4 : M <= 24 ? 8 : 16;
+  return M <= 24 ? 4 : M <= 32 ? 8 : 16;
 }
 
 cudaError_t launch_1c(const RouterArgs& a, bool pdl, cudaStream_t s, bool probe, bool* fits) {
-  return a.M <= 8 ? launch_1c_nt<1>(a, pdl, s, probe, fits) : launch_1c_nt<2>(a, pdl, s, probe, fits);
+  const int rows = rows_per_cluster(a.M, a.w_dtype == DT_NVFP4);
+  return rows <= 8 ? launch_1c_nt<1>(a, rows, pdl, s, probe, fits)
+                   : launch_1c_nt<2>(a, rows, pdl, s, probe, fits);
 }
 
 }  // namespace
 
 bool gemv1c_eligible(int M, int H, int E, bool fp4) {
-  if (M < 1 || M > 4 * k1cRows || E % 16 != 0 || E < 16 || E > 256 || H % (fp4 ? 256 : 32) != 0)
+  if (M < 1 || M > k1cMaxM || E % 16 != 0 || E < 16 || E > 256 || H % (fp4 ? 256 : 32) != 0)
     return false;
   if (gemv1c_smem(H, fp4, fp4 && gemv1c_predec(H)) > k1cMaxDynSmem) return false;
   // the cluster must be schedulable with this much shared memory per CTA
@@ -919,7 +944,7 @@ bool gemv1c_eligible(int M, int H, int E, bool fp4) {
   static std::map<std::tuple<int, int, int, int>, bool> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  const auto key = std::make_tuple(dev, (M <= 8 ? 1 : 2) + (fp4 ? 2 : 0), E, H);  // one cluster's fit
+  const auto key = std::make_tuple(dev, 2 * rows_per_cluster(M, fp4) + (fp4 ? 1 : 0), E, H);  // one cluster's fit
   std::lock_guard<std::mutex> lk(mu);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;

@@ -28,7 +28,7 @@ int gemv_cluster_size(int H);
 cudaError_t launch_gemv(const RouterArgs& a, bool select, bool pdl, cudaStream_t stream);
 
 // Small-M single-cluster router (E <= 256, W_gate in shared memory): one
-// cluster per 16 rows, M <= 64.
+// cluster per group of 4, 8 or 16 rows (at most four clusters), M <= 64.
 bool gemv1c_eligible(int M, int H, int E, bool fp4);
 cudaError_t launch_gemv1c(const RouterArgs& a, bool pdl, cudaStream_t stream);
 

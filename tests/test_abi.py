@@ -123,7 +123,7 @@ def test_route_table_argument_errors():
 def test_regime_choice():
     # the single-cluster kernel is chosen only where a device can schedule it
     assert R.router_regime(8, 2048, 256, 8) in (R.GBR_REGIME_GEMV, R.GBR_REGIME_GEMV1C)
-    # a cluster per 16 rows where the device can hold one, else split clusters
+    # a cluster per row group where the device can hold one, else split clusters
     assert R.router_regime(64, 4096, 256, 6) in (R.GBR_REGIME_GEMV, R.GBR_REGIME_GEMV1C)
     f32 = R.make_opts(x_dtype=R.GBR_F32, w_dtype=R.GBR_F32)
     assert R.router_regime(4, 256, 16, 2, f32) == R.GBR_REGIME_GENERIC

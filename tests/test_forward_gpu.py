@@ -107,12 +107,12 @@ def test_decode_softmax(M, dup):
 @pytest.mark.parametrize("M", [1, 16, 64])
 def test_sqrt_softplus_bias(M):
     case = synth.make_case(C["C2"], M=M, seed=10 + M, dup_frac=0.1)
-    # above 16 rows: one cluster per 16 rows
+    # one cluster per 4 (M <= 16), 8 (M <= 32) or 16 rows
     check_case(case, expect_regime=R.GBR_REGIME_GEMV1C)
     check_case(case, flags=R.GBR_FLAG_NO_SINGLE_CLUSTER, expect_regime=R.GBR_REGIME_GEMV)
 
 
-@pytest.mark.parametrize("M", [3, 5, 9, 13, 16, 17, 37, 63])
+@pytest.mark.parametrize("M", [3, 5, 7, 9, 13, 16, 17, 25, 31, 33, 37, 63])
 def test_ragged_M(M):
     check_case(synth.make_case(C["C2"], M=M, seed=M))
     check_case(synth.make_case(C["C1"], M=M, seed=M), flags=R.GBR_FLAG_NO_SINGLE_CLUSTER)
@@ -129,7 +129,7 @@ def test_m2_route_table_fused():
         check_case(case, table=True, expect_regime=R.GBR_REGIME_GEMV1C)
         check_case(case, table=True, flags=R.GBR_FLAG_NO_SINGLE_CLUSTER)
         check_case(case, table=True, flags=R.GBR_FLAG_FORCE_GENERIC)
-    for M in (4, 8, 16, 64):
+    for M in (4, 6, 8, 10, 16, 18, 26, 64):  # row pairs across 4-, 8- and 16-row groups
         check_case(synth.make_case(cfg, M=M, seed=M), table=True)
         check_case(synth.make_case(cfg, M=M, seed=M), table=True,
                    flags=R.GBR_FLAG_NO_SINGLE_CLUSTER)
@@ -181,7 +181,7 @@ def test_single_cluster_hidden_limits(H):
     check_case(synth.make_case(cfg, M=4, seed=H))
 
 
-@pytest.mark.parametrize("M", [1, 2, 8, 16])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 16, 20])
 def test_nvfp4_weights_small_M(M):
     case = synth.make_case(C["C2"], M=M, seed=4 + M, w_dtype=synth.NVFP4)
     check_case(case, expect_regime=R.GBR_REGIME_GEMV1C)
@@ -192,7 +192,7 @@ def test_nvfp4_weights_small_M(M):
 
 
 def test_nvfp4_small_M_other_paths():
-    # 16 < M <= 64: a cluster per 16 rows (the last one ragged); H not a
+    # 32 < M <= 64: a cluster per 16 rows (the last one ragged); H not a
     # multiple of 256 takes the generic kernel
     check_case(synth.make_case(C["C2"], M=33, seed=1, w_dtype=synth.NVFP4),
                expect_regime=R.GBR_REGIME_GEMV1C)
