@@ -165,6 +165,71 @@ __global__ void __launch_bounds__(kLaneWarps * 32)
   if (lane < ng) count[g0 + lane] = __popc(F);
 }
 
+// Groups of N = T*k entries, N a multiple of 4 up to 16, with 16-byte
+// aligned ids and 4-byte aligned masks and maps: one lane per group reads
+// the group's ids with 16-byte loads straight into registers, finds each
+// entry's first occurrence there, and scatters the unique ids and token
+// masks into its own shared-memory row (written and read back by the same
+// thread, so no barrier), from which it stores its table rows with 16-byte
+// (ids) and 4-byte (masks, map) stores.
+template <int N>
+__global__ void __launch_bounds__(kLaneWarps * 32)
+    k_route_table_vec(const int32_t* __restrict__ idx, int G, int k,
+                      int32_t* __restrict__ unique, uint8_t* __restrict__ mask,
+                      uint8_t* __restrict__ map, int32_t* __restrict__ count) {
+  __shared__ __align__(16) int32_t s_un[kLaneWarps * 32][N];
+  __shared__ __align__(4) uint8_t s_mk[kLaneWarps * 32][N];
+  const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= G) return;
+  int32_t v[N];
+  const int4* src = reinterpret_cast<const int4*>(idx + g * N);
+#pragma unroll
+  for (int c = 0; c < N / 4; ++c) {
+    const int4 q = __ldg(src + c);
+    v[4 * c] = q.x, v[4 * c + 1] = q.y, v[4 * c + 2] = q.z, v[4 * c + 3] = q.w;
+  }
+  int32_t* un = s_un[threadIdx.x];
+  uint8_t* mk = s_mk[threadIdx.x];
+#pragma unroll
+  for (int c = 0; c < N / 4; ++c) {
+    reinterpret_cast<int4*>(un)[c] = make_int4(-1, -1, -1, -1);
+    reinterpret_cast<uint32_t*>(mk)[c] = 0u;
+  }
+  // first occurrence of each entry's id, and the set of first occurrences
+  int fp[N];
+  uint32_t F = 0u;
+#pragma unroll
+  for (int p = 0; p < N; ++p) {
+    int f = p;
+#pragma unroll
+    for (int q = p - 1; q >= 0; --q) f = (v[q] == v[p]) ? q : f;
+    fp[p] = f;
+    F |= (f == p ? 1u : 0u) << p;
+  }
+  uint32_t mp[N / 4];
+#pragma unroll
+  for (int c = 0; c < N / 4; ++c) mp[c] = 0u;
+  int tok = 0, rem = 0;  // token of entry p = p / k
+#pragma unroll
+  for (int p = 0; p < N; ++p) {
+    const int u = __popc(F & ((1u << fp[p]) - 1u));  // unique position of the id
+    mp[p / 4] |= (uint32_t)u << (8 * (p % 4));
+    if (fp[p] == p) un[u] = v[p];
+    mk[u] = (uint8_t)(mk[u] | (1u << tok));
+    if (++rem == k) rem = 0, ++tok;
+  }
+  int4* du = reinterpret_cast<int4*>(unique + g * N);
+  uint32_t* dk = reinterpret_cast<uint32_t*>(mask + g * N);
+  uint32_t* dm = reinterpret_cast<uint32_t*>(map + g * N);
+#pragma unroll
+  for (int c = 0; c < N / 4; ++c) {
+    du[c] = reinterpret_cast<const int4*>(un)[c];
+    dk[c] = reinterpret_cast<const uint32_t*>(mk)[c];
+    dm[c] = mp[c];
+  }
+  count[g] = __popc(F);
+}
+
 __global__ void k_near_tie_keys(const float* __restrict__ z, const float* __restrict__ bias, int n,
                                 int act, float* __restrict__ hi, float* __restrict__ lo) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
@@ -197,7 +262,19 @@ cudaError_t launch_select(const float* logits, const float* bias, int M, int E, 
 cudaError_t launch_route_table(const int32_t* idx, int groups, int T, int k, int32_t* unique,
                                uint8_t* mask, uint8_t* map, int32_t* count, cudaStream_t stream) {
   const dim3 block(kTblWarps * 32);
-  if (T * k <= kLaneMax) {
+  const int n = T * k;
+  const bool vec = n % 4 == 0 && n <= 16 && ((uintptr_t)idx | (uintptr_t)unique) % 16 == 0 &&
+                   ((uintptr_t)mask | (uintptr_t)map) % 4 == 0;
+  if (vec) {
+    const dim3 grid((unsigned)(((long long)groups + kLaneWarps * 32 - 1) / (kLaneWarps * 32)));
+    const dim3 lb(kLaneWarps * 32);
+    switch (n) {
+      case 4: k_route_table_vec<4><<<grid, lb, 0, stream>>>(idx, groups, k, unique, mask, map, count); break;
+      case 8: k_route_table_vec<8><<<grid, lb, 0, stream>>>(idx, groups, k, unique, mask, map, count); break;
+      case 12: k_route_table_vec<12><<<grid, lb, 0, stream>>>(idx, groups, k, unique, mask, map, count); break;
+      default: k_route_table_vec<16><<<grid, lb, 0, stream>>>(idx, groups, k, unique, mask, map, count); break;
+    }
+  } else if (T * k <= kLaneMax) {
     const long long warps = (groups + 31) / 32;
     const dim3 grid((unsigned)((warps + kLaneWarps - 1) / kLaneWarps));
     k_route_table_lane<<<grid, dim3(kLaneWarps * 32), 0, stream>>>(idx, groups, T, k, unique, mask,

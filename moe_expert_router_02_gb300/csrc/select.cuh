@@ -79,14 +79,29 @@ __device__ __forceinline__ void cas_desc(uint64_t& a, uint64_t& b) {
   b = lo;
 }
 
-// Sorts VPL packed values descending in registers (odd-even transposition;
-// fully unrolled, so every index is static).
+// Sorts VPL packed values descending in registers, fully unrolled so that
+// every index is static: 4 and 8 values by the minimal comparator networks
+// (5 comparators in 3 layers; 19 in 6 layers, Knuth TAOCP vol. 3,
+// sec. 5.3.4), any other count by odd-even transposition.
 template <int VPL>
 __device__ __forceinline__ void sort_desc(uint64_t (&v)[VPL]) {
+  if constexpr (VPL == 8) {
+    cas_desc(v[0], v[2]), cas_desc(v[1], v[3]), cas_desc(v[4], v[6]), cas_desc(v[5], v[7]);
+    cas_desc(v[0], v[4]), cas_desc(v[1], v[5]), cas_desc(v[2], v[6]), cas_desc(v[3], v[7]);
+    cas_desc(v[0], v[1]), cas_desc(v[2], v[3]), cas_desc(v[4], v[5]), cas_desc(v[6], v[7]);
+    cas_desc(v[2], v[4]), cas_desc(v[3], v[5]);
+    cas_desc(v[1], v[4]), cas_desc(v[3], v[6]);
+    cas_desc(v[1], v[2]), cas_desc(v[3], v[4]), cas_desc(v[5], v[6]);
+  } else if constexpr (VPL == 4) {
+    cas_desc(v[0], v[1]), cas_desc(v[2], v[3]);
+    cas_desc(v[0], v[2]), cas_desc(v[1], v[3]);
+    cas_desc(v[1], v[2]);
+  } else {
 #pragma unroll
-  for (int pass = 0; pass < VPL; ++pass) {
+    for (int pass = 0; pass < VPL; ++pass) {
 #pragma unroll
-    for (int j = pass & 1; j + 1 < VPL; j += 2) cas_desc(v[j], v[j + 1]);
+      for (int j = pass & 1; j + 1 < VPL; j += 2) cas_desc(v[j], v[j + 1]);
+    }
   }
 }
 

@@ -50,7 +50,8 @@ def test_1e5_seeded_pairs():
     assert_table_equal(synth.table_pairs(100000, 6, 256, seed=0))
 
 
-@pytest.mark.parametrize("T,k", [(2, 6), (1, 1), (1, 16), (4, 3), (8, 16), (3, 5), (2, 16)])
+@pytest.mark.parametrize("T,k", [(2, 6), (1, 1), (1, 16), (4, 3), (8, 16), (3, 5), (2, 16),
+                                 (2, 2), (2, 4), (4, 2), (8, 2), (1, 4), (4, 4), (8, 1), (1, 12)])
 def test_duplicates_and_group_sizes(T, k):
     gen = synth.rng(T * 100 + k)
     assert_table_equal(gen.integers(0, 5, size=(333, T, k)).astype(np.int32))
@@ -63,6 +64,31 @@ def test_ragged_group_counts(T, k, G):
     # counts that leave the last warp's groups partly empty
     gen = synth.rng(G * 7 + T + k)
     assert_table_equal(gen.integers(0, 9, size=(G, T, k)).astype(np.int32))
+
+
+@pytest.mark.parametrize("T,k", [(2, 6), (2, 8), (4, 1)])
+def test_unaligned_buffers(T, k):
+    """Group sizes that take 16-byte loads and stores (T*k a multiple of 4)
+    on buffers offset by one element: the same table through the general
+    kernel."""
+    import torch
+    G = 77
+    n = T * k
+    host = synth.rng(T + 10 * k).integers(0, 7, size=(G, T, k)).astype(np.int32)
+    src = torch.zeros(G * n + 1, dtype=torch.int32, device="cuda")
+    src[1:] = dev(host.reshape(-1))
+    un = torch.full((G * n + 1,), -9, dtype=torch.int32, device="cuda")
+    mk = torch.full((G * n + 1,), 0xEE, dtype=torch.uint8, device="cuda")
+    mp = torch.full((G * n + 1,), 0xEE, dtype=torch.uint8, device="cuda")
+    cnt = torch.full((G,), -9, dtype=torch.int32, device="cuda")
+    R.route_table(src[1:], G, T, k, un[1:], mk[1:], mp[1:], cnt)
+    torch.cuda.synchronize()
+    ref = oracle.route_table(host)
+    got = (un[1:].cpu().numpy().reshape(G, n), mk[1:].cpu().numpy().reshape(G, n),
+           mp[1:].cpu().numpy().reshape(G, T, k), cnt.cpu().numpy())
+    for name, g, r in zip(("unique", "mask", "map", "count"), got, ref):
+        assert np.array_equal(g, r), name
+    assert int(un[0]) == -9 and int(mk[0]) == 0xEE and int(mp[0]) == 0xEE
 
 
 def test_graph_replay_with_changing_inputs():
