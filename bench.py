@@ -36,7 +36,7 @@ LAYERS = 40          # router calls per decode token (one per MoE layer)
 # decode workload, valid only for the sources that kernel is built from: its
 # file (kernel and launcher) and the headers that file includes.
 DECODE_SOURCES = ("gemv.cu", "kernels.h", "select.cuh", "dfkey.cuh", "common.cuh")
-TRAFFIC = {"decode": {"bytes": 1158144, "src_sha": "cab06bd03d6b9e5e"}}
+TRAFFIC = {"decode": {"bytes": 1156693, "src_sha": "b0cadfb85b80161a"}}
 
 
 def kernel_src_sha(files=DECODE_SOURCES):
@@ -687,7 +687,7 @@ def run_phase_stamps(args):
                                   f"({rows} rows)",
                       "calls": n - 1, "median_ns": res, "selection_ns": res_sel,
                       "rows_selected": n * M, "rows_reranked": refines[0],
-                      "rows_fp64": refines[1]}))
+                      "rows_fp64": refines[1], "rows_pair_rounds": refines[2]}))
 
 
 def run_phase_stamps_split(args):

@@ -983,11 +983,12 @@ extern "C" int router_phase_stamps(unsigned long long* host, int* calls, int* ct
                            sizeof(g_sel_stamps)) != cudaSuccess)
     return 3;
   // then the re-rank counts since the last call (rows re-ranked, rows
-  // taken to FP64), which restart from zero
+  // taken to FP64, rows whose 32-bit rounds ran again on (key, index)
+  // pairs), which restart from zero
   if (cudaMemcpyFromSymbol(host + kStampCalls * 16 * kStampPhases + 16 * 5, g_sel_refines,
                            sizeof(g_sel_refines)) != cudaSuccess)
     return 3;
-  static const unsigned long long zr[2] = {};
+  static const unsigned long long zr[3] = {};
   if (cudaMemcpyToSymbol(g_sel_refines, zr, sizeof(zr)) != cudaSuccess) return 3;
   static const unsigned zero[16] = {};
   return cudaMemcpyToSymbol(g_stamp_seq, zero, sizeof(zero)) == cudaSuccess ? 0 : 3;

@@ -44,9 +44,11 @@ namespace gbr {
 // selection of each CTA rank wins.
 namespace {
 __device__ unsigned long long g_sel_stamps[16][5];
-// rows whose selection took the near-tie re-rank, and of those the rows
-// that went on to FP64 keys (warp selections of this translation unit)
-__device__ unsigned long long g_sel_refines[2];
+// rows whose selection took the near-tie re-rank, of those the rows that
+// went on to FP64 keys, and rows whose 32-bit rounds met equal truncated
+// keys and ran again on (key, index) pairs (warp selections of this
+// translation unit)
+__device__ unsigned long long g_sel_refines[3];
 }
 #define SEL_STAMP(i)                                                           \
   do {                                                                         \
@@ -101,6 +103,35 @@ __device__ __forceinline__ void sort_desc(uint64_t (&v)[VPL]) {
     for (int pass = 0; pass < VPL; ++pass) {
 #pragma unroll
       for (int j = pass & 1; j + 1 < VPL; j += 2) cas_desc(v[j], v[j + 1]);
+    }
+  }
+}
+
+// The same networks on 32-bit values (one max and one min per comparator).
+__device__ __forceinline__ void cas_desc32(uint32_t& a, uint32_t& b) {
+  const uint32_t hi = max(a, b), lo = min(a, b);
+  a = hi;
+  b = lo;
+}
+
+template <int VPL>
+__device__ __forceinline__ void sort_desc32(uint32_t (&v)[VPL]) {
+  if constexpr (VPL == 8) {
+    cas_desc32(v[0], v[2]), cas_desc32(v[1], v[3]), cas_desc32(v[4], v[6]), cas_desc32(v[5], v[7]);
+    cas_desc32(v[0], v[4]), cas_desc32(v[1], v[5]), cas_desc32(v[2], v[6]), cas_desc32(v[3], v[7]);
+    cas_desc32(v[0], v[1]), cas_desc32(v[2], v[3]), cas_desc32(v[4], v[5]), cas_desc32(v[6], v[7]);
+    cas_desc32(v[2], v[4]), cas_desc32(v[3], v[5]);
+    cas_desc32(v[1], v[4]), cas_desc32(v[3], v[6]);
+    cas_desc32(v[1], v[2]), cas_desc32(v[3], v[4]), cas_desc32(v[5], v[6]);
+  } else if constexpr (VPL == 4) {
+    cas_desc32(v[0], v[1]), cas_desc32(v[2], v[3]);
+    cas_desc32(v[0], v[2]), cas_desc32(v[1], v[3]);
+    cas_desc32(v[1], v[2]);
+  } else {
+#pragma unroll
+    for (int pass = 0; pass < VPL; ++pass) {
+#pragma unroll
+      for (int j = pass & 1; j + 1 < VPL; j += 2) cas_desc32(v[j], v[j + 1]);
     }
   }
 }
@@ -406,27 +437,76 @@ __device__ __noinline__ void warp_select_row_act(const Ld ld, const float* __res
     }
   }
   SEL_STAMP(0);
-  sort_desc<VPL>(pk);
-  SEL_STAMP(1);
-
   // k+1 rounds for the biased scores: the (k+1)-th key is kept for the gap
   // test; softmax has none and stops at k.
   const int kk = act == ACT_SOFTMAX ? k : min(k + 1, E);
   int sel_idx = -1;
   float sel_key = 0.0f;
-  for (int r = 0; r < kk; ++r) {
-    const uint32_t bo = (uint32_t)(pk[0] >> 32);
-    const uint32_t wbest = __reduce_max_sync(kFull, bo);
-    const uint32_t cand = (bo == wbest) ? 0xffffffffu - (uint32_t)pk[0] : 0xffffffffu;
-    const uint32_t widx = __reduce_min_sync(kFull, cand);  // lowest index among equal keys
-    if (lane == r) {
-      sel_idx = (int)widx;
-      sel_key = float_of_ord(wbest);
-    }
-    if ((int)(widx & 31u) == lane) {
+  bool exact = true;
+  if constexpr (VPL <= 8 && act == ACT_SOFTMAX) {
+    // Softmax, E <= 256: rounds over one 32-bit word per entry, the key's
+    // top 24 bits and 255 - index in the low 8 (a larger word: a larger
+    // truncated key, or the same one and a lower index), so a round is one
+    // warp maximum. (The biased scores measured slower this way.)
+    // Truncation keeps order (t(a) > t(b) implies a > b), so when the kk
+    // words picked and the best word left have strictly decreasing
+    // truncated keys, the kk picked are the top kk of the exact keys in
+    // exact order; otherwise the rounds below on (key, index) pairs decide.
+    uint32_t c[VPL];
 #pragma unroll
-      for (int j = 0; j + 1 < VPL; ++j) pk[j] = pk[j + 1];
-      pk[VPL - 1] = 0ull;
+    for (int j = 0; j < VPL; ++j)
+      c[j] = pk[j] ? (((uint32_t)(pk[j] >> 32) & 0xffffff00u) | (255u - (uint32_t)(lane + 32 * j)))
+                   : 0u;
+    sort_desc32<VPL>(c);
+    SEL_STAMP(1);
+    uint32_t mine = 0u;  // lane r <= kk: the word of round r
+    for (int r = 0; r <= kk; ++r) {
+      const uint32_t wbest = __reduce_max_sync(kFull, c[0]);
+      mine = lane == r ? wbest : mine;
+      const bool win = (int)(wbest & 31u) == (31 - lane);  // (255 - e) & 31 = 31 - e % 32
+#pragma unroll
+      for (int j = 0; j + 1 < VPL; ++j) c[j] = win ? c[j + 1] : c[j];
+      c[VPL - 1] = win ? 0u : c[VPL - 1];
+    }
+    const uint32_t after = __shfl_down_sync(kFull, mine, 1);
+    const bool tie = lane < kk && after != 0u && (mine >> 8) == (after >> 8);
+    exact = __any_sync(kFull, tie);
+#ifdef GBR_PHASE_STAMPS
+    if (exact && lane == 0) atomicAdd(&g_sel_refines[2], 1ull);
+#endif
+    if (!exact) {
+      // lane r < kk: its expert, and the exact key from the lane holding it
+      const int e = 255 - (int)(mine & 0xffu);
+      const int src = e & 31, js = lane < kk ? e >> 5 : -1;
+      uint32_t ko = 0u;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        const uint32_t v = __shfl_sync(kFull, (uint32_t)(pk[j] >> 32), src);
+        ko = j == js ? v : ko;
+      }
+      if (lane < kk) {
+        sel_idx = e;
+        sel_key = float_of_ord(ko);
+      }
+    }
+  }
+  if (exact) {
+    sort_desc<VPL>(pk);
+    SEL_STAMP(1);
+    for (int r = 0; r < kk; ++r) {
+      const uint32_t bo = (uint32_t)(pk[0] >> 32);
+      const uint32_t wbest = __reduce_max_sync(kFull, bo);
+      const uint32_t cand = (bo == wbest) ? 0xffffffffu - (uint32_t)pk[0] : 0xffffffffu;
+      const uint32_t widx = __reduce_min_sync(kFull, cand);  // lowest index among equal keys
+      if (lane == r) {
+        sel_idx = (int)widx;
+        sel_key = float_of_ord(wbest);
+      }
+      if ((int)(widx & 31u) == lane) {
+#pragma unroll
+        for (int j = 0; j + 1 < VPL; ++j) pk[j] = pk[j + 1];
+        pk[VPL - 1] = 0ull;
+      }
     }
   }
 

@@ -229,6 +229,21 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 
+// AND of a predicate over the kEpiWarps epilogue warps (named barrier 2,
+// used for nothing else).
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 2, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(kEpiWarps * 32)
+      : "memory");
+  return r != 0u;
+}
+
 __device__ __forceinline__ void cluster_sync_tc() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");
@@ -1028,6 +1043,9 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
           if (PAIR) mma_commit_pair(smem_u32(&empty[s]));
           else mma_commit(smem_u32(&empty[s]));
         }
+        // after a give-up the accumulator is incomplete: no commit, so the
+        // epilogue's wait for it gives up too instead of reading it
+        if (!go) break;
         const uint32_t done = smem_u32(plan.fin(sg) ? accf : accp);
         if (PAIR) mma_commit_pair(done);
         else mma_commit(done);
@@ -1276,7 +1294,10 @@ __global__ void __launch_bounds__((kEpiWarps + 2) * 32, 1)
     const bool ok = has_fin && mbar_wait_warp(wstat, smem_u32(accf), 0);
     TC_STAMP(3);
     tc_fence_after();
-    const bool all_ok = __all_sync(kFull, ok);
+    // one answer for all epilogue warps (the blocks it guards hold named
+    // barriers): a warp whose bounded wait gave up just before the
+    // accumulator landed must not leave its peers waiting at them
+    const bool all_ok = epi_all(ok);
     if (all_ok && nparts > 0) {
       const uint32_t pbytes = (uint32_t)E * BM * 4;
       for (int q = plan.p0 + pre; q <= grp; ++q) {

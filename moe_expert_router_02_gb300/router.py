@@ -247,19 +247,20 @@ def phase_stamps(with_refines=False):
     numpy array [calls, ctas, phases] of %globaltimer ns (0 = not stamped),
     and the last selection's sub-phase stamps per CTA rank [16, 5]; with
     with_refines, also the counts of warp selections (small-M kernels) that
-    re-ranked near ties and that went on to FP64 since the previous read."""
+    re-ranked near ties, that went on to FP64, and whose 32-bit rounds ran
+    again on (key, index) pairs since the previous read."""
     import numpy as np
     L = lib()
     c, t, p = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     L.router_phase_stamps(None, ctypes.byref(c), ctypes.byref(t), ctypes.byref(p))
     n = c.value * t.value * p.value
-    buf = np.zeros(n + 16 * 5 + 2, dtype=np.uint64)
+    buf = np.zeros(n + 16 * 5 + 3, dtype=np.uint64)
     if L.router_phase_stamps(buf.ctypes.data_as(ctypes.c_void_p), ctypes.byref(c), ctypes.byref(t),
                              ctypes.byref(p)) != 0:
         raise RuntimeError("router_phase_stamps failed")
     st, sel = buf[:n].reshape(c.value, t.value, p.value), buf[n:n + 80].reshape(16, 5)
     if with_refines:
-        return st, sel, (int(buf[n + 80]), int(buf[n + 81]))
+        return st, sel, (int(buf[n + 80]), int(buf[n + 81]), int(buf[n + 82]))
     return st, sel
 
 
