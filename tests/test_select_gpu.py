@@ -58,6 +58,28 @@ def test_all_boundary_tie_kinds_softmax(M):
         assert_exact(rows[s:s + M], 8, synth.SOFTMAX)
 
 
+@pytest.mark.parametrize("spacing", [1, 3, 255, 256, 257, 4096])
+@pytest.mark.parametrize("E,k", [(256, 8), (128, 6), (64, 4)])
+def test_softmax_keys_close_in_their_top_bits(spacing, E, k):
+    """The softmax selection ranks 32-bit words holding a key's top 24 bits
+    and falls back to (key, index) rounds when two of its picks, or its
+    last pick and the best word left, share those bits. Rows whose 2k
+    largest logits sit a multiple of `spacing` ulps apart (some equal,
+    spread over lanes and slots) take the fallback (spacing < 256), the
+    32-bit rounds alone (spacing >= 256, multiples that cross the
+    truncation step) or both; the ids equal the oracle's either way."""
+    gen = synth.rng(spacing * 7 + E + k)
+    M = 96
+    rows = gen.normal(0.0, 1.0, size=(M, E)).astype(np.float32)
+    n = 2 * k
+    for r in range(M):
+        cols = gen.choice(E, n, replace=False)
+        steps = np.cumsum(gen.integers(0, 3, size=n))  # some equal neighbours
+        base = np.array([4.0 + 0.5 * (r % 5)], dtype=np.float32).view(np.int32)[0]
+        rows[r, cols] = (base + steps * spacing).astype(np.int32).view(np.float32)
+    assert_exact(rows, k, synth.SOFTMAX)
+
+
 def test_sqrt_softplus_bias_boundary_ties():
     rows, bias, kinds = synth.tie_rows_sqrt_softplus(60, 256, 6, seed=3)
     for r in range(len(rows)):  # the bias differs per row: one call per row
